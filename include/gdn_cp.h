@@ -1,0 +1,237 @@
+/*
+ * gdn_cp.h -- C ABI of the context-parallel Gated DeltaNet forward for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (sources are two public web pages):
+ *   [FLA-CP] flash-linear-attention, fla/ops/cp/context.py: get_cp_cu_seqlens
+ *            and build_cp_context (the per-shard cu_seqlens plan).
+ *   [HP-CP]  hyper-parallel, linear_attention_context_parallel.py: the causal
+ *            conv1d + SiLU with the previous shard's halo
+ *            (_causal_conv1d_with_cp_halo), the chunked gated delta rule in
+ *            WY/UT form (_prepare_gdn_chunks_for_summary,
+ *            _run_prepared_gdn_chunks), the shard state summary
+ *            (_compute_gdn_state_summary_from_prepared) and its prefix merge
+ *            (_merge_gdn_prefix_state_summaries_torch).
+ *
+ * The gated delta rule, per sequence and value head, with S a [dk, dv] fp32
+ * state:   S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *          o_t = S_t^T (scale q_t)
+ * A long sequence may be cut into P contiguous "virtual shards" of one
+ * device's memory; each shard's state map S_out = M S_in + N is combined by
+ * a prefix scan so that the sharded result equals the unsharded one.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" must be CUDA device (or managed) memory; the
+ *     caller allocates and owns every buffer.  Except for the workspace of
+ *     gdn_shard_fwd, no entry point needs scratch memory, and none allocates.
+ *   - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL
+ *     = the legacy default stream).  No entry point synchronises the host.
+ *   - Tokens are packed, batch 1: a token-major [T, ...] layout with
+ *     sequence boundaries in cu_seqlens (int32, device, [num_seqs + 1],
+ *     cu_seqlens[0] = 0, non-decreasing, cu_seqlens[num_seqs] = T).
+ *     Empty sequences are allowed.
+ *   - Head layout: Hk query/key heads, Hv value heads, Hv % Hk == 0; value
+ *     head h reads query/key head h / (Hv / Hk) (repeat_interleave on the
+ *     head dimension, [HP-CP] the P2P wrapper's forward).
+ *   - Supported: dk, dv in {32, 64, 128}; conv kernel size 1..4; chunk 64.
+ *   - dtype GDN_BF16: q/k/v/x/beta/o/conv weights in bf16, arithmetic and
+ *     the state in fp32.  GDN_F32: everything fp32.  g is always fp32.
+ *   - Errors detectable on the host return a non-OK status before anything
+ *     is enqueued; gdn_last_error() then describes the first failing check.
+ *     Errors that depend on device data (a malformed cu_seqlens) are written
+ *     to a device status word (see gdn_cp_plan) and never trap.
+ */
+#ifndef GDN_CP_H
+#define GDN_CP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misaligned buffer */
+    GDN_ERR_UNSUPPORTED_SHAPE = 2, /* dk/dv/conv_k/channels outside the supported set */
+    GDN_ERR_DTYPE = 3,             /* unknown gdn_dtype */
+    GDN_ERR_NOT_DIVISIBLE = 4,     /* T % n_shards != 0 ([HP-CP] _slice_local_cp) */
+    GDN_ERR_SHARD_TOO_SHORT = 5,   /* T / n_shards < conv_k - 1 ([HP-CP] conv halo check) */
+    GDN_ERR_BAD_CU_SEQLENS = 6,    /* device status only: cu_seqlens malformed */
+    GDN_ERR_TIMEOUT = 7,           /* device status only: a bounded wait expired */
+    GDN_ERR_CUDA = 8,              /* a CUDA launch failed; see gdn_last_error() */
+    GDN_ERR_WORKSPACE = 9          /* workspace missing or smaller than required */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* flags for gdn_chunk_fwd / gdn_chunk_summary / gdn_shard_fwd */
+enum {
+    /* replace q and k by x * rsqrt(sum(x^2) + 1e-6) per head before use
+       ([HP-CP] _l2norm_torch, use_qk_l2norm_in_kernel) */
+    GDN_QK_L2NORM = 1u
+};
+
+/* Human-readable name of a status code (static string). */
+const char *gdn_status_string(gdn_status s);
+
+/* Thread-local description of the last non-OK status returned on this
+   thread ("" if none). */
+const char *gdn_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Shard plan  ([FLA-CP] get_cp_cu_seqlens, steps 1-5)
+ *
+ * For each shard r < n_shards (part = T / n_shards, rs = r * part,
+ * re = rs + part, cu = cu_seqlens):
+ *   s = #{i : cu[i+1] <= rs}            start_seq_idx (searchsorted right)
+ *   e = #{i < num_seqs : cu[i] < re}    end_seq_idx   (searchsorted left)
+ *   local_cu = dedupe(clamp(cu[s..e], rs, re) - rs)   (unique_consecutive)
+ *   pre_num_conv_tokens = max(0, rs - cu[s])
+ *   pre_num_ranks  = r - cu[s] / part;        is_first_rank = (pre == 0)
+ *   post_num_ranks = (cu[e] - 1) / part - r;  is_last_rank  = (post == 0)
+ *
+ * `plan` is a device int32 buffer of gdn_cp_plan_words(num_seqs, n_shards)
+ * words, laid out as:
+ *   plan[0]                                  status word (0 = OK, else a
+ *                                            gdn_status: BAD_CU_SEQLENS when
+ *                                            cu[0] != 0, cu decreases, or
+ *                                            cu[num_seqs] % n_shards != 0)
+ *   plan[GDN_PLAN_REC(r) + GDN_PLAN_*]       the fields below for shard r
+ *   plan[GDN_PLAN_CU(num_seqs, n_shards, r) + i], 0 <= i <= local_num_seqs
+ *                                            local cu_seqlens of shard r
+ * Needs 1 <= n_shards <= 65536 and num_seqs >= 1.  The whole plan is
+ * computed on the device: no device-to-host copy of cu_seqlens.
+ * ---------------------------------------------------------------------- */
+enum {
+    GDN_PLAN_LOCAL_NUM_SEQS = 0,
+    GDN_PLAN_START_SEQ_IDX = 1,
+    GDN_PLAN_END_SEQ_IDX = 2,
+    GDN_PLAN_PRE_NUM_RANKS = 3,
+    GDN_PLAN_POST_NUM_RANKS = 4,
+    GDN_PLAN_IS_FIRST_RANK = 5,
+    GDN_PLAN_IS_LAST_RANK = 6,
+    GDN_PLAN_PRE_NUM_CONV_TOKENS = 7,
+    GDN_PLAN_SEG_OFFSET = 8, /* sum of local_num_seqs over shards < r */
+    GDN_PLAN_NFIELDS = 9
+};
+#define GDN_PLAN_REC(r) (1 + (int64_t)(r) * GDN_PLAN_NFIELDS)
+#define GDN_PLAN_CU(num_seqs, n_shards, r) \
+    (1 + (int64_t)(n_shards) * GDN_PLAN_NFIELDS + (int64_t)(r) * ((num_seqs) + 1))
+
+int64_t gdn_cp_plan_words(int32_t num_seqs, int32_t n_shards);
+
+gdn_status gdn_cp_plan(const int32_t *cu_seqlens, int32_t num_seqs, int32_t n_shards,
+                       int32_t *plan, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Causal depthwise conv1d + SiLU with a halo
+ * ([HP-CP] _causal_conv1d_with_cp_halo; zero history before each sequence
+ * start, as the varlen plan's pre_num_conv_tokens implies)
+ *
+ *   y[t, c] = silu(bias[c] + sum_{j < conv_k} w[c, j] * x'[t - conv_k + 1 + j, c])
+ *
+ * x' is x within the token's own sequence and 0 before its start, except
+ * that the FIRST sequence continues from `halo`: halo is [conv_k - 1,
+ * channels] (row stride `channels`), its last row being the token just
+ * before x[0]; only its last `halo_len` rows are history (0 <= halo_len <=
+ * conv_k - 1; halo may be NULL when halo_len == 0).
+ *   x     device [T, channels] dtype, row stride ldx (elements)
+ *   w     device [channels, conv_k] dtype;  bias device [channels] or NULL
+ *   y     device [T, channels] dtype, row stride ldy; must not overlap x
+ * Needs channels % 8 == 0, ldx and ldy multiples of 8, and 16-byte aligned
+ * x, y and halo.  Accumulates in fp32; bf16 output rounds to nearest even.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_conv_silu(const void *x, int64_t ldx, gdn_dtype dtype, int32_t T,
+                         int32_t channels, const void *w, const void *bias, int32_t conv_k,
+                         const int32_t *cu_seqlens, int32_t num_seqs, const void *halo,
+                         int32_t halo_len, void *y, int64_t ldy, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Chunked (C = 64) gated delta rule forward, WY/UT form
+ * ([HP-CP] _prepare_gdn_chunks_for_summary + _run_prepared_gdn_chunks)
+ *
+ *   q, k  device [T, Hk, dk] dtype at q + t*ldq + h*dk + i (same for k)
+ *   v     device [T, Hv, dv] dtype at v + t*ldv + h*dv + j
+ *   g     device [T, Hv] fp32 log-gates (per-token decay exp(g))
+ *   beta  device [T, Hv] dtype
+ *   h0    device [num_seqs, Hv, dk, dv] fp32 initial states, or NULL (= 0)
+ *   o     device [T, Hv, dv] dtype (dense)
+ *   h_final device [num_seqs, Hv, dk, dv] fp32 state after each sequence's
+ *         last token (h0 or 0 for an empty sequence), or NULL
+ *   scale multiplies q (1/sqrt(dk) in the pages)
+ * Chunks restart at every sequence start; a sequence's last chunk is padded
+ * with beta = 0, g = 0 rows that are never stored.  Row strides must be
+ * multiples of 8 elements and q/k/v 16-byte aligned.  o may not alias the
+ * inputs.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, int64_t ldq,
+                         int64_t ldk, int64_t ldv, gdn_dtype dtype, const float *g,
+                         const void *beta, const float *h0, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int32_t T, int32_t Hk, int32_t Hv, int32_t dk,
+                         int32_t dv, float scale, uint32_t flags, void *o, float *h_final,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * State summary of each sequence ([HP-CP]
+ * _compute_gdn_state_summary_from_prepared): the affine map of the state
+ * across the sequence,  S_end = M S_start + N, with
+ *   M = prod_t exp(g_t) (I - beta_t k_t k_t^T)   device [num_seqs, Hv, dk, dk] fp32
+ *   N = the state reached from S_start = 0       device [num_seqs, Hv, dk, dv] fp32
+ * computed chunk by chunk on the augmented state [N | M] from [0 | I].
+ * Inputs as in gdn_chunk_fwd (q is not needed).
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_chunk_summary(const void *k, const void *v, int64_t ldk, int64_t ldv,
+                             gdn_dtype dtype, const float *g, const void *beta,
+                             const int32_t *cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                             int32_t Hv, int32_t dk, int32_t dv, uint32_t flags, float *M,
+                             float *N, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Prefix merge of shard summaries ([HP-CP]
+ * _merge_gdn_prefix_state_summaries_torch), for every value head h:
+ *   S_in[0] = S0 (or 0);   S_in[r] = M[r-1] S_in[r-1] + N[r-1],  r = 1..P-1
+ *   M device [P, Hv, dk, dk], N device [P, Hv, dk, dv], S0 device [Hv, dk, dv]
+ *   or NULL, S_in device [P, Hv, dk, dv]; all fp32.  M[P-1], N[P-1] unused.
+ * Sequential over r in fp32, parallel over heads and value columns.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_state_combine(const float *M, const float *N, const float *S0, int32_t P,
+                             int32_t Hv, int32_t dk, int32_t dv, float *S_in, void *stream);
+
+/* ------------------------------------------------------------------------
+ * The whole path on P virtual shards of one device:
+ *   plan -> conv + SiLU (halo = previous shard's rows) -> q/k/v views of the
+ *   conv output -> chunked gated delta rule per shard (pass 1; shards that
+ *   continue a sequence from an earlier shard run the [N | M] summary) ->
+ *   prefix merge -> pass 2 for the continuing shards.
+ *   x       device [T, Cch] dtype, Cch = 2*Hk*dk + Hv*dv, fused channel order
+ *           [Q (Hk*dk) | K (Hk*dk) | V (Hv*dv)] ([HP-CP] torch.split of
+ *           mixed_qkv); row stride Cch
+ *   conv_w  device [Cch, conv_k] dtype; conv_b device [Cch] dtype or NULL
+ *   g, beta, h0, o, h_final as in gdn_chunk_fwd
+ *   plan_out  device int32 [gdn_cp_plan_words(num_seqs, n_shards)] or NULL:
+ *           receives a copy of the plan (incl. its status word)
+ *   workspace device, >= gdn_shard_fwd_workspace_size(...) bytes, 256-byte
+ *           aligned; its contents on entry do not matter
+ * With n_shards == 1 this is the ordinary (unsharded) forward.  Checks on
+ * the host: T % n_shards == 0 and T / n_shards >= conv_k - 1.  A malformed
+ * cu_seqlens sets the plan status word and every later kernel returns
+ * without touching o / h_final.
+ * ---------------------------------------------------------------------- */
+size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
+                                    int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype);
+
+gdn_status gdn_shard_fwd(const void *x, const void *conv_w, const void *conv_b, int32_t conv_k,
+                         const float *g, const void *beta, const float *h0,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         int32_t n_shards, gdn_dtype dtype, void *workspace,
+                         size_t workspace_bytes, void *o, float *h_final, int32_t *plan_out,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_CP_H */

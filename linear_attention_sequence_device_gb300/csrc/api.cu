@@ -1,0 +1,301 @@
+// C ABI of libgdncp: host-side validation, status codes and stream-ordered
+// launches.  Nothing here allocates memory or synchronises the host.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+static thread_local char g_err[512] = "";
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+gdn_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+// cudaFuncAttributeMaxDynamicSharedMemorySize, set once per (device, kernel).
+gdn_status set_smem_attr(const void* func, size_t bytes) {
+    constexpr int kMaxDev = 64, kMaxFn = 32;
+    static thread_local const void* done[kMaxDev][kMaxFn] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return check_launch("cudaGetDevice");
+    for (int i = 0; i < kMaxFn; ++i) {
+        if (done[dev][i] == func) return GDN_OK;
+        if (done[dev][i] == nullptr) {
+            if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+                cudaSuccess)
+                return check_launch("cudaFuncSetAttribute");
+            done[dev][i] = func;
+            return GDN_OK;
+        }
+    }
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return check_launch("cudaFuncSetAttribute");
+    return GDN_OK;
+}
+
+int chunk_col_tile(gdn_dtype dt, int dk, int dv) {
+    if (dt == GDN_F32) return 32;
+    int t = dk < dv ? dk : dv;
+    return t < 64 ? t : 64;
+}
+
+static bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static size_t esize(gdn_dtype dt) { return dt == GDN_BF16 ? 2 : 4; }
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// checks shared by gdn_chunk_fwd / gdn_chunk_summary / gdn_shard_fwd
+static gdn_status check_heads(gdn_dtype dt, int T, int num_seqs, int Hk, int Hv, int dk, int dv) {
+    if (dt != GDN_F32 && dt != GDN_BF16) return fail(GDN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+    if (T < 0 || num_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "T=%d num_seqs=%d", T, num_seqs);
+    if (Hk < 1 || Hv < 1 || Hv % Hk != 0)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "Hv=%d must be a positive multiple of Hk=%d", Hv, Hk);
+    if (Hv > 65535) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "Hv=%d too large", Hv);
+    if (!dim_ok(dk) || !dim_ok(dv))
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "dk=%d dv=%d must be in {32,64,128}", dk, dv);
+    return GDN_OK;
+}
+
+static gdn_status check_row(const void* p, int64_t ld, int64_t minld, const char* name) {
+    if (!p) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!al16(p)) return fail(GDN_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+    if (ld < minld || ld % 8 != 0)
+        return fail(GDN_ERR_INVALID_ARG, "row stride of %s (%lld) must be >= %lld and a multiple of 8",
+                    name, (long long)ld, (long long)minld);
+    return GDN_OK;
+}
+
+static gdn_status launch_chunk(const ChunkParams& p, gdn_dtype dt, int src, dim3 grid, cudaStream_t s) {
+    if (grid.x == 0) return GDN_OK;
+    return dt == GDN_BF16 ? launch_chunk_bf16(p, src, grid, s) : launch_chunk_f32(p, src, grid, s);
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED_SHAPE: return "GDN_ERR_UNSUPPORTED_SHAPE";
+        case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE";
+        case GDN_ERR_NOT_DIVISIBLE: return "GDN_ERR_NOT_DIVISIBLE";
+        case GDN_ERR_SHARD_TOO_SHORT: return "GDN_ERR_SHARD_TOO_SHORT";
+        case GDN_ERR_BAD_CU_SEQLENS: return "GDN_ERR_BAD_CU_SEQLENS";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+const char* gdn_last_error(void) { return g_err; }
+
+int64_t gdn_cp_plan_words(int32_t num_seqs, int32_t n_shards) {
+    if (num_seqs < 1 || n_shards < 1) return 0;
+    return 1 + (int64_t)n_shards * GDN_PLAN_NFIELDS + (int64_t)n_shards * ((int64_t)num_seqs + 1);
+}
+
+gdn_status gdn_cp_plan(const int32_t* cu_seqlens, int32_t num_seqs, int32_t n_shards, int32_t* plan,
+                       void* stream) {
+    if (!cu_seqlens || !plan) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens/plan is NULL");
+    if (num_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "num_seqs=%d < 1", num_seqs);
+    if (n_shards < 1 || n_shards > 65536)
+        return fail(GDN_ERR_INVALID_ARG, "n_shards=%d not in [1, 65536]", n_shards);
+    return launch_plan(cu_seqlens, num_seqs, n_shards, plan, (cudaStream_t)stream);
+}
+
+gdn_status gdn_conv_silu(const void* x, int64_t ldx, gdn_dtype dtype, int32_t T, int32_t channels,
+                         const void* w, const void* bias, int32_t conv_k, const int32_t* cu_seqlens,
+                         int32_t num_seqs, const void* halo, int32_t halo_len, void* y, int64_t ldy,
+                         void* stream) {
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return fail(GDN_ERR_DTYPE, "unknown dtype %d", (int)dtype);
+    if (T < 0 || num_seqs < 1 || channels < 1)
+        return fail(GDN_ERR_INVALID_ARG, "T=%d num_seqs=%d channels=%d", T, num_seqs, channels);
+    if (channels % 8 != 0) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "channels=%d not a multiple of 8", channels);
+    if (conv_k < 1 || conv_k > 4) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", conv_k);
+    if (halo_len < 0 || halo_len > conv_k - 1)
+        return fail(GDN_ERR_INVALID_ARG, "halo_len=%d not in [0, conv_k-1]", halo_len);
+    if (halo_len > 0 && (!halo || !al16(halo)))
+        return fail(GDN_ERR_INVALID_ARG, "halo must be a 16-byte aligned pointer when halo_len > 0");
+    if (!w || !cu_seqlens) return fail(GDN_ERR_INVALID_ARG, "w/cu_seqlens is NULL");
+    if (T == 0) return GDN_OK;
+    gdn_status st;
+    if ((st = check_row(x, ldx, channels, "x")) != GDN_OK) return st;
+    if ((st = check_row(y, ldy, channels, "y")) != GDN_OK) return st;
+    return launch_conv(x, ldx, dtype, T, channels, w, bias, conv_k, cu_seqlens, num_seqs, halo,
+                       halo_len, y, ldy, nullptr, 1, (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ldq, int64_t ldk,
+                         int64_t ldv, gdn_dtype dtype, const float* g, const void* beta,
+                         const float* h0, const int32_t* cu_seqlens, int32_t num_seqs, int32_t T,
+                         int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         void* o, float* h_final, void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (T > 0) {
+        if ((st = check_row(q, ldq, (int64_t)Hk * dk, "q")) != GDN_OK) return st;
+        if ((st = check_row(k, ldk, (int64_t)Hk * dk, "k")) != GDN_OK) return st;
+        if ((st = check_row(v, ldv, (int64_t)Hv * dv, "v")) != GDN_OK) return st;
+        if (!g || !beta || !o) return fail(GDN_ERR_INVALID_ARG, "g/beta/o is NULL");
+        if (!al16(o)) return fail(GDN_ERR_INVALID_ARG, "o must be 16-byte aligned");
+    }
+    if (h_final && (reinterpret_cast<uintptr_t>(h_final) & 7u))
+        return fail(GDN_ERR_INVALID_ARG, "h_final must be 8-byte aligned");
+    ChunkParams p{};
+    p.q = q; p.k = k; p.v = v; p.ldq = ldq; p.ldk = ldk; p.ldv = ldv;
+    p.g = g; p.beta = beta; p.h0 = h0; p.cu = cu_seqlens;
+    p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
+    p.col_tile = chunk_col_tile(dtype, dk, dv);
+    dim3 grid(num_seqs, Hv, dv / p.col_tile);
+    return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_summary(const void* k, const void* v, int64_t ldk, int64_t ldv, gdn_dtype dtype,
+                             const float* g, const void* beta, const int32_t* cu_seqlens,
+                             int32_t num_seqs, int32_t T, int32_t Hk, int32_t Hv, int32_t dk,
+                             int32_t dv, uint32_t flags, float* M, float* N, void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens || !M || !N) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens/M/N is NULL");
+    if ((reinterpret_cast<uintptr_t>(M) | reinterpret_cast<uintptr_t>(N)) & 7u)
+        return fail(GDN_ERR_INVALID_ARG, "M and N must be 8-byte aligned");
+    if (T > 0) {
+        if ((st = check_row(k, ldk, (int64_t)Hk * dk, "k")) != GDN_OK) return st;
+        if ((st = check_row(v, ldv, (int64_t)Hv * dv, "v")) != GDN_OK) return st;
+        if (!g || !beta) return fail(GDN_ERR_INVALID_ARG, "g/beta is NULL");
+    }
+    ChunkParams p{};
+    p.q = k; p.k = k; p.v = v; p.ldq = ldk; p.ldk = ldk; p.ldv = ldv;
+    p.g = g; p.beta = beta; p.cu = cu_seqlens;
+    p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = 1.f; p.flags = flags; p.sumN = N; p.sumM = M;
+    p.col_tile = chunk_col_tile(dtype, dk, dv);
+    dim3 grid(num_seqs, Hv, (dv + dk) / p.col_tile);
+    return launch_chunk(p, dtype, JOBS_SUMMARY, grid, (cudaStream_t)stream);
+}
+
+gdn_status gdn_state_combine(const float* M, const float* N, const float* S0, int32_t P, int32_t Hv,
+                             int32_t dk, int32_t dv, float* S_in, void* stream) {
+    if (!M || !N || !S_in) return fail(GDN_ERR_INVALID_ARG, "M/N/S_in is NULL");
+    if (P < 1 || Hv < 1 || Hv > 65535) return fail(GDN_ERR_INVALID_ARG, "P=%d Hv=%d", P, Hv);
+    if (!dim_ok(dk) || !dim_ok(dv))
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "dk=%d dv=%d must be in {32,64,128}", dk, dv);
+    return launch_combine(M, N, S0, P, Hv, dk, dv, S_in, nullptr, (cudaStream_t)stream);
+}
+
+size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
+                                    int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
+    if (T < 0 || num_seqs < 1 || n_shards < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
+    const size_t cch = 2 * (size_t)Hk * dk + (size_t)Hv * dv;
+    const size_t carry = (size_t)n_shards * Hv * dk;
+    return align256(sizeof(int32_t) * (size_t)gdn_cp_plan_words(num_seqs, n_shards)) +
+           align256((size_t)T * cch * esize(dtype)) +
+           2 * align256(carry * dv * sizeof(float)) +  // carry N, S_in
+           align256(carry * dk * sizeof(float));       // carry M
+}
+
+gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k,
+                         const float* g, const void* beta, const float* h0,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         int32_t n_shards, gdn_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* o, float* h_final, int32_t* plan_out, void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (n_shards < 1 || n_shards > 65536)
+        return fail(GDN_ERR_INVALID_ARG, "n_shards=%d not in [1, 65536]", n_shards);
+    if (T < n_shards) return fail(GDN_ERR_INVALID_ARG, "T=%d < n_shards=%d", T, n_shards);
+    if (T % n_shards != 0)
+        return fail(GDN_ERR_NOT_DIVISIBLE, "T=%d is not divisible by n_shards=%d", T, n_shards);
+    if (conv_k < 1 || conv_k > 4) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", conv_k);
+    if (n_shards > 1 && T / n_shards < conv_k - 1)
+        return fail(GDN_ERR_SHARD_TOO_SHORT, "shard length %d < conv halo %d", T / n_shards, conv_k - 1);
+    if (!x || !conv_w || !g || !beta || !cu_seqlens || !o)
+        return fail(GDN_ERR_INVALID_ARG, "x/conv_w/g/beta/cu_seqlens/o is NULL");
+    if (!al16(x) || !al16(o)) return fail(GDN_ERR_INVALID_ARG, "x and o must be 16-byte aligned");
+    if (h_final && (reinterpret_cast<uintptr_t>(h_final) & 7u))
+        return fail(GDN_ERR_INVALID_ARG, "h_final must be 8-byte aligned");
+    const size_t need = gdn_shard_fwd_workspace_size(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
+    if (!workspace || workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t cch = 2 * (int64_t)Hk * dk + (int64_t)Hv * dv;
+    const int P = n_shards;
+    char* ws = static_cast<char*>(workspace);
+    const int64_t words = gdn_cp_plan_words(num_seqs, P);
+    int32_t* plan = reinterpret_cast<int32_t*>(ws);
+    ws += align256(sizeof(int32_t) * (size_t)words);
+    void* y = ws;
+    ws += align256((size_t)T * cch * esize(dtype));
+    const size_t carry = (size_t)P * Hv * dk;
+    float* carryN = reinterpret_cast<float*>(ws);
+    ws += align256(carry * dv * sizeof(float));
+    float* S_in = reinterpret_cast<float*>(ws);
+    ws += align256(carry * dv * sizeof(float));
+    float* carryM = reinterpret_cast<float*>(ws);
+
+    // 1. plan
+    if ((st = launch_plan(cu_seqlens, num_seqs, P, plan, s)) != GDN_OK) return st;
+    // 2. conv + SiLU, each shard reading its halo from the previous shard's rows
+    if ((st = launch_conv(x, cch, dtype, T, (int)cch, conv_w, conv_b, conv_k, cu_seqlens, num_seqs,
+                          nullptr, 0, y, cch, plan, P, s)) != GDN_OK)
+        return st;
+    // 3. pass 1: every segment with a known initial state, plus [N | M] summaries
+    ChunkParams p{};
+    const size_t es = esize(dtype);
+    p.q = y;
+    p.k = static_cast<const char*>(y) + (size_t)Hk * dk * es;
+    p.v = static_cast<const char*>(y) + (size_t)2 * Hk * dk * es;
+    p.ldq = p.ldk = p.ldv = cch;
+    p.g = g; p.beta = beta; p.h0 = h0; p.cu = cu_seqlens;
+    p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
+    p.sumN = carryN; p.sumM = carryM; p.S_in = S_in; p.plan = plan; p.n_shards = P;
+    p.col_tile = chunk_col_tile(dtype, dk, dv);
+    {
+        dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
+        if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
+    }
+    if (P > 1) {
+        // 4. prefix merge of the shard carries
+        if ((st = launch_combine(carryM, carryN, nullptr, P, Hv, dk, dv, S_in, plan, s)) != GDN_OK)
+            return st;
+        // 5. pass 2: the first segment of every shard that continues a sequence
+        dim3 grid(P, Hv, dv / p.col_tile);
+        if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS2, grid, s)) != GDN_OK) return st;
+    }
+    if (h_final) {
+        if ((st = launch_empty_seq_final(cu_seqlens, num_seqs, Hv, dk, dv, h0, h_final, plan, s)) != GDN_OK)
+            return st;
+    }
+    if (plan_out) {
+        if (cudaMemcpyAsync(plan_out, plan, sizeof(int32_t) * (size_t)words, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+            return check_launch("plan copy");
+    }
+    return GDN_OK;
+}
+
+}  // extern "C"

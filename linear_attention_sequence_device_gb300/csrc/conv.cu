@@ -1,0 +1,186 @@
+// Causal depthwise conv1d + SiLU with the previous shard's halo
+// (hyper-parallel page, _causal_conv1d_with_cp_halo; zero history before a
+// sequence start as implied by the varlen plan's pre_num_conv_tokens).
+//
+// HBM-bound stencil.  Each thread owns 8 consecutive channels (one 16-byte
+// bf16 vector, two for fp32) of a strip of R rows and slides a register
+// window of the last conv_k - 1 input rows down the strip, so every input
+// element is read once (plus conv_k - 1 halo rows per strip).  A warp covers
+// 256 contiguous channels of a row: fully coalesced 512-byte transactions.
+// Grid: (channel blocks, strips per shard, shards).
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int NT = 128;
+constexpr int R = 32;  // rows per strip
+
+struct ConvParams {
+    const void* x; int64_t ldx;
+    void* y; int64_t ldy;
+    const void* w; const void* b;
+    int T, C, Kc;
+    const int32_t* cu; int num_seqs;   // explicit mode (plan == null)
+    const void* halo; int halo_len;    // explicit mode
+    const int32_t* plan; int P;        // shard mode
+};
+
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* f) {
+        uint4 raw = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* f) {
+        uint4 raw;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = raw;
+    }
+};
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float* p, float* f) {
+        float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* f) {
+        reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+};
+
+template <typename T, int KC>
+__global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
+    const int c0 = (blockIdx.x * NT + threadIdx.x) * 8;
+    if (c0 >= p.C) return;
+    int part, rs;
+    const int32_t* lc;   // local cu_seqlens of this shard
+    int nloc;            // number of local sequences
+    int hlen;            // rows of history before local row 0 for the first sequence
+    if (p.plan) {
+        if (p.plan[0] != 0) return;  // malformed cu_seqlens
+        const int r = blockIdx.z;
+        part = p.T / p.P;
+        rs = r * part;
+        const int32_t* rec = p.plan + GDN_PLAN_REC(r);
+        lc = p.plan + GDN_PLAN_CU(p.num_seqs, p.P, r);
+        nloc = rec[GDN_PLAN_LOCAL_NUM_SEQS];
+        hlen = min(KC - 1, (int)rec[GDN_PLAN_PRE_NUM_CONV_TOKENS]);
+    } else {
+        part = p.T;
+        rs = 0;
+        lc = p.cu;
+        nloc = p.num_seqs;
+        hlen = p.halo_len;
+    }
+    const int lt0 = blockIdx.y * R;
+    if (lt0 >= part) return;
+    const int lt1 = min(part, lt0 + R);
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    T* __restrict__ y = static_cast<T*>(p.y);
+
+    float wr[KC][8], br[8];
+    {
+        const T* w = static_cast<const T*>(p.w);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+#pragma unroll
+            for (int j = 0; j < KC; ++j) wr[j][c] = Elem<T>::to_f(w[(int64_t)(c0 + c) * KC + j]);
+            br[c] = p.b ? Elem<T>::to_f(static_cast<const T*>(p.b)[c0 + c]) : 0.f;
+        }
+    }
+    // local sequence containing row lt0 and the next boundary after it
+    int seg = upper_bound_minus1(lc, nloc, lt0);
+    if (seg > nloc - 1) seg = nloc - 1;  // lt0 == part cannot happen; guard anyway
+    int seg_start = lc[seg];
+    int next = seg + 1 <= nloc ? lc[seg + 1] : part;
+
+    // window: win[j] holds input row (t - (KC-1) + j) for j < KC-1
+    float win[KC > 1 ? KC - 1 : 1][8];
+#pragma unroll
+    for (int j = 0; j < KC - 1; ++j) {
+        const int lrow = lt0 - (KC - 1) + j;  // local row index of the history entry
+        bool have = false;
+        const T* src = nullptr;
+        if (lrow >= seg_start && lrow >= 0) {
+            have = true;
+            src = x + (int64_t)(rs + lrow) * p.ldx + c0;
+        } else if (seg == 0 && seg_start - lrow <= hlen) {
+            const int m = seg_start - lrow;  // rows before the shard start (1 = adjacent)
+            have = true;
+            if (p.plan) src = x + (int64_t)(rs - m) * p.ldx + c0;  // previous shard's rows
+            else src = static_cast<const T*>(p.halo) + (int64_t)(KC - 1 - m) * p.C + c0;
+        }
+        if (have) Vec8<T>::load(src, win[j]);
+        else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
+        }
+    }
+    for (int t = lt0; t < lt1; ++t) {
+        while (t == next) {  // a new sequence starts: no history
+#pragma unroll
+            for (int j = 0; j < KC - 1; ++j)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
+            ++seg;
+            next = seg + 1 <= nloc ? lc[seg + 1] : part;
+        }
+        float cur[8];
+        Vec8<T>::load(x + (int64_t)(rs + t) * p.ldx + c0, cur);
+        float out[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float acc = br[c];
+#pragma unroll
+            for (int j = 0; j < KC - 1; ++j) acc = fmaf(wr[j][c], win[j][c], acc);
+            acc = fmaf(wr[KC - 1][c], cur[c], acc);
+            out[c] = acc / (1.f + expf(-acc));
+        }
+        Vec8<T>::store(y + (int64_t)(rs + t) * p.ldy + c0, out);
+#pragma unroll
+        for (int j = 0; j + 1 < KC - 1; ++j)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[j][c] = win[j + 1][c];
+        if (KC > 1) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[KC > 1 ? KC - 2 : 0][c] = cur[c];
+        }
+    }
+}
+
+template <typename T>
+gdn_status launch_t(const ConvParams& p, dim3 grid, cudaStream_t s) {
+    switch (p.Kc) {
+        case 1: conv_kernel<T, 1><<<grid, NT, 0, s>>>(p); break;
+        case 2: conv_kernel<T, 2><<<grid, NT, 0, s>>>(p); break;
+        case 3: conv_kernel<T, 3><<<grid, NT, 0, s>>>(p); break;
+        case 4: conv_kernel<T, 4><<<grid, NT, 0, s>>>(p); break;
+        default: return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", p.Kc);
+    }
+    return check_launch("conv_kernel");
+}
+
+}  // namespace
+
+gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, const void* w,
+                       const void* b, int Kc, const int32_t* cu, int num_seqs, const void* halo,
+                       int halo_len, void* y, int64_t ldy, const int32_t* plan, int P,
+                       cudaStream_t s) {
+    ConvParams p{x, ldx, y, ldy, w, b, T, C, Kc, cu, num_seqs, halo, halo_len, plan, plan ? P : 1};
+    const int part = T / p.P;
+    dim3 grid((C / 8 + NT - 1) / NT, (part + R - 1) / R, p.P);
+    if (grid.y == 0) return GDN_OK;
+    return dt == GDN_BF16 ? launch_t<__nv_bfloat16>(p, grid, s) : launch_t<float>(p, grid, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,224 @@
+// Internal declarations shared by the CUDA translation units of libgdncp.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_cp.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;  // chunk size C of the WY/UT form
+
+// ----------------------------------------------------------------------------
+// host-side error reporting (api.cu)
+// ----------------------------------------------------------------------------
+gdn_status fail(gdn_status s, const char* fmt, ...);
+gdn_status check_launch(const char* what);
+
+// ----------------------------------------------------------------------------
+// small device helpers
+// ----------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ float to_f(float x) { return x; }
+    static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// index of the last i in [0, n] with a[i] <= x (a non-decreasing, a[0] <= x)
+__device__ __forceinline__ int upper_bound_minus1(const int32_t* a, int n, int x) {
+    int lo = 0, hi = n;  // invariant: a[lo] <= x, answer in [lo, hi]
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ----------------------------------------------------------------------------
+// chunk kernels: one CTA runs one "job" = one token range of one value head
+// and one tile of state columns, chunk after chunk.
+// ----------------------------------------------------------------------------
+struct ChunkJob {
+    int t0, t1;            // tokens [t0, t1)
+    int hv;                // value head
+    int col0;              // first state column of this tile (within V or M)
+    const float* init;     // initial state tile (row stride init_ld), or null = 0
+    int64_t init_ld;
+    float* fin;            // final state tile destination (row stride fin_ld), or null
+    int64_t fin_ld;
+    bool identity_init;    // M part of a summary: start from identity columns
+    bool value_zero;       // M part of a summary: value columns are zero
+    bool write_o;
+};
+
+// Where a chunk kernel gets its jobs from.
+enum JobSource : int {
+    JOBS_SEQS = 0,        // gdn_chunk_fwd: grid (num_seqs, Hv, dv tiles)
+    JOBS_SUMMARY = 1,     // gdn_chunk_summary: grid (num_seqs, Hv, (dv + dk) tiles)
+    JOBS_SHARD_PASS1 = 2, // gdn_shard_fwd pass 1: grid (num_seqs + P, Hv, (dv + dk) tiles)
+    JOBS_SHARD_PASS2 = 3  // gdn_shard_fwd pass 2: grid (P, Hv, dv tiles)
+};
+
+struct ChunkParams {
+    const void* q; const void* k; const void* v;
+    int64_t ldq, ldk, ldv;
+    const float* g;
+    const void* beta;
+    const float* h0;
+    const int32_t* cu;      // global cu_seqlens
+    int num_seqs, T, Hk, Hv, dk, dv;
+    float scale;
+    uint32_t flags;
+    void* o;                // [T, Hv, dv]
+    float* h_final;         // [num_seqs, Hv, dk, dv] or null
+    // summaries / shard path
+    float* sumN;            // [n, Hv, dk, dv]
+    float* sumM;            // [n, Hv, dk, dk]
+    const float* S_in;      // [P, Hv, dk, dv]
+    const int32_t* plan;    // plan words (shard path)
+    int n_shards;
+    int col_tile;           // state columns per CTA
+};
+
+// Resolve blockIdx -> job.  Returns false when this CTA has nothing to do.
+__device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob& j) {
+    const int hv = blockIdx.y;
+    const int nvt = p.dv / p.col_tile;
+    const int z = blockIdx.z;
+    j.hv = hv;
+    j.identity_init = false;
+    j.value_zero = false;
+    j.init = nullptr;
+    j.fin = nullptr;
+    j.init_ld = p.dv;
+    j.fin_ld = p.dv;
+    auto clampT = [&](int t) { return t < 0 ? 0 : (t > p.T ? p.T : t); };
+    if (src == JOBS_SEQS || src == JOBS_SUMMARY) {
+        const int n = blockIdx.x;
+        j.t0 = clampT(__ldg(p.cu + n));
+        j.t1 = clampT(__ldg(p.cu + n + 1));
+        if (j.t1 < j.t0) j.t1 = j.t0;
+        if (src == JOBS_SEQS) {
+            j.col0 = z * p.col_tile;
+            j.write_o = true;
+            const int64_t st = ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;
+            if (p.h0) j.init = p.h0 + st;
+            if (p.h_final) j.fin = p.h_final + st;
+            return true;
+        }
+        j.write_o = false;
+        if (z < nvt) {
+            j.col0 = z * p.col_tile;
+            j.fin = p.sumN + ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;
+        } else {
+            j.col0 = (z - nvt) * p.col_tile;
+            j.identity_init = true;
+            j.value_zero = true;
+            j.fin = p.sumM + ((int64_t)n * p.Hv + hv) * p.dk * p.dk + j.col0;
+            j.fin_ld = p.dk;
+        }
+        return true;
+    }
+    // ---- shard path -------------------------------------------------------
+    const int32_t* plan = p.plan;
+    if (__ldg(plan) != 0) return false;  // malformed cu_seqlens: do nothing
+    const int P = p.n_shards;
+    const int part = p.T / P;
+    const int64_t cu_base = 1 + (int64_t)P * GDN_PLAN_NFIELDS;
+    if (src == JOBS_SHARD_PASS2) {
+        const int r = blockIdx.x;
+        const int32_t* rec = plan + 1 + (int64_t)r * GDN_PLAN_NFIELDS;
+        if (__ldg(rec + GDN_PLAN_IS_FIRST_RANK)) return false;
+        if (z >= nvt) return false;
+        const int32_t* lc = plan + cu_base + (int64_t)r * (p.num_seqs + 1);
+        const int nloc = __ldg(rec + GDN_PLAN_LOCAL_NUM_SEQS);
+        const int post = __ldg(rec + GDN_PLAN_POST_NUM_RANKS);
+        const int n = __ldg(rec + GDN_PLAN_START_SEQ_IDX);
+        j.t0 = r * part;
+        j.t1 = r * part + __ldg(lc + 1);
+        j.col0 = z * p.col_tile;
+        j.write_o = true;
+        j.init = p.S_in + ((int64_t)r * p.Hv + hv) * p.dk * p.dv + j.col0;
+        const bool continues = (nloc == 1 && post > 0);
+        if (!continues && p.h_final)
+            j.fin = p.h_final + ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;
+        return true;
+    }
+    // pass 1: blockIdx.x = flat (shard, local segment) slot
+    const int slot = blockIdx.x;
+    int lo = 0, hi = P - 1;  // last shard with seg_offset <= slot
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(plan + 1 + (int64_t)mid * GDN_PLAN_NFIELDS + GDN_PLAN_SEG_OFFSET) <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    const int r = lo;
+    const int32_t* rec = plan + 1 + (int64_t)r * GDN_PLAN_NFIELDS;
+    const int i = slot - __ldg(rec + GDN_PLAN_SEG_OFFSET);
+    const int nloc = __ldg(rec + GDN_PLAN_LOCAL_NUM_SEQS);
+    if (i < 0 || i >= nloc) return false;
+    const int32_t* lc = plan + cu_base + (int64_t)r * (p.num_seqs + 1);
+    const bool first_rank = __ldg(rec + GDN_PLAN_IS_FIRST_RANK) != 0;
+    const int post = __ldg(rec + GDN_PLAN_POST_NUM_RANKS);
+    const bool continues_in = (i == 0 && !first_rank);
+    const bool continues_out = (i == nloc - 1 && post > 0);
+    j.t0 = r * part + __ldg(lc + i);
+    j.t1 = r * part + __ldg(lc + i + 1);
+    const int64_t carry_st = ((int64_t)r * p.Hv + hv) * p.dk * p.dv;
+    if (continues_in) {
+        if (!continues_out) return false;       // only pass 2 for this segment
+        // spanning shard: affine summary [N | M] from [0 | I]
+        j.write_o = false;
+        if (z < nvt) {
+            j.col0 = z * p.col_tile;
+            j.fin = p.sumN + carry_st + j.col0;
+        } else {
+            j.col0 = (z - nvt) * p.col_tile;
+            j.identity_init = true;
+            j.value_zero = true;
+            j.fin = p.sumM + ((int64_t)r * p.Hv + hv) * p.dk * p.dk + j.col0;
+            j.fin_ld = p.dk;
+        }
+        return true;
+    }
+    if (z >= nvt) return false;
+    // segment starts a sequence in this shard: initial state is known
+    const int n = upper_bound_minus1(p.cu, p.num_seqs, j.t0);
+    j.col0 = z * p.col_tile;
+    j.write_o = true;
+    const int64_t st = ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;
+    if (p.h0) j.init = p.h0 + st;
+    if (continues_out) j.fin = p.sumN + carry_st + j.col0;  // constant carry (M = 0)
+    else if (p.h_final) j.fin = p.h_final + st;
+    return true;
+}
+
+// launchers (chunk_bf16.cu / chunk_f32.cu)
+gdn_status launch_chunk_bf16(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
+gdn_status launch_chunk_f32(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
+int chunk_col_tile(gdn_dtype dt, int dk, int dv);
+
+// plan.cu
+gdn_status launch_plan(const int32_t* cu, int num_seqs, int P, int32_t* plan, cudaStream_t s);
+// conv.cu: per-shard conv; plan == null -> one shard with an explicit halo
+gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, const void* w,
+                       const void* b, int Kc, const int32_t* cu, int num_seqs, const void* halo,
+                       int halo_len, void* y, int64_t ldy, const int32_t* plan, int P,
+                       cudaStream_t s);
+// combine.cu: plan == null -> every shard affine
+gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
+                          int dv, float* S_in, const int32_t* plan, cudaStream_t s);
+// empty sequences in the shard path: h_final = h0 or 0
+gdn_status launch_empty_seq_final(const int32_t* cu, int num_seqs, int Hv, int dk, int dv,
+                                  const float* h0, float* h_final, const int32_t* plan,
+                                  cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,99 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+that include/gdn_cp.h declares, and rejects bad arguments on the host with
+the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn_cp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_sequence_device_gb300 import build, binding
+    build.build_library()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gdn_[a-z_0-9]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from linear_attention_sequence_device_gb300 import binding
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in binding.SIGNATURES, n
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"GDN_OK"), (4, b"GDN_ERR_NOT_DIVISIBLE"), (9, b"GDN_ERR_WORKSPACE")]:
+        assert lib.gdn_status_string(code) == name
+
+
+def test_plan_words(lib):
+    assert lib.gdn_cp_plan_words(3, 2) == 1 + 2 * 9 + 2 * 4
+    assert lib.gdn_cp_plan_words(0, 2) == 0
+
+
+FAKE = ctypes.c_void_p(4096)  # never dereferenced: every call below fails on the host
+
+
+def shard_call(lib, **kw):
+    a = dict(x=FAKE, w=FAKE, b=None, conv_k=4, g=FAKE, beta=FAKE, h0=None, cu=FAKE, N=1, T=256,
+             Hk=2, Hv=2, dk=32, dv=32, scale=0.1, flags=1, P=2, dt=0, ws=FAKE, ws_bytes=1 << 40,
+             o=FAKE, hf=None, plan=None)
+    a.update(kw)
+    st = lib.gdn_shard_fwd(a["x"], a["w"], a["b"], a["conv_k"], a["g"], a["beta"], a["h0"],
+                           a["cu"], a["N"], a["T"], a["Hk"], a["Hv"], a["dk"], a["dv"], a["scale"],
+                           a["flags"], a["P"], a["dt"], a["ws"], a["ws_bytes"], a["o"], a["hf"],
+                           a["plan"], None)
+    return st, lib.gdn_last_error().decode()
+
+
+def test_shard_fwd_host_errors(lib):
+    assert shard_call(lib, T=250, P=8)[0] == 4                       # not divisible
+    assert shard_call(lib, T=16, P=8)[0] == 5                        # shard 2 < halo 3
+    assert shard_call(lib, dk=48)[0] == 2                            # unsupported dk
+    assert shard_call(lib, Hk=3, Hv=4)[0] == 2                       # Hv % Hk
+    assert shard_call(lib, dt=7)[0] == 3                             # dtype
+    assert shard_call(lib, conv_k=5)[0] == 2
+    assert shard_call(lib, x=None)[0] == 1
+    st, msg = shard_call(lib, ws_bytes=16)
+    assert st == 9 and "workspace" in msg
+    assert shard_call(lib, T=4, P=8)[0] == 1                         # fewer tokens than shards
+
+
+def test_chunk_fwd_host_errors(lib):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ldq=64, ldk=64, ldv=64, dt=1, T=10, Hk=2, Hv=2, dk=32,
+                 dv=32, N=1)
+        a.update(kw)
+        return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["ldq"], a["ldk"], a["ldv"], a["dt"],
+                                 FAKE, FAKE, None, FAKE, a["N"], a["T"], a["Hk"], a["Hv"], a["dk"],
+                                 a["dv"], 0.1, 0, FAKE, None, None)
+    assert call(ldq=60) == 1          # stride below Hk * dk
+    assert call(ldq=68) == 1          # stride not a multiple of 8
+    assert call(q=ctypes.c_void_p(4104)) == 1  # misaligned
+    assert call(N=0) == 1
+    assert call(dv=96) == 2
+
+
+def test_conv_host_errors(lib):
+    def call(**kw):
+        a = dict(C=64, K=4, halo=None, hl=0, T=8)
+        a.update(kw)
+        return lib.gdn_conv_silu(FAKE, a["C"], 1, a["T"], a["C"], FAKE, None, a["K"], FAKE, 1,
+                                 a["halo"], a["hl"], FAKE, a["C"], None)
+    assert call(C=60) == 2
+    assert call(K=0) == 2
+    assert call(hl=3) == 1            # halo_len > 0 without a halo pointer
+    assert call(hl=4, halo=FAKE) == 1  # halo_len > conv_k - 1
