@@ -1,0 +1,375 @@
+"""Benchmark of the context-parallel Gated DeltaNet forward on GB300.
+
+One step = one gdn_shard_fwd call (plan, conv + SiLU with halo, chunked gated
+delta rule, and for P > 1 the prefix merge and second pass) over one batch of
+seeded synthetic input resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the workload on its own GPU (weak scaling, no
+collective on the data path); value = total tokens of all ranks / the
+slowest rank's time.  --impl reference times the fp64 CPU oracle (the only
+reference implementation that exists for this path) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd tokens/s at 1 GB300 (bf16, d=128) and % of roofline; oracle tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def workload(name):
+    import workloads as W
+    return W.CONFIGS[name]()
+
+
+def algorithmic(w):
+    """Algorithmic bytes and FLOPs of the chunk step (real tokens, C = 64);
+    the UT triangular solve is ALU work and not credited."""
+    e = 2 if w.dtype == "bf16" else 4
+    T, Hk, Hv, K, V, C = w.T, w.Hk, w.Hv, w.dk, w.dv, 64
+    chunk_bytes = T * (2 * Hk * K * e + Hv * V * e      # q, k, v in
+                       + Hv * V * e                      # o out
+                       + Hv * (4 + e))                   # g fp32, beta
+    chunk_bytes += w.N * Hv * K * V * 4                  # h_final
+    if w.h0_std:
+        chunk_bytes += w.N * Hv * K * V * 4
+    flops = T * (4 * C * K * Hk + (2 * C * K + 4 * C * V + 6 * K * V) * Hv)
+    conv_bytes = 2 * T * w.Cch * e
+    return chunk_bytes, flops, conv_bytes
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.samples = []
+        if self.proc is None:
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return None
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if s[4 + i].lower().startswith("active")})
+        pw = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(self.samples)}
+
+
+def time_loop(fn, n, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(n):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / n  # ms
+
+
+def to_dev(a, dtype, dev):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+
+def oracle_prefix_runner(w):
+    """Returns run(S): the fp64 oracle (whole path) on the first S tokens."""
+    import oracle
+    import workloads as W
+    cu = w.cu_seqlens()
+
+    def run(S):
+        cu_s = np.concatenate([cu[cu < S], [S]]).astype(np.int64)
+        x = W.as_f64(w.x(rows=(0, S)), w.dtype)
+        cw = W.as_f64(w.conv_w(), w.dtype)
+        g = w.g(rows=(0, S)).astype(np.float64)
+        b = W.as_f64(w.beta(rows=(0, S)), w.dtype)
+        h0 = w.h0()
+        h0 = None if h0 is None else h0[: len(cu_s) - 1].astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.path_forward(x, cw, None, g, b, h0, cu_s, w.Hk, w.Hv, w.dk, w.dv, w.scale)
+        return time.perf_counter() - t0
+    return run
+
+
+def calibrate(run, T, budget_s):
+    S = 256
+    dt = run(S)
+    while dt < budget_s / 2.5 and S * 2 <= T:
+        S *= 2
+        dt = run(S)
+    return S, dt
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The fp64 oracle (whole path) on a bounded prefix of the workload."""
+    import oracle
+    run = oracle_prefix_runner(w)
+    S, dt = calibrate(run, w.T, budget_s)
+    threads = oracle.max_threads()
+    return {"value": S / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {S} tokens of the {w.name} workload (all {w.Hv} value heads, "
+                      f"conv + L2 norm + token recurrence in fp64), {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = workload(args.config)
+    import oracle
+    oracle.build()
+    import workloads as W
+    W.build_synth()
+    run = oracle_prefix_runner(w)
+    S, _ = calibrate(run, w.T, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        run(S)
+    per = [run(S) for _ in range(args.steps)]
+    dt = float(np.median(per))
+    v = S / dt
+    cb = {"value": v, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+          "sample": f"first {S} tokens of the {w.name} workload per step (all {w.Hv} value heads, "
+                    f"conv + L2 norm + token recurrence in fp64), median {dt:.2f} s"}
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
+            "config": config_dict(w), "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": w.name, "T": w.T, "num_seqs": w.N, "Hk": w.Hk, "Hv": w.Hv, "dk": w.dk,
+            "dv": w.dv, "n_shards": w.n_shards, "conv_k": w.conv_k, "dtype": w.dtype,
+            "l2": "inputs larger than L2 (raw qkv %.0f MiB)" % (w.T * w.Cch * (2 if w.dtype == "bf16" else 4) / 2**20)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import linear_attention_sequence_device_gb300 as g
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workload(args.config)
+    P = w.n_shards
+    # inputs: rank-specific seed so replicas are independent problems
+    if rank:
+        w = w.replace(seed=w.seed + 1000 * rank)
+    x_h, cw_h, g_h, b_h = w.x(), w.conv_w(), w.g(), w.beta()
+    h0_h = w.h0()
+    x, cw = to_dev(x_h, w.dtype, dev), to_dev(cw_h, w.dtype, dev)
+    gg, bb = to_dev(g_h, "f32", dev), to_dev(b_h, w.dtype, dev)
+    h0 = None if h0_h is None else to_dev(h0_h, "f32", dev)
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ws = torch.empty(g.shard_fwd_workspace_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, tdt),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty((w.T, w.Hv, w.dv), dtype=tdt, device=dev)
+    hf_d = torch.empty((w.N, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        g.gdn_shard_fwd(x, cw, None, gg, bb, cu, w.Hk, w.Hv, w.dk, w.dv, P, h0=h0, workspace=ws,
+                        out=o, h_final=hf_d)
+
+    launches_per_step = 3 + 1 + (2 if P > 1 else 0)  # plan, conv, pass 1, empty-seq final (+ merge, pass 2)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ms = time_loop(step, args.steps, stream)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.T / (ms * 1e-3)
+
+    # ---- end to end through the public API with host buffers ----
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    xh = pin(x_h.view(np.int16) if w.dtype == "bf16" else x_h)
+    gh, bh = pin(g_h), pin(b_h.view(np.int16) if w.dtype == "bf16" else b_h)
+    cuh = pin(w.cu_seqlens())
+    oh = torch.empty((w.T, w.Hv, w.dv), dtype=tdt).pin_memory()
+    hfh = torch.empty((w.N, w.Hv, w.dk, w.dv), dtype=torch.float32).pin_memory()
+    xd_e = torch.empty_like(x)
+    gd_e, bd_e, cud_e = torch.empty_like(gg), torch.empty_like(bb), torch.empty_like(cu)
+
+    def e2e_step():
+        xd_e.view(torch.int16 if w.dtype == "bf16" else tdt).copy_(xh, non_blocking=True)
+        gd_e.copy_(gh, non_blocking=True)
+        bd_e.view(torch.int16 if w.dtype == "bf16" else tdt).copy_(bh, non_blocking=True)
+        cud_e.copy_(cuh, non_blocking=True)
+        g.gdn_shard_fwd(xd_e, cw, None, gd_e, bd_e, cud_e, w.Hk, w.Hv, w.dk, w.dv, P, h0=h0,
+                        workspace=ws, out=o, h_final=hf_d)
+        oh.copy_(o, non_blocking=True)
+        hfh.copy_(hf_d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms = time_loop(e2e_step, e2e_steps, stream)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * xh.element_size() + gh.numel() * 4 + bh.numel() * bh.element_size() + cuh.numel() * 4
+    d2h = oh.numel() * oh.element_size() + hfh.numel() * 4
+
+    # ---- dominant kernel: the chunk kernel alone (same kernel, same work) ----
+    Cch = w.Cch
+    y = torch.empty((w.T, Cch), dtype=tdt, device=dev)
+    g.gdn_conv_silu(x, cw, None, cu, out=y)
+    q = y[:, :w.Hk * w.dk].view(w.T, w.Hk, w.dk)
+    k = y[:, w.Hk * w.dk:2 * w.Hk * w.dk].view(w.T, w.Hk, w.dk)
+    v = y[:, 2 * w.Hk * w.dk:].view(w.T, w.Hv, w.dv)
+    hf_k = torch.empty((w.N, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
+    o_k = torch.empty_like(o)
+
+    def chunk_only():
+        g.gdn_chunk_fwd(q, k, v, gg, bb, cu, h0=h0, l2norm=True, out=o_k)
+
+    def conv_only():
+        g.gdn_conv_silu(x, cw, None, cu, out=y)
+
+    for _ in range(3):
+        chunk_only()
+        conv_only()
+    n_k = max(5, min(args.steps, 50))
+    chunk_ms = time_loop(chunk_only, n_k, stream)
+    conv_ms = time_loop(conv_only, n_k, stream)
+    del hf_k
+
+    peaks, peak_src = load_peaks()
+    chunk_bytes, flops, conv_bytes = algorithmic(w)
+    hbm = float(peaks["hbm_gbs"])
+    tfl = float(peaks["bf16_tflops"])
+    t_bytes = chunk_bytes / (hbm * 1e9)
+    t_flops = flops / (tfl * 1e12)
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", f"chunk_traffic_{w.name}.json")
+    if os.path.exists(tp):
+        traffic = json.load(open(tp)).get("bytes_per_launch")
+    if t_bytes >= t_flops:
+        ach = chunk_bytes / (chunk_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic}
+    else:
+        ach = flops / (chunk_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tfl, "unit": "TFLOP/s",
+                "frac": ach / tfl, "traffic": traffic}
+    roof.update({"kernel": "chunk_bf16_kernel" if w.dtype == "bf16" else "chunk_f32_kernel",
+                 "kernel_ms": chunk_ms, "peak_source": peak_src + " (burst)",
+                 "algorithmic_bytes": chunk_bytes, "algorithmic_flops": flops,
+                 "tensor_frac": (flops / (chunk_ms * 1e-3) / 1e12) / tfl,
+                 "roofline_ms": max(t_bytes, t_flops) * 1e3})
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded counter-based generator; no dataset)",
+            "config": config_dict(w),
+            "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": roof,
+            "kernels": {"chunk_ms": chunk_ms, "conv_ms": conv_ms,
+                        "conv_GBps": conv_bytes / (conv_ms * 1e-3) / 1e9,
+                        "conv_frac_hbm": conv_bytes / (conv_ms * 1e-3) / 1e9 / hbm},
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(workload(args.config))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="packed_varlen")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -227,6 +227,7 @@ def gdn_shard_fwd(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shar
                   scale=None, l2norm=True, workspace=None, out=None, h_final=True,
                   want_plan=False):
     """The whole path on n_shards virtual shards.  x [T, 2*Hk*dk + Hv*dv].
+    h_final: True (allocate), False (skip) or an output tensor [N, Hv, dk, dv].
     Returns (o [T, Hv, dv], h_final [N, Hv, dk, dv] or None, plan words or None)."""
     dt = x.dtype
     for t, n in ((x, "x"), (conv_w, "conv_w"), (conv_b, "conv_b"), (beta, "beta")):
@@ -241,7 +242,11 @@ def gdn_shard_fwd(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shar
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
     o = torch.empty((T, Hv, dv), dtype=dt, device=x.device) if out is None else out
-    hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=x.device) if h_final else None
+    if isinstance(h_final, torch.Tensor):
+        _need(h_final, "h_final", torch.float32)
+        hf = h_final
+    else:
+        hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=x.device) if h_final else None
     plan = torch.empty(plan_words(N, n_shards), dtype=torch.int32, device=x.device) \
         if want_plan else None
     _check(load().gdn_shard_fwd(_p(x.contiguous()), _p(conv_w.contiguous()), _p(conv_b),

@@ -232,7 +232,8 @@ def lengths_geometric(seed, T, p, lo, hi):
 
 def tiny(**kw) -> Workload:
     """1 sequence of 256 tokens, 2 heads, d=32, fp32, 2 virtual shards, seed 0."""
-    return Workload("tiny", 256, 2, 2, 32, 32, "f32", 2, 0, (256,), **kw)
+    return Workload("tiny", 256, 2, 2, 32, 32, "f32", kw.pop("n_shards", 2), kw.pop("seed", 0),
+                    (256,), **kw)
 
 
 def packed_varlen(T: int = 32768, **kw) -> Workload:
