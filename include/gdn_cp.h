@@ -230,6 +230,36 @@ gdn_status gdn_shard_fwd(const void *x, const void *conv_w, const void *conv_b, 
                          size_t workspace_bytes, void *o, float *h_final, int32_t *plan_out,
                          void *stream);
 
+/* ------------------------------------------------------------------------
+ * gdn_shard_fwd without a caller workspace.  The source pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- a plugin whose host application owns all device buffers
+ * and passes it only inputs and outputs, or a latency-critical loop that may
+ * not call cudaMalloc (which can synchronise the device).
+ *
+ * Same arguments and results as gdn_shard_fwd, minus the workspace.  The
+ * scratch is one file-scope device array of GDN_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) that every device loading the library holds until the process
+ * exits.  A problem whose gdn_shard_fwd_workspace_size(...) exceeds it is
+ * rejected with GDN_ERR_WORKSPACE before anything is enqueued.  The entry
+ * point never calls cudaMalloc/cudaFree or any allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's
+ *     contents; nothing in it needs to start at zero.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on it:
+ *     serialise them, e.g. on one stream.
+ * ---------------------------------------------------------------------- */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+gdn_status gdn_shard_fwd_noalloc(const void *x, const void *conv_w, const void *conv_b,
+                                 int32_t conv_k, const float *g, const void *beta, const float *h0,
+                                 const int32_t *cu_seqlens, int32_t num_seqs, int32_t T,
+                                 int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale,
+                                 uint32_t flags, int32_t n_shards, gdn_dtype dtype, void *o,
+                                 float *h_final, int32_t *plan_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,7 +48,11 @@ SIGNATURES = {
     "gdn_shard_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      _i32, _i32, _i32, _f32, _u32, _i32, ctypes.c_int, _vp, _sz,
                                      _vp, _vp, _vp, _vp]),
+    "gdn_shard_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
+                                             _i32, _i32, _i32, _i32, _f32, _u32, _i32,
+                                             ctypes.c_int, _vp, _vp, _vp, _vp]),
 }
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -256,3 +260,32 @@ def gdn_shard_fwd(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shar
                                 n_shards, _dt(x), _p(workspace), workspace.numel(), _p(o), _p(hf),
                                 _p(plan), _stream()))
     return o, hf, plan
+
+
+def gdn_shard_fwd_noalloc(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shards,
+                          h0=None, scale=None, l2norm=True, out=None, h_final=True):
+    """gdn_shard_fwd for callers that cannot allocate device memory: the
+    library's fixed 32 MiB scratch array replaces the workspace (see
+    gdn_cp.h).  This wrapper itself only allocates the outputs when they are
+    not given.  Returns (o, h_final or None)."""
+    dt = x.dtype
+    for t, n in ((x, "x"), (conv_w, "conv_w"), (conv_b, "conv_b"), (beta, "beta")):
+        _need(t, n, dt)
+    _need(g, "g", torch.float32)
+    _need(h0, "h0", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T = x.shape[0]
+    N = cu_seqlens.numel() - 1
+    scale = dk ** -0.5 if scale is None else scale
+    o = torch.empty((T, Hv, dv), dtype=dt, device=x.device) if out is None else out
+    if isinstance(h_final, torch.Tensor):
+        hf = h_final
+    else:
+        hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=x.device) if h_final else None
+    _check(load().gdn_shard_fwd_noalloc(_p(x.contiguous()), _p(conv_w.contiguous()), _p(conv_b),
+                                        conv_w.shape[1], _p(g.contiguous()), _p(beta.contiguous()),
+                                        _p(None if h0 is None else h0.contiguous()),
+                                        _p(cu_seqlens), N, T, Hk, Hv, dk, dv, float(scale),
+                                        GDN_QK_L2NORM if l2norm else 0, n_shards, _dt(x), _p(o),
+                                        _p(hf), None, _stream()))
+    return o, hf
