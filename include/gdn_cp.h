@@ -80,6 +80,12 @@ const char *gdn_status_string(gdn_status s);
    thread ("" if none). */
 const char *gdn_last_error(void);
 
+/* Number of bounded device-side waits (on the tensor core) that expired on
+   the current device since load or the last reset; such a wait makes its
+   kernel stop early and leave its outputs incomplete.  Synchronises the
+   device (a copy from device memory).  reset != 0 zeroes the counter. */
+gdn_status gdn_device_timeouts(int32_t *count, int reset);
+
 /* ------------------------------------------------------------------------
  * Shard plan  ([FLA-CP] get_cp_cu_seqlens, steps 1-5)
  *

@@ -32,6 +32,7 @@ _vp, _i32, _i64, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_in
 SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_error": (ctypes.c_char_p, []),
+    "gdn_device_timeouts": (ctypes.c_int, [_vp, ctypes.c_int]),
     "gdn_cp_plan_words": (_i64, [_i32, _i32]),
     "gdn_cp_plan": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp]),
     "gdn_conv_silu": (ctypes.c_int, [_vp, _i64, ctypes.c_int, _i32, _i32, _vp, _vp, _i32, _vp,
@@ -121,6 +122,13 @@ def _row_stride(t: torch.Tensor, name: str) -> int:
 # ----------------------------------------------------------------------------
 # entry points
 # ----------------------------------------------------------------------------
+
+def device_timeouts(reset: bool = False) -> int:
+    """Bounded device waits that expired since load / the last reset (syncs)."""
+    n = ctypes.c_int32(0)
+    _check(load().gdn_device_timeouts(ctypes.byref(n), 1 if reset else 0))
+    return n.value
+
 
 def plan_words(num_seqs: int, n_shards: int) -> int:
     return int(load().gdn_cp_plan_words(num_seqs, n_shards))

@@ -17,10 +17,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdncp.so")
-SOURCES = ["api.cu", "plan.cu", "conv.cu", "chunk_bf16.cu", "chunk_f32.cu", "combine.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "conv.cu", "chunk_bf16.cu", "chunk_f32.cu", "chunk_tc.cu",
+           "combine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+              "-I", CSRC]
 
 
 def nvcc() -> str:
@@ -68,7 +69,7 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
                 print(out)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs])
+        run([cc, *ARCH, "-rdc=true", "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
 

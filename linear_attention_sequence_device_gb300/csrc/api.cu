@@ -47,6 +47,7 @@ gdn_status set_smem_attr(const void* func, size_t bytes) {
 }
 
 int chunk_col_tile(gdn_dtype dt, int dk, int dv) {
+    if (chunk_tc_eligible(dt, dk, dv)) return 128;
     if (dt == GDN_F32) return 32;
     int t = dk < dv ? dk : dv;
     return t < 64 ? t : 64;
@@ -80,6 +81,7 @@ static gdn_status check_row(const void* p, int64_t ld, int64_t minld, const char
 
 static gdn_status launch_chunk(const ChunkParams& p, gdn_dtype dt, int src, dim3 grid, cudaStream_t s) {
     if (grid.x == 0) return GDN_OK;
+    if (chunk_tc_eligible(dt, p.dk, p.dv)) return launch_chunk_tc(p, src, grid, s);
     return dt == GDN_BF16 ? launch_chunk_bf16(p, src, grid, s) : launch_chunk_f32(p, src, grid, s);
 }
 
@@ -106,6 +108,20 @@ const char* gdn_status_string(gdn_status s) {
 }
 
 const char* gdn_last_error(void) { return g_err; }
+
+gdn_status gdn_device_timeouts(int32_t* count, int reset) {
+    if (!count) return fail(GDN_ERR_INVALID_ARG, "count is NULL");
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gdn_timeouts, sizeof(int));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading the timeout counter: %s", cudaGetErrorString(e));
+    *count = v;
+    if (reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_gdn_timeouts, &zero, sizeof(int));
+        if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "resetting the timeout counter: %s", cudaGetErrorString(e));
+    }
+    return GDN_OK;
+}
 
 int64_t gdn_cp_plan_words(int32_t num_seqs, int32_t n_shards) {
     if (num_seqs < 1 || n_shards < 1) return 0;

@@ -204,6 +204,10 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
 // launchers (chunk_bf16.cu / chunk_f32.cu)
 gdn_status launch_chunk_bf16(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
 gdn_status launch_chunk_f32(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
+// tcgen05 kernel (chunk_tc.cu): bf16 with d_k = d_v = 128, full-width state tiles
+bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv);
+gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
+extern __device__ int g_gdn_timeouts;
 int chunk_col_tile(gdn_dtype dt, int dk, int dv);
 
 // plan.cu

@@ -1,0 +1,109 @@
+// Blackwell (sm_100 family) tensor-core helpers: tcgen05 MMA with operands
+// in shared memory (128-byte swizzled canonical layouts), accumulators in
+// tensor memory (TMEM), completion through an mbarrier.  Inline PTX only.
+#pragma once
+
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Element offset of (r, c) in a bf16 tile of R rows whose columns are split
+// into atoms of 64 (128 bytes per row): atom a holds columns [64a, 64a+64),
+// row r of an atom sits at 128 r bytes and its 16-byte chunk k at position
+// k ^ (r & 7).  Tiles start on a 1024-byte boundary.
+__host__ __device__ __forceinline__ int sw128(int R, int r, int c) {
+    return (c >> 6) * R * 64 + r * 64 + ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
+}
+// Element offset of 16-byte chunk `ch` (8 elements) of row r.
+__host__ __device__ __forceinline__ int sw128_chunk(int R, int r, int ch) {
+    return (ch >> 3) * R * 64 + r * 64 + (((ch & 7) ^ (r & 7)) << 3);
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets, descriptor version 1 (bits 46-48), 128-byte swizzle (bits 61-63).
+__device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// K-major operand (rows = M or N, K contiguous) of a tile with R rows whose
+// first row is at `base`; descriptor of the 16-wide K step kk.
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int R, int kk) {
+    return desc(base + (uint32_t)((kk >> 2) * R * 128 + (kk & 3) * 32), 16, 1024);
+}
+// MN-major operand stored as [K rows][MN columns] in atoms of 64 columns,
+// atoms `atom_bytes` apart; descriptor of the 16-row K step kk.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, uint32_t atom_bytes, int kk) {
+    return desc(base + (uint32_t)(kk * 16 * 128), atom_bytes, 1024);
+}
+
+// Instruction descriptor, kind::f16 with bf16 inputs and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn, bool neg_a) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((neg_a ? 1u : 0u) << 13) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint64_t* mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+        smem_addr(mbar)));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* mbar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(mbar)), "r"(count));
+    asm volatile("fence.mbarrier_init.release.cluster;");
+}
+// Bounded wait for the mbarrier phase with parity `parity`; true when done.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t limit) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < limit && !done; ++it) {
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_addr(mbar)), "r"(parity));
+    }
+    return done != 0;
+}
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;"); }
+// make generic-proxy shared-memory writes visible to the tensor core
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
+// (lane base + i), columns [col, col + 32).
+__device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace tc
+}  // namespace gdn

@@ -241,3 +241,10 @@ def test_state_combine_vs_oracle(dk, dv, P):
                                    N.astype(np.float32).astype(np.float64),
                                    None if s0 is None else s0.astype(np.float32).astype(np.float64))
         assert rel_l2(f64(got), exp) < 1e-5
+
+
+def test_zz_no_device_wait_expired():
+    """No bounded tensor-core wait expired during the kernel tests above."""
+    import linear_attention_sequence_device_gb300 as g
+    torch.cuda.synchronize()
+    assert g.binding.device_timeouts() == 0
