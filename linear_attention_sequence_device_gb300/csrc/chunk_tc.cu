@@ -4,7 +4,7 @@
 // One CTA (8 warps) runs one job: a token range of one value head with the
 // full 128-column state, chunk after chunk (C = 64).  Every product is
 // written transposed so that its M dimension is 128 (a head dimension):
-//   Gram     [Q;K] K^T                -> [128 x 64]   (rows 0-63: Q K^T, 64-127: K K^T)
+//   Gram     [Q;K] [Q;K]^T             -> [128 x 128]  (Q K^T and K K^T blocks, norms on the diagonal)
 //   W^T      K^T (T diag(beta e^G))^T  -> [128 x 64]
 //   U^T      V^T (T diag(beta))^T      -> [128 x 64]
 //   v_new^T  U^T - S^T W^T             -> [128 x 64]   (negated-A accumulate)
@@ -14,9 +14,12 @@
 // one tile serves as K-major operand of one product and MN-major operand of
 // another.  The fp32 state S^T is held in registers (thread = value row,
 // each warpgroup one half of the key columns) and copied to shared memory
-// in bf16 as the A operand of the next chunk.  The 64x64 UT inverse runs in
-// fp32 on the FFMA pipe.  Waits on the tensor core are bounded: on expiry
-// the kernel counts a timeout, frees its tensor memory and returns.
+// in bf16 as the A operand of the next chunk.  The Gram product is taken as
+// [Q;K][Q;K]^T so that its diagonal gives the q/k L2 norms, which are then
+// folded into scale factors (q and k are never rewritten normalised).  The
+// 64x64 UT inverse runs in place with tf32 mma.sync block products.  Waits
+// on the tensor core are bounded: on expiry the kernel counts a timeout,
+// frees its tensor memory and returns.
 #include "chunk_common.cuh"
 #include "tc_util.cuh"
 
@@ -32,30 +35,28 @@ constexpr uint32_t kSpin = 1u << 24;  // try_wait polls before a wait is declare
 typedef __nv_bfloat16 bf16;
 
 struct SmemTC {
-    bf16 QK[128 * 128];  // rows 0-63: Q (rescaled to scale e^G Q after the Gram), 64-127: K
+    bf16 QK[128 * 128];  // rows 0-63: Q (rescaled to scale e^G Q / |q| after the Gram), 64-127: K
     bf16 V[64 * 128];    // [token][value column]
     bf16 W[64 * 128];    // [token][key column]
     bf16 S[128 * 128];   // S^T [value column][key column], bf16 copy of the state
-    bf16 Aqk[64 * 64];   // scale Q K^T o Gamma (lower incl. diagonal) [i][j]
+    bf16 Aqk[64 * 64];   // scale Q^ K^T o Gamma (lower incl. diagonal) [i][j]
     bf16 Tb[64 * 64];    // T diag(beta)
-    bf16 Tbg[64 * 64];   // T diag(beta e^G)
+    bf16 Tbg[64 * 64];   // T diag(beta e^G / |k|)
     union {
-        struct {
-            float L[64 * LDF];
-            float Tm[64 * LDF];
-        } solve;
+        float LT[64 * LDF];      // L, then T = (I + L)^-1 in place
         struct {
             bf16 VN[128 * 64];   // v_new^T [value column][token]
-            bf16 VNd[128 * 64];  // (v_new o e^{G_last - G})^T
+            bf16 VNd[128 * 64];  // (v_new o e^{G_last - G} / |k|)^T
         } vn;
     } u;
-    float X[3 * 16 * 17];
     float g[64], beta[64], G[64], eG[64], eGl[64];
+    float rn[128];       // 1/|q_i| (rows 0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
     uint64_t mbar;
     uint32_t tmem_slot;
 };
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
+constexpr uint32_t ID_N128 = tc::idesc_bf16(128, 128, false, false, false);
 constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
 constexpr uint32_t ID_N64_NEG = tc::idesc_bf16(128, 64, false, false, true);
 constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_U = tmem + 128, T_O = tmem + 192, T_DS = tmem + 256;
+    const uint32_t T_GRAM = tmem, T_W = tmem + 128, T_U = tmem + 192, T_O = tmem + 256, T_DS = tmem + 320;
     const uint32_t aQK = tc::smem_addr(sm.QK), aK = aQK + 64 * 128, aV = tc::smem_addr(sm.V);
     const uint32_t aW = tc::smem_addr(sm.W), aS = tc::smem_addr(sm.S), aA = tc::smem_addr(sm.Aqk);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
@@ -146,61 +147,47 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         }
         cp_async_wait_all();
         __syncthreads();
-        if (l2) {  // q, k <- x * rsqrt(|x|^2 + 1e-6): 16 lanes per row, one 16-byte chunk each
-            const int sub = lane >> 4, c8 = lane & 15;
-            for (int r = warp * 2 + sub; r < 128; r += 16) {
-                uint4* ptr = reinterpret_cast<uint4*>(&sm.QK[tc::sw128_chunk(128, r, c8)]);
-                uint4 raw = *ptr;
-                __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                float f[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 t2 = __bfloat1622float2(h[i]);
-                    f[2 * i] = t2.x;
-                    f[2 * i + 1] = t2.y;
-                }
-                float ss = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
-#pragma unroll
-                for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                const float rn = rsqrtf(ss + 1e-6f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] *= rn;
-                *ptr = pack8(f);
-            }
-        }
         if (warp == 0) gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
         tc::fence_async_smem();
         __syncthreads();
 
-        // ---- Gram products: [Q;K] K^T ----
+        // ---- Gram products: [Q;K] [Q;K]^T (the diagonal gives the L2 norms) ----
         if (tid == 0) {
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma(T_GRAM, tc::desc_k(aQK, 128, kk), tc::desc_k(aK, 128, kk), ID_N64, kk > 0);
+                tc::mma(T_GRAM, tc::desc_k(aQK, 128, kk), tc::desc_k(aQK, 128, kk), ID_N128, kk > 0);
             tc::commit(&sm.mbar);
         }
         if (!(alive = wait_mma())) break;
+        if (wg == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the Gram diagonal (x . x for row x)
+            float dg[32];
+            tc::ld32(T_GRAM + lb + (row & ~31), dg);
+            float d = dg[0];
+#pragma unroll
+            for (int c = 1; c < 32; ++c) d = (c == lane) ? dg[c] : d;
+            sm.rn[row] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
+        }
+        __syncthreads();
         {
             float gv[32];
-            tc::ld32(T_GRAM + lb + 32 * wg, gv);
+            tc::ld32(T_GRAM + lb + 64 + 32 * wg, gv);
             const int i = row & 63;
             const float Gi = sm.G[i];
-            if (row < 64) {  // A = scale Q K^T o Gamma, lower triangle incl. diagonal
+            if (row < 64) {  // A = scale Q^ K^T o Gamma, lower triangle incl. diagonal
+                const float fi = p.scale * sm.rn[i];
                 float a[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int j = 32 * wg + c;
-                    a[c] = (j <= i) ? p.scale * gv[c] * __expf(Gi - sm.G[j]) : 0.f;
+                    a[c] = (j <= i) ? fi * sm.rn[64 + j] * gv[c] * __expf(Gi - sm.G[j]) : 0.f;
                 }
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8)
                     *reinterpret_cast<uint4*>(&sm.Aqk[tc::sw128_chunk(64, i, 4 * wg + c8)]) = pack8(&a[8 * c8]);
-            } else {         // L = beta_i K K^T o Gamma, strictly lower
-                const float bi = sm.beta[i];
-                float* Lrow = sm.u.solve.L + i * LDF + 32 * wg;
+            } else {         // L = beta_i K^ K^T o Gamma, strictly lower
+                const float fi = sm.beta[i] * sm.rn[row];
+                float* Lrow = sm.u.LT + i * LDF + 32 * wg;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     float4 l4;
@@ -208,7 +195,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int j = 32 * wg + c + e;
-                        lv[e] = (j < i) ? bi * gv[c + e] * __expf(Gi - sm.G[j]) : 0.f;
+                        lv[e] = (j < i) ? fi * sm.rn[64 + j] * gv[c + e] * __expf(Gi - sm.G[j]) : 0.f;
                     }
                     *reinterpret_cast<float4*>(Lrow + c) = l4;
                 }
@@ -216,17 +203,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         }
         tc::fence_before();
         __syncthreads();
-        unit_lower_inverse64<NT, LDF>(sm.u.solve.L, sm.u.solve.Tm, sm.X);
-        // ---- T diag(beta), T diag(beta e^G) in bf16; Q <- scale e^G Q ----
+        unit_lower_inverse64_inplace<LDF>(sm.u.LT, tid, [] { __syncthreads(); });
+        // ---- T diag(beta), T diag(beta e^G / |k|) in bf16; Q <- scale e^G Q / |q| ----
         for (int e = tid; e < 64 * 8; e += NT) {
             const int i = e >> 3, c8 = e & 7;
-            const float* trow = sm.u.solve.Tm + i * LDF + 8 * c8;
+            const float* trow = sm.u.LT + i * LDF + 8 * c8;
             float tbv[8], tbg[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int j = 8 * c8 + c;
                 tbv[c] = trow[c] * sm.beta[j];
-                tbg[c] = tbv[c] * sm.eG[j];
+                tbg[c] = tbv[c] * sm.eG[j] * sm.rn[64 + j];
             }
             *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
             *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
@@ -237,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 uint4* ptr = reinterpret_cast<uint4*>(&sm.QK[tc::sw128_chunk(128, r, c8)]);
                 uint4 raw = *ptr;
                 __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                const float f = p.scale * sm.eG[r];
+                const float f = p.scale * sm.eG[r] * sm.rn[r];
                 float x[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -266,8 +253,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         {  // W [token][key column] <- W^T rows (thread = key column)
             float wv[32];
             tc::ld32(T_W + lb + 32 * wg, wv);
+            bf16* wb = sm.W + (row >> 6) * 64 * 64 + 32 * wg * 64 + (row & 7);
+            const int dch = (row & 63) >> 3;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sm.W[tc::sw128(64, 32 * wg + c, row)] = __float2bfloat16_rn(wv[c]);
+            for (int c = 0; c < 32; ++c) wb[64 * c + ((dch ^ (c & 7)) << 3)] = __float2bfloat16_rn(wv[c]);
         }
         tc::fence_before();
         tc::fence_async_smem();
@@ -290,7 +279,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             for (int c8 = 0; c8 < 4; ++c8) {
                 float d8[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) d8[c] = vv[8 * c8 + c] * sm.eGl[32 * wg + 8 * c8 + c];
+                for (int c = 0; c < 8; ++c) {
+                    const int j = 32 * wg + 8 * c8 + c;
+                    d8[c] = vv[8 * c8 + c] * sm.eGl[j] * sm.rn[64 + j];
+                }
                 *reinterpret_cast<uint4*>(&sm.u.vn.VN[tc::sw128_chunk(128, row, 4 * wg + c8)]) = pack8(&vv[8 * c8]);
                 *reinterpret_cast<uint4*>(&sm.u.vn.VNd[tc::sw128_chunk(128, row, 4 * wg + c8)]) = pack8(d8);
             }
@@ -319,11 +311,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         if (job.write_o) {
             float ov[32];
             tc::ld32(T_O + lb + 32 * wg, ov);
+            bf16* ob = o + ((int64_t)(tb + 32 * wg) * p.Hv + hv) * 128 + row;
+            const int64_t ostride = (int64_t)p.Hv * 128;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int i = 32 * wg + c;
-                if (i < valid) o[((int64_t)(tb + i) * p.Hv + hv) * 128 + row] = __float2bfloat16_rn(ov[c]);
-            }
+            for (int c = 0; c < 32; ++c)
+                if (32 * wg + c < valid) ob[c * ostride] = __float2bfloat16_rn(ov[c]);
         }
         {  // S <- e^{G_last} S + dS
             const float a = sm.eG[63];
