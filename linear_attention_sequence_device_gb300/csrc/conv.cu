@@ -28,6 +28,19 @@ struct ConvParams {
 
 template <typename T> struct Vec8;
 template <> struct Vec8<__nv_bfloat16> {
+    struct Raw { uint4 v; };  // eight bf16 as loaded
+    static __device__ __forceinline__ Raw load_raw(const __nv_bfloat16* p) {
+        return Raw{*reinterpret_cast<const uint4*>(p)};
+    }
+    static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
     static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* f) {
         uint4 raw = *reinterpret_cast<const uint4*>(p);
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -47,6 +60,14 @@ template <> struct Vec8<__nv_bfloat16> {
     }
 };
 template <> struct Vec8<float> {
+    struct Raw { float4 a, b; };
+    static __device__ __forceinline__ Raw load_raw(const float* p) {
+        return Raw{reinterpret_cast<const float4*>(p)[0], reinterpret_cast<const float4*>(p)[1]};
+    }
+    static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
+        f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+        f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
+    }
     static __device__ __forceinline__ void load(const float* p, float* f) {
         float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
@@ -59,7 +80,7 @@ template <> struct Vec8<float> {
 };
 
 template <typename T, int KC>
-__global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(NT, 3) conv_kernel(const ConvParams p) {
     const int c0 = (blockIdx.x * NT + threadIdx.x) * 8;
     if (c0 >= p.C) return;
     int part, rs;
@@ -126,34 +147,46 @@ __global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
             for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
         }
     }
-    for (int t = lt0; t < lt1; ++t) {
-        while (t == next) {  // a new sequence starts: no history
+    // rows in groups of RB: all loads of a group are issued before any compute,
+    // so each thread keeps RB 16-byte loads in flight
+    constexpr int RB = 8;
+    for (int t0 = lt0; t0 < lt1; t0 += RB) {
+        typename Vec8<T>::Raw raw[RB];
 #pragma unroll
-            for (int j = 0; j < KC - 1; ++j)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
-            ++seg;
-            next = seg + 1 <= nloc ? lc[seg + 1] : part;
+        for (int u = 0; u < RB; ++u) {
+            if (t0 + u < lt1) raw[u] = Vec8<T>::load_raw(x + (int64_t)(rs + t0 + u) * p.ldx + c0);
         }
-        float cur[8];
-        Vec8<T>::load(x + (int64_t)(rs + t) * p.ldx + c0, cur);
-        float out[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            float acc = br[c];
+        for (int u = 0; u < RB; ++u) {
+            const int t = t0 + u;
+            if (t >= lt1) break;
+            while (t == next) {  // a new sequence starts: no history
 #pragma unroll
-            for (int j = 0; j < KC - 1; ++j) acc = fmaf(wr[j][c], win[j][c], acc);
-            acc = fmaf(wr[KC - 1][c], cur[c], acc);
-            out[c] = acc / (1.f + expf(-acc));
-        }
-        Vec8<T>::store(y + (int64_t)(rs + t) * p.ldy + c0, out);
+                for (int j = 0; j < KC - 1; ++j)
 #pragma unroll
-        for (int j = 0; j + 1 < KC - 1; ++j)
+                    for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
+                ++seg;
+                next = seg + 1 <= nloc ? lc[seg + 1] : part;
+            }
+            float cur[8], out[8];
+            Vec8<T>::unpack(raw[u], cur);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) win[j][c] = win[j + 1][c];
-        if (KC > 1) {
+            for (int c = 0; c < 8; ++c) {
+                float acc = br[c];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) win[KC > 1 ? KC - 2 : 0][c] = cur[c];
+                for (int j = 0; j < KC - 1; ++j) acc = fmaf(wr[j][c], win[j][c], acc);
+                acc = fmaf(wr[KC - 1][c], cur[c], acc);
+                out[c] = acc / (1.f + expf(-acc));
+            }
+            Vec8<T>::store(y + (int64_t)(rs + t) * p.ldy + c0, out);
+#pragma unroll
+            for (int j = 0; j + 1 < KC - 1; ++j)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) win[j][c] = win[j + 1][c];
+            if (KC > 1) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) win[KC > 1 ? KC - 2 : 0][c] = cur[c];
+            }
         }
     }
 }
