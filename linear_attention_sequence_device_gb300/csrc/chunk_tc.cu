@@ -1,25 +1,31 @@
 // bf16 chunk kernel for d_k = d_v = 128 on the 5th-generation tensor cores
 // (tcgen05.mma, accumulators in tensor memory).
 //
-// One CTA (8 warps) runs one job: a token range of one value head with the
-// full 128-column state, chunk after chunk (C = 64).  Every product is
-// written transposed so that its M dimension is 128 (a head dimension):
-//   Gram     [Q;K] [Q;K]^T             -> [128 x 128]  (Q K^T and K K^T blocks, norms on the diagonal)
-//   W^T      K^T (T diag(beta e^G))^T  -> [128 x 64]
-//   U^T      V^T (T diag(beta))^T      -> [128 x 64]
-//   v_new^T  U^T - S^T W^T             -> [128 x 64]   (negated-A accumulate)
-//   o^T      S^T Q~^T + v_new^T A^T    -> [128 x 64]   (Q~ = scale e^G Q)
-//   dS^T     (v_new o e^{G_last-G})^T K -> [128 x 128]
+// One CTA runs one job: a token range of one value head with the full
+// 128-column state, chunk after chunk (C = 64).  Every product is written
+// transposed so that its M dimension is 128 (a head dimension):
+//   Gram     [Q;K] [Q;K]^T              -> [128 x 128] (Q K^T and K K^T blocks, norms on the diagonal)
+//   W^T      K^T (T diag(beta e^G/|k|))^T -> [128 x 64]
+//   U^T      V^T (T diag(beta))^T        -> [128 x 64]
+//   v_new^T  U^T - S^T W^T               -> [128 x 64]   (negated-A accumulate)
+//   o^T      S^T Q~^T + v_new^T A^T      -> [128 x 64]   (Q~ = scale e^G Q / |q|)
+//   dS^T     (v_new o e^{G_last-G}/|k|)^T K -> [128 x 128]
 // Operands sit in shared memory in the 128-byte-swizzled canonical layout;
 // one tile serves as K-major operand of one product and MN-major operand of
-// another.  The fp32 state S^T is held in registers (thread = value row,
-// each warpgroup one half of the key columns) and copied to shared memory
-// in bf16 as the A operand of the next chunk.  The Gram product is taken as
-// [Q;K][Q;K]^T so that its diagonal gives the q/k L2 norms, which are then
-// folded into scale factors (q and k are never rewritten normalised).  The
-// 64x64 UT inverse runs in place with tf32 mma.sync block products.  Waits
-// on the tensor core are bounded: on expiry the kernel counts a timeout,
-// frees its tensor memory and returns.
+// another.
+//
+// Two warpgroups work on different chunks at once:
+//   producer (warps 0-3): everything that does not depend on the state --
+//     loads, the Gram product, the L2 norms (from the Gram diagonal, folded
+//     into scale factors), A and L, the in-place UT inverse (tf32 mma.sync
+//     block products), W and U -- for chunk c+1 while
+//   consumer (warps 4-7) runs the state chain of chunk c: v_new, then o and
+//     dS, then S <- e^{G_last} S + dS with the fp32 state in registers
+//     (thread = value row) and a bf16 copy in shared memory as the A operand.
+// Q/K, A, the per-chunk scale factors and U (in tensor memory) are double
+// buffered ("slots"); W is single buffered with its own release barrier.
+// Every wait is bounded: on expiry the kernel counts a timeout, both groups
+// leave their loops, and the tensor memory is freed.
 #include "chunk_common.cuh"
 #include "tc_util.cuh"
 
@@ -31,28 +37,36 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int LDF = 68;
-constexpr uint32_t kSpin = 1u << 24;  // try_wait polls before a wait is declared stuck
+constexpr uint32_t kSpin = 1u << 20;  // try_wait polls before a wait is declared stuck
+constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two warpgroups
 typedef __nv_bfloat16 bf16;
 
-struct SmemTC {
-    bf16 QK[128 * 128];  // rows 0-63: Q (rescaled to scale e^G Q / |q| after the Gram), 64-127: K
-    bf16 V[64 * 128];    // [token][value column]
-    bf16 W[64 * 128];    // [token][key column]
-    bf16 S[128 * 128];   // S^T [value column][key column], bf16 copy of the state
-    bf16 Aqk[64 * 64];   // scale Q^ K^T o Gamma (lower incl. diagonal) [i][j]
-    bf16 Tb[64 * 64];    // T diag(beta)
-    bf16 Tbg[64 * 64];   // T diag(beta e^G / |k|)
-    union {
-        float LT[64 * LDF];      // L, then T = (I + L)^-1 in place
-        struct {
-            bf16 VN[128 * 64];   // v_new^T [value column][token]
-            bf16 VNd[128 * 64];  // (v_new o e^{G_last - G} / |k|)^T
-        } vn;
-    } u;
+struct SlotSmall {
+    float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of dS
+    float eglast;   // e^{G_last}
+    int tb, valid;  // first token and valid rows of the chunk
+    int pad;
+};
+
+struct SmemWS {
+    bf16 QK[2][128 * 128];  // per slot: rows 0-63 Q (then Q~), rows 64-127 K
+    bf16 Aqk[2][64 * 64];   // per slot: scale Q^ K^T o Gamma, lower incl. diagonal
+    bf16 W[64 * 128];       // [token][key column]
+    bf16 V[64 * 128];       // [token][value column]
+    bf16 S[128 * 128];      // S^T [value column][key column] (bf16 copy of the state)
+    bf16 VN[128 * 64];      // v_new^T [value column][token]
+    bf16 VNd[128 * 64];     // v_new^T scaled by the dS token factor
+    bf16 Tb[64 * 64];       // T diag(beta)
+    bf16 Tbg[64 * 64];      // T diag(beta e^G / |k|)
+    float LT[64 * LDF];     // L, then T = (I + L)^-1 in place
+    SlotSmall slot[2];
     float g[64], beta[64], G[64], eG[64], eGl[64];
-    float rn[128];       // 1/|q_i| (rows 0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
-    uint64_t mbar;
+    float rn[128];          // 1/|q_i| (0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
+    uint64_t mbar_p, mbar_s;  // tensor-core completion, producer / consumer
+    uint64_t full[2], empty[2], wfree;
     uint32_t tmem_slot;
+    int lpt_len[kMaxLptItems];
+    int lpt_pick;
 };
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
@@ -71,275 +85,337 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src) {
     extern __shared__ unsigned char smem_raw[];
-    SmemTC& sm = *reinterpret_cast<SmemTC*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
+    SmemWS& sm = *reinterpret_cast<SmemWS*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
     ChunkJob job;
-    if (!make_job(p, src, job)) return;
+    int bx, by, bz;
+    lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
+    if (!make_job(p, src, job, bx, by, bz)) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2;                // which half of the columns this thread handles
-    const int row = (warp & 3) * 32 + lane;  // tensor-memory lane = row of every [128 x N] product
+    const bool producer = warp < 4;
+    const int gt = tid & 127;  // thread index in its warpgroup == tensor-memory lane
+    const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const int hv = job.hv, hk = hv / (p.Hv / p.Hk);
-    const bf16* __restrict__ q = static_cast<const bf16*>(p.q);
-    const bf16* __restrict__ k = static_cast<const bf16*>(p.k);
-    const bf16* __restrict__ v = static_cast<const bf16*>(p.v);
-    const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
-    bf16* __restrict__ o = static_cast<bf16*>(p.o);
-    const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
 
-    if (tid == 0) tc::mbar_init(&sm.mbar, 1);
+    if (tid == 0) {
+        tc::mbar_init(&sm.mbar_p, 1);
+        tc::mbar_init(&sm.mbar_s, 1);
+        tc::mbar_init(&sm.full[0], 1);
+        tc::mbar_init(&sm.full[1], 1);
+        tc::mbar_init(&sm.empty[0], 1);
+        tc::mbar_init(&sm.empty[1], 1);
+        tc::mbar_init(&sm.wfree, 1);
+    }
     if (warp == 0) tc::tmem_alloc(&sm.tmem_slot, 512);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
-    const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t T_GRAM = tmem, T_W = tmem + 128, T_U = tmem + 192, T_O = tmem + 256, T_DS = tmem + 320;
-    const uint32_t aQK = tc::smem_addr(sm.QK), aK = aQK + 64 * 128, aV = tc::smem_addr(sm.V);
-    const uint32_t aW = tc::smem_addr(sm.W), aS = tc::smem_addr(sm.S), aA = tc::smem_addr(sm.Aqk);
+    const uint32_t T_GRAM = tmem, T_W = tmem + 128, T_O = tmem + 320, T_DS = tmem + 384;
+    const uint32_t T_U[2] = {tmem + 192, tmem + 256};
+    const uint32_t aQK[2] = {tc::smem_addr(sm.QK[0]), tc::smem_addr(sm.QK[1])};
+    const uint32_t aA[2] = {tc::smem_addr(sm.Aqk[0]), tc::smem_addr(sm.Aqk[1])};
+    const uint32_t aW = tc::smem_addr(sm.W), aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S);
+    const uint32_t aVN = tc::smem_addr(sm.VN), aVNd = tc::smem_addr(sm.VNd);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
-    const uint32_t aVN = tc::smem_addr(sm.u.vn.VN), aVNd = tc::smem_addr(sm.u.vn.VNd);
-    uint32_t phase = 0;
-    bool alive = true;
-
-    // fp32 state: S^T[row][64 wg + c]
-    float Sr[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c) {
-        const int d = 64 * wg + c;
-        float s0 = 0.f;
-        if (job.identity_init) s0 = (d == job.col0 + row) ? 1.f : 0.f;
-        else if (job.init) s0 = job.init[(int64_t)d * job.init_ld + row];
-        Sr[c] = s0;
-    }
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * wg + c8)]) = pack8(&Sr[8 * c8]);
-
-    auto wait_mma = [&]() -> bool {
-        const bool done = tc::mbar_wait(&sm.mbar, phase, kSpin);
-        phase ^= 1u;
-        const bool all = __syncthreads_and(done) != 0;
-        if (!all && tid == 0) atomicAdd(&g_gdn_timeouts, 1);
-        tc::fence_after();
-        return all;
-    };
-
     const int nch = (job.t1 - job.t0 + 63) / 64;
-    for (int ch = 0; ch < nch && alive; ++ch) {
-        const int tb = job.t0 + ch * 64;
-        const int valid = min(64, job.t1 - tb);
-        __syncthreads();
-        // ---- load the chunk; rows past the segment end read as zero ----
-        for (int e = tid; e < 64 * 16; e += NT) {
-            const int r = e >> 4, c8 = e & 15;
-            const int64_t t = tb + (r < valid ? r : 0);
-            const int nb = r < valid ? 16 : 0;
-            cp_async16(&sm.QK[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
-            cp_async16(&sm.QK[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
-            if (!job.value_zero)
-                cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8, nb);
-        }
-        cp_async_commit();
-        if (tid < 64) {
-            const int64_t t = tb + tid;
-            sm.g[tid] = tid < valid ? __ldg(p.g + t * p.Hv + hv) : 0.f;
-            sm.beta[tid] = tid < valid ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
-        }
-        cp_async_wait_all();
-        __syncthreads();
-        if (warp == 0) gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
-        tc::fence_async_smem();
-        __syncthreads();
+    bool ok = true;
+    // base descriptors; a K step adds a constant to the start-address field
+    const uint64_t dQK[2] = {tc::desc(aQK[0], 16, 1024), tc::desc(aQK[1], 16, 1024)};
+    const uint64_t dKmn[2] = {tc::desc(aQK[0] + 64 * 128, 128 * 128, 1024), tc::desc(aQK[1] + 64 * 128, 128 * 128, 1024)};
+    const uint64_t dA[2] = {tc::desc(aA[0], 16, 1024), tc::desc(aA[1], 16, 1024)};
+    const uint64_t dW = tc::desc(aW, 16, 1024), dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024);
+    const uint64_t dVN = tc::desc(aVN, 16, 1024), dVNd = tc::desc(aVNd, 16, 1024);
+    const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
 
-        // ---- Gram products: [Q;K] [Q;K]^T (the diagonal gives the L2 norms) ----
-        if (tid == 0) {
+    if (producer) {
+        // ====================== producer warpgroup ======================
+        const bf16* __restrict__ q = static_cast<const bf16*>(p.q);
+        const bf16* __restrict__ k = static_cast<const bf16*>(p.k);
+        const bf16* __restrict__ v = static_cast<const bf16*>(p.v);
+        const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
+        const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
+        uint32_t ph = 0;
+        auto wait_mma = [&]() -> bool {
+            const bool done = tc::mbar_wait(&sm.mbar_p, ph, kSpin);
+            ph ^= 1u;
+            const bool all = tc::bar_and(BAR_P, 128, done);
             tc::fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma(T_GRAM, tc::desc_k(aQK, 128, kk), tc::desc_k(aQK, 128, kk), ID_N128, kk > 0);
-            tc::commit(&sm.mbar);
-        }
-        if (!(alive = wait_mma())) break;
-        if (wg == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the Gram diagonal (x . x for row x)
-            float dg[32];
-            tc::ld32(T_GRAM + lb + (row & ~31), dg);
-            float d = dg[0];
-#pragma unroll
-            for (int c = 1; c < 32; ++c) d = (c == lane) ? dg[c] : d;
-            sm.rn[row] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
-        }
-        __syncthreads();
-        {
-            float gv[32];
-            tc::ld32(T_GRAM + lb + 64 + 32 * wg, gv);
-            const int i = row & 63;
-            const float Gi = sm.G[i];
-            if (row < 64) {  // A = scale Q^ K^T o Gamma, lower triangle incl. diagonal
-                const float fi = p.scale * sm.rn[i];
-                float a[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int j = 32 * wg + c;
-                    a[c] = (j <= i) ? fi * sm.rn[64 + j] * gv[c] * __expf(Gi - sm.G[j]) : 0.f;
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4*>(&sm.Aqk[tc::sw128_chunk(64, i, 4 * wg + c8)]) = pack8(&a[8 * c8]);
-            } else {         // L = beta_i K^ K^T o Gamma, strictly lower
-                const float fi = sm.beta[i] * sm.rn[row];
-                float* Lrow = sm.u.LT + i * LDF + 32 * wg;
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    float4 l4;
-                    float* lv = &l4.x;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 32 * wg + c + e;
-                        lv[e] = (j < i) ? fi * sm.rn[64 + j] * gv[c + e] * __expf(Gi - sm.G[j]) : 0.f;
-                    }
-                    *reinterpret_cast<float4*>(Lrow + c) = l4;
-                }
-            }
-        }
-        tc::fence_before();
-        __syncthreads();
-        unit_lower_inverse64_inplace<LDF>(sm.u.LT, tid, [] { __syncthreads(); });
-        // ---- T diag(beta), T diag(beta e^G / |k|) in bf16; Q <- scale e^G Q / |q| ----
-        for (int e = tid; e < 64 * 8; e += NT) {
-            const int i = e >> 3, c8 = e & 7;
-            const float* trow = sm.u.LT + i * LDF + 8 * c8;
-            float tbv[8], tbg[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int j = 8 * c8 + c;
-                tbv[c] = trow[c] * sm.beta[j];
-                tbg[c] = tbv[c] * sm.eG[j] * sm.rn[64 + j];
-            }
-            *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
-            *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
-        }
-        if (job.write_o) {
-            for (int e = tid; e < 64 * 16; e += NT) {
+            return all;
+        };
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            const int tb = job.t0 + 64 * c;
+            const int valid = min(64, job.t1 - tb);
+            if (c >= 2 && !(ok = tc::bar_and(BAR_P, 128, tc::mbar_wait(&sm.empty[s], ((c >> 1) - 1) & 1, kSpin))))
+                break;
+            tc::fence_after();
+            bf16* QKs = sm.QK[s];
+            for (int e = gt; e < 64 * 16; e += 128) {
                 const int r = e >> 4, c8 = e & 15;
-                uint4* ptr = reinterpret_cast<uint4*>(&sm.QK[tc::sw128_chunk(128, r, c8)]);
-                uint4 raw = *ptr;
-                __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                const float f = p.scale * sm.eG[r] * sm.rn[r];
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 t2 = __bfloat1622float2(h[i]);
-                    x[2 * i] = t2.x * f;
-                    x[2 * i + 1] = t2.y * f;
-                }
-                *ptr = pack8(x);
-            }
-        }
-        tc::fence_async_smem();
-        __syncthreads();
-
-        // ---- W^T = K^T Tbg^T, U^T = V^T Tb^T ----
-        if (tid == 0) {
-            tc::fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                tc::mma(T_W, tc::desc_mn(aK, 128 * 128, kk), tc::desc_k(aTbg, 64, kk), ID_N64_AMN, kk > 0);
+                const int64_t t = tb + (r < valid ? r : 0);
+                const int nb = r < valid ? 16 : 0;
+                cp_async16(&QKs[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
+                cp_async16(&QKs[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
                 if (!job.value_zero)
-                    tc::mma(T_U, tc::desc_mn(aV, 64 * 128, kk), tc::desc_k(aTb, 64, kk), ID_N64_AMN, kk > 0);
+                    cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8, nb);
             }
-            tc::commit(&sm.mbar);
-        }
-        if (!(alive = wait_mma())) break;
-        {  // W [token][key column] <- W^T rows (thread = key column)
-            float wv[32];
-            tc::ld32(T_W + lb + 32 * wg, wv);
-            bf16* wb = sm.W + (row >> 6) * 64 * 64 + 32 * wg * 64 + (row & 7);
-            const int dch = (row & 63) >> 3;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) wb[64 * c + ((dch ^ (c & 7)) << 3)] = __float2bfloat16_rn(wv[c]);
-        }
-        tc::fence_before();
-        tc::fence_async_smem();
-        __syncthreads();
-
-        // ---- v_new^T = U^T - S^T W^T ----
-        if (tid == 0) {
-            tc::fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma(T_U, tc::desc_k(aS, 128, kk), tc::desc_k(aW, 64, kk), ID_N64_NEG,
-                        (!job.value_zero) || kk > 0);
-            tc::commit(&sm.mbar);
-        }
-        if (!(alive = wait_mma())) break;
-        {
-            float vv[32];
-            tc::ld32(T_U + lb + 32 * wg, vv);
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float d8[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int j = 32 * wg + 8 * c8 + c;
-                    d8[c] = vv[8 * c8 + c] * sm.eGl[j] * sm.rn[64 + j];
-                }
-                *reinterpret_cast<uint4*>(&sm.u.vn.VN[tc::sw128_chunk(128, row, 4 * wg + c8)]) = pack8(&vv[8 * c8]);
-                *reinterpret_cast<uint4*>(&sm.u.vn.VNd[tc::sw128_chunk(128, row, 4 * wg + c8)]) = pack8(d8);
+            cp_async_commit();
+            if (gt < 64) {
+                const int64_t t = tb + gt;
+                sm.g[gt] = gt < valid ? __ldg(p.g + t * p.Hv + hv) : 0.f;
+                sm.beta[gt] = gt < valid ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
             }
-        }
-        tc::fence_before();
-        tc::fence_async_smem();
-        __syncthreads();
-
-        // ---- o^T = S^T Q~^T + v_new^T A^T ; dS^T = VNd K ----
-        if (tid == 0) {
-            tc::fence_after();
-            if (job.write_o) {
+            cp_async_wait_all();
+            tc::fence_async_smem();
+            tc::bar_sync(BAR_P, 128);
+            // Gram [Q;K][Q;K]^T; the gate prefix meanwhile
+            if (gt == 0) {
+                tc::fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_O, tc::desc_k(aS, 128, kk), tc::desc_k(aQK, 128, kk), ID_N64, kk > 0);
+                    tc::mma(T_GRAM, dQK[s] + tc::koff(128, kk), dQK[s] + tc::koff(128, kk), ID_N128, kk > 0);
+                tc::commit(&sm.mbar_p);
+            }
+            if (warp == 0) gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
+            if (!(ok = wait_mma())) break;
+            {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
+                float dg[32];
+                tc::ld32(T_GRAM + lb + (gt & ~31), dg);
+                float d = dg[0];
+#pragma unroll
+                for (int c2 = 1; c2 < 32; ++c2) d = (c2 == lane) ? dg[c2] : d;
+                sm.rn[gt] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
+            }
+            tc::bar_sync(BAR_P, 128);
+            {  // A (rows 0-63) and L (rows 64-127) from the Q K^T / K K^T blocks
+                const int i = gt & 63;
+                const float Gi = sm.G[i];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float gv[32];
+                    tc::ld32(T_GRAM + lb + 64 + 32 * half, gv);
+                    if (gt < 64) {
+                        const float fi = p.scale * sm.rn[i];
+                        float a[32];
+#pragma unroll
+                        for (int c2 = 0; c2 < 32; ++c2) {
+                            const int j = 32 * half + c2;
+                            a[c2] = (j <= i) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
+                        }
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            *reinterpret_cast<uint4*>(&sm.Aqk[s][tc::sw128_chunk(64, i, 4 * half + c8)]) =
+                                pack8(&a[8 * c8]);
+                    } else {
+                        const float fi = sm.beta[i] * sm.rn[gt];
+                        float* Lrow = sm.LT + i * LDF + 32 * half;
+#pragma unroll
+                        for (int c2 = 0; c2 < 32; c2 += 4) {
+                            float4 l4;
+                            float* lv = &l4.x;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = 32 * half + c2 + e;
+                                lv[e] = (j < i) ? fi * sm.rn[64 + j] * gv[c2 + e] * __expf(Gi - sm.G[j]) : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(Lrow + c2) = l4;
+                        }
+                    }
+                }
+            }
+            tc::fence_before();
+            tc::bar_sync(BAR_P, 128);
+            unit_lower_inverse64_inplace<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, 128); });
+            // T diag(beta), T diag(beta e^G / |k|); Q~ = scale e^G Q / |q|; slot factors
+            for (int e = gt; e < 64 * 8; e += 128) {
+                const int i = e >> 3, c8 = e & 7;
+                const float* trow = sm.LT + i * LDF + 8 * c8;
+                float tbv[8], tbg[8];
+#pragma unroll
+                for (int c2 = 0; c2 < 8; ++c2) {
+                    const int j = 8 * c8 + c2;
+                    tbv[c2] = trow[c2] * sm.beta[j];
+                    tbg[c2] = tbv[c2] * sm.eG[j] * sm.rn[64 + j];
+                }
+                *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
+                *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
+            }
+            if (job.write_o) {
+                for (int e = gt; e < 64 * 16; e += 128) {
+                    const int r = e >> 4, c8 = e & 15;
+                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
+                    uint4 raw = *ptr;
+                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+                    const float f = p.scale * sm.eG[r] * sm.rn[r];
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 t2 = __bfloat1622float2(h[i]);
+                        x[2 * i] = t2.x * f;
+                        x[2 * i + 1] = t2.y * f;
+                    }
+                    *ptr = pack8(x);
+                }
+            }
+            if (gt < 64) sm.slot[s].fac[gt] = sm.eGl[gt] * sm.rn[64 + gt];
+            if (gt == 0) {
+                sm.slot[s].eglast = sm.eG[63];
+                sm.slot[s].tb = tb;
+                sm.slot[s].valid = valid;
+            }
+            tc::fence_async_smem();
+            tc::bar_sync(BAR_P, 128);
+            // W^T = K^T Tbg^T, U^T = V^T Tb^T
+            if (gt == 0) {
+                tc::fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    tc::mma(T_W, dKmn[s] + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                    if (!job.value_zero)
+                        tc::mma(T_U[s], dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                }
+                tc::commit(&sm.mbar_p);
+            }
+            if (!(ok = wait_mma())) break;
+            // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
+            if (c >= 1 && !(ok = tc::bar_and(BAR_P, 128, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
+            {
+                float wv[32];
+                const int dch = (gt & 63) >> 3;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tc::ld32(T_W + lb + 32 * half, wv);
+                    bf16* wb = sm.W + (gt >> 6) * 64 * 64 + 32 * half * 64 + (gt & 7);
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::bar_sync(BAR_P, 128);
+            if (gt == 0) tc::mbar_arrive(&sm.full[s]);
+        }
+    } else {
+        // ====================== consumer warpgroup ======================
+        bf16* __restrict__ o = static_cast<bf16*>(p.o);
+        uint32_t ph = 0;
+        auto wait_mma = [&]() -> bool {
+            const bool done = tc::mbar_wait(&sm.mbar_s, ph, kSpin);
+            ph ^= 1u;
+            const bool all = tc::bar_and(BAR_S, 128, done);
+            tc::fence_after();
+            return all;
+        };
+        // state S^T row gt (value column gt), all 128 key columns
+        float Sr[128];
+#pragma unroll
+        for (int d = 0; d < 128; ++d) {
+            float s0 = 0.f;
+            if (job.identity_init) s0 = (d == job.col0 + gt) ? 1.f : 0.f;
+            else if (job.init) s0 = job.init[(int64_t)d * job.init_ld + gt];
+            Sr[d] = s0;
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8)
+            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, gt, c8)]) = pack8(&Sr[8 * c8]);
+        tc::fence_async_smem();
+        tc::bar_sync(BAR_S, 128);
+        const int64_t ostride = (int64_t)p.Hv * 128;
+        auto store_o = [&](int otb, int ovalid) {
+            float ov[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tc::ld32(T_O + lb + 32 * half, ov);
+                bf16* ob = o + ((int64_t)(otb + 32 * half) * p.Hv + hv) * 128 + gt;
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2)
+                    if (32 * half + c2 < ovalid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
+            }
+        };
+        int o_tb = 0, o_valid = 0;
+        bool o_pending = false;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            if (!(ok = tc::bar_and(BAR_S, 128, tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
+            tc::fence_after();
+            // v_new^T = U^T - S^T W^T
+            if (gt == 0) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma(T_U[s], dS + tc::koff(128, kk), dW + tc::koff(64, kk), ID_N64_NEG,
+                            (!job.value_zero) || kk > 0);
+                tc::commit(&sm.mbar_s);
+            }
+            if (o_pending) store_o(o_tb, o_valid);  // previous chunk's output, while the MMA runs
+            if (!(ok = wait_mma())) break;
+            if (gt == 0) tc::mbar_arrive(&sm.wfree);
+            {
+                const float* fac = sm.slot[s].fac;
+                float vv[32];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tc::ld32(T_U[s] + lb + 32 * half, vv);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float d8[8];
+#pragma unroll
+                        for (int c2 = 0; c2 < 8; ++c2) d8[c2] = vv[8 * c8 + c2] * fac[32 * half + 8 * c8 + c2];
+                        *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, gt, 4 * half + c8)]) = pack8(&vv[8 * c8]);
+                        *reinterpret_cast<uint4*>(&sm.VNd[tc::sw128_chunk(128, gt, 4 * half + c8)]) = pack8(d8);
+                    }
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::bar_sync(BAR_S, 128);
+            // o^T = S^T Q~^T + v_new^T A^T ; dS^T = VNd K
+            if (gt == 0) {
+                tc::fence_after();
+                if (job.write_o) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma(T_O, dS + tc::koff(128, kk), dQK[s] + tc::koff(128, kk), ID_N64, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma(T_O, dVN + tc::koff(128, kk), dA[s] + tc::koff(64, kk), ID_N64, 1);
+                }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma(T_O, tc::desc_k(aVN, 128, kk), tc::desc_k(aA, 64, kk), ID_N64, 1);
+                    tc::mma(T_DS, dVNd + tc::koff(128, kk), dKmn[s] + tc::mnoff(kk), ID_N128_BMN, kk > 0);
+                tc::commit(&sm.mbar_s);
             }
+            if (!(ok = wait_mma())) break;
+            const float eglast = sm.slot[s].eglast;
+            o_tb = sm.slot[s].tb;
+            o_valid = sm.slot[s].valid;
+            o_pending = job.write_o;
+            tc::fence_before();
+            tc::bar_sync(BAR_S, 128);
+            if (gt == 0) tc::mbar_arrive(&sm.empty[s]);
+            {  // S <- e^{G_last} S + dS
+                float ds[32];
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma(T_DS, tc::desc_k(aVNd, 128, kk), tc::desc_mn(aK, 128 * 128, kk), ID_N128_BMN, kk > 0);
-            tc::commit(&sm.mbar);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    tc::ld32(T_DS + lb + 32 * q4, ds);
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) Sr[32 * q4 + c2] = fmaf(eglast, Sr[32 * q4 + c2], ds[c2]);
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 16; ++c8)
+                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, gt, c8)]) = pack8(&Sr[8 * c8]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::bar_sync(BAR_S, 128);
         }
-        if (!(alive = wait_mma())) break;
-        if (job.write_o) {
-            float ov[32];
-            tc::ld32(T_O + lb + 32 * wg, ov);
-            bf16* ob = o + ((int64_t)(tb + 32 * wg) * p.Hv + hv) * 128 + row;
-            const int64_t ostride = (int64_t)p.Hv * 128;
+        if (ok && o_pending) store_o(o_tb, o_valid);
+        if (ok && job.fin) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (32 * wg + c < valid) ob[c * ostride] = __float2bfloat16_rn(ov[c]);
+            for (int d = 0; d < 128; ++d) job.fin[(int64_t)d * job.fin_ld + gt] = Sr[d];
         }
-        {  // S <- e^{G_last} S + dS
-            const float a = sm.eG[63];
-            float ds[32];
-            tc::ld32(T_DS + lb + 64 * wg, ds);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) Sr[c] = fmaf(a, Sr[c], ds[c]);
-            tc::ld32(T_DS + lb + 64 * wg + 32, ds);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) Sr[32 + c] = fmaf(a, Sr[32 + c], ds[c]);
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * wg + c8)]) = pack8(&Sr[8 * c8]);
-        }
-        tc::fence_before();
     }
-    if (alive && job.fin) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) job.fin[(int64_t)(64 * wg + c) * job.fin_ld + row] = Sr[c];
-    }
-    if (!alive) {
-        // a stuck wait: give the tensor core a last bounded chance to drain
-        tc::mbar_wait(&sm.mbar, phase ^ 1u, kSpin);
-    }
+    if (!ok && gt == 0) atomicAdd(&g_gdn_timeouts, 1);
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -352,7 +428,7 @@ gdn_status set_smem_attr(const void* func, size_t bytes);
 bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv) { return dt == GDN_BF16 && dk == 128 && dv == 128; }
 
 gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_t s) {
-    const size_t smem = sizeof(SmemTC) + 1024;
+    const size_t smem = sizeof(SmemWS) + 1024;
     gdn_status st = set_smem_attr((const void*)chunk_tc_kernel, smem);
     if (st != GDN_OK) return st;
     chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src);

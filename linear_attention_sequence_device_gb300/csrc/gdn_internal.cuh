@@ -88,11 +88,12 @@ struct ChunkParams {
     int col_tile;           // state columns per CTA
 };
 
-// Resolve blockIdx -> job.  Returns false when this CTA has nothing to do.
-__device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob& j) {
-    const int hv = blockIdx.y;
+// Resolve a block index (bx = job item, by = value head, bz = state tile)
+// -> job.  Returns false when this CTA has nothing to do.
+__device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob& j, int bx, int by, int bz) {
+    const int hv = by;
     const int nvt = p.dv / p.col_tile;
-    const int z = blockIdx.z;
+    const int z = bz;
     j.hv = hv;
     j.identity_init = false;
     j.value_zero = false;
@@ -102,7 +103,7 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
     j.fin_ld = p.dv;
     auto clampT = [&](int t) { return t < 0 ? 0 : (t > p.T ? p.T : t); };
     if (src == JOBS_SEQS || src == JOBS_SUMMARY) {
-        const int n = blockIdx.x;
+        const int n = bx;
         j.t0 = clampT(__ldg(p.cu + n));
         j.t1 = clampT(__ldg(p.cu + n + 1));
         if (j.t1 < j.t0) j.t1 = j.t0;
@@ -134,7 +135,7 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
     const int part = p.T / P;
     const int64_t cu_base = 1 + (int64_t)P * GDN_PLAN_NFIELDS;
     if (src == JOBS_SHARD_PASS2) {
-        const int r = blockIdx.x;
+        const int r = bx;
         const int32_t* rec = plan + 1 + (int64_t)r * GDN_PLAN_NFIELDS;
         if (__ldg(rec + GDN_PLAN_IS_FIRST_RANK)) return false;
         if (z >= nvt) return false;
@@ -152,8 +153,8 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
             j.fin = p.h_final + ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;
         return true;
     }
-    // pass 1: blockIdx.x = flat (shard, local segment) slot
-    const int slot = blockIdx.x;
+    // pass 1: bx = flat (shard, local segment) slot
+    const int slot = bx;
     int lo = 0, hi = P - 1;  // last shard with seg_offset <= slot
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -199,6 +200,73 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
     if (continues_out) j.fin = p.sumN + carry_st + j.col0;  // constant carry (M = 0)
     else if (p.h_final) j.fin = p.h_final + st;
     return true;
+}
+
+__device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob& j) {
+    return make_job(p, src, j, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// Tokens of job item x (the grid's x index) for the given job source; -1 if
+// the item has no work.  Used to start the longest jobs first.
+__device__ __forceinline__ int job_item_length(const ChunkParams& p, int src, int x) {
+    if (src == JOBS_SEQS || src == JOBS_SUMMARY) {
+        const int a = __ldg(p.cu + x), b = __ldg(p.cu + x + 1);
+        return b > a ? b - a : 0;
+    }
+    const int32_t* plan = p.plan;
+    if (__ldg(plan) != 0) return -1;
+    const int P = p.n_shards;
+    const int64_t cu_base = 1 + (int64_t)P * GDN_PLAN_NFIELDS;
+    if (src == JOBS_SHARD_PASS2) {
+        const int32_t* rec = plan + 1 + (int64_t)x * GDN_PLAN_NFIELDS;
+        if (__ldg(rec + GDN_PLAN_IS_FIRST_RANK)) return -1;
+        return __ldg(plan + cu_base + (int64_t)x * (p.num_seqs + 1) + 1);
+    }
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(plan + 1 + (int64_t)mid * GDN_PLAN_NFIELDS + GDN_PLAN_SEG_OFFSET) <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int32_t* rec = plan + 1 + (int64_t)lo * GDN_PLAN_NFIELDS;
+    const int i = x - __ldg(rec + GDN_PLAN_SEG_OFFSET);
+    if (i < 0 || i >= __ldg(rec + GDN_PLAN_LOCAL_NUM_SEQS)) return -1;
+    const int32_t* lc = plan + cu_base + (int64_t)lo * (p.num_seqs + 1);
+    return __ldg(lc + i + 1) - __ldg(lc + i);
+}
+
+// Longest-first block order.  The hardware starts CTAs roughly in linear
+// block order, so the linear index L is mapped to (item of rank L / (heads *
+// tiles), head, tile) with items ranked by decreasing length (ties by index).
+// Cooperative over the CTA (all NT threads); len is shared scratch of
+// kMaxLptItems ints.  Grids with more items keep the natural order.
+constexpr int kMaxLptItems = 512;
+template <int NT>
+__device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* len, int* pick, int& bx,
+                                          int& by, int& bz) {
+    const int S = gridDim.x;
+    bx = blockIdx.x;
+    by = blockIdx.y;
+    bz = blockIdx.z;
+    if (S > kMaxLptItems) return;
+    for (int s = threadIdx.x; s < S; s += NT) len[s] = job_item_length(p, src, s);
+    __syncthreads();
+    const int64_t L = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int per = gridDim.y * gridDim.z;
+    const int r = (int)(L / per), rem = (int)(L % per);
+    for (int n = threadIdx.x; n < S; n += NT) {
+        const int ln = len[n];
+        int rank = 0;
+        for (int m = 0; m < S; ++m) {
+            const int lm = len[m];
+            rank += (lm > ln) || (lm == ln && m < n);
+        }
+        if (rank == r) *pick = n;
+    }
+    __syncthreads();
+    bx = *pick;
+    by = rem % gridDim.y;
+    bz = rem / gridDim.y;
 }
 
 // launchers (chunk_bf16.cu / chunk_f32.cu)

@@ -35,6 +35,12 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int R, int kk) {
     return desc(base + (uint32_t)((kk >> 2) * R * 128 + (kk & 3) * 32), 16, 1024);
 }
+// Start-address increments (in 16-byte units) of K step kk, to add to a base
+// descriptor: K-major tile of R rows; MN-major tile ([K rows][MN columns]).
+__host__ __device__ constexpr uint64_t koff(int R, int kk) {
+    return (uint64_t)(((kk >> 2) * R * 128 + (kk & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnoff(int kk) { return (uint64_t)((kk * 16 * 128) >> 4); }
 // MN-major operand stored as [K rows][MN columns] in atoms of 64 columns,
 // atoms `atom_bytes` apart; descriptor of the 16-row K step kk.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t base, uint32_t atom_bytes, int kk) {
