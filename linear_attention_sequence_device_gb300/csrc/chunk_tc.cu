@@ -14,14 +14,15 @@
 // one tile serves as K-major operand of one product and MN-major operand of
 // another.
 //
-// Two warpgroups work on different chunks at once:
-//   producer (warps 0-3): everything that does not depend on the state --
+// Two roles of two warpgroups each work on different chunks at once (the
+// two warpgroups of a role split the columns of every elementwise step):
+//   producer (warps 0-7): everything that does not depend on the state --
 //     loads, the Gram product, the L2 norms (from the Gram diagonal, folded
 //     into scale factors), A and L, the in-place UT inverse (tf32 mma.sync
 //     block products), W and U -- for chunk c+1 while
-//   consumer (warps 4-7) runs the state chain of chunk c: v_new, then o and
+//   consumer (warps 8-15) runs the state chain of chunk c: v_new, then o and
 //     dS, then S <- e^{G_last} S + dS with the fp32 state in registers
-//     (thread = value row) and a bf16 copy in shared memory as the A operand.
+//     (thread = value row, half the key columns) and a bf16 copy in shared memory as the A operand.
 // Q/K, A, the per-chunk scale factors and U (in tensor memory) are double
 // buffered ("slots"); W is single buffered with its own release barrier.
 // Every wait is bounded: on expiry the kernel counts a timeout, both groups
@@ -35,7 +36,8 @@ __device__ int g_gdn_timeouts;  // bounded waits that expired (read by gdn_devic
 
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;
+constexpr int GS = 256;  // threads per role (two warpgroups)
 constexpr int LDF = 68;
 constexpr uint32_t kSpin = 1u << 20;  // try_wait polls before a wait is declared stuck
 constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two warpgroups
@@ -92,8 +94,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     if (!make_job(p, src, job, bx, by, bz)) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool producer = warp < 4;
-    const int gt = tid & 127;  // thread index in its warpgroup == tensor-memory lane
+    const bool producer = warp < 8;
+    const int gt = tid & (GS - 1);  // thread index in its role
+    const int row = gt & 127;       // tensor-memory lane = row of every [128 x N] product
+    const int half = gt >> 7;       // which half of the columns this thread handles
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const int hv = job.hv, hk = hv / (p.Hv / p.Hk);
 
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         auto wait_mma = [&]() -> bool {
             const bool done = tc::mbar_wait(&sm.mbar_p, ph, kSpin);
             ph ^= 1u;
-            const bool all = tc::bar_and(BAR_P, 128, done);
+            const bool all = tc::bar_and(BAR_P, GS, done);
             tc::fence_after();
             return all;
         };
@@ -147,11 +151,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             const int s = c & 1;
             const int tb = job.t0 + 64 * c;
             const int valid = min(64, job.t1 - tb);
-            if (c >= 2 && !(ok = tc::bar_and(BAR_P, 128, tc::mbar_wait(&sm.empty[s], ((c >> 1) - 1) & 1, kSpin))))
+            if (c >= 2 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.empty[s], ((c >> 1) - 1) & 1, kSpin))))
                 break;
             tc::fence_after();
             bf16* QKs = sm.QK[s];
-            for (int e = gt; e < 64 * 16; e += 128) {
+            for (int e = gt; e < 64 * 16; e += GS) {
                 const int r = e >> 4, c8 = e & 15;
                 const int64_t t = tb + (r < valid ? r : 0);
                 const int nb = r < valid ? 16 : 0;
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             cp_async_wait_all();
             tc::fence_async_smem();
-            tc::bar_sync(BAR_P, 128);
+            tc::bar_sync(BAR_P, GS);
             // Gram [Q;K][Q;K]^T; the gate prefix meanwhile
             if (gt == 0) {
                 tc::fence_after();
@@ -179,23 +183,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             if (warp == 0) gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
             if (!(ok = wait_mma())) break;
-            {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
+            if (half == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
                 float dg[32];
-                tc::ld32(T_GRAM + lb + (gt & ~31), dg);
+                tc::ld32(T_GRAM + lb + (row & ~31), dg);
                 float d = dg[0];
 #pragma unroll
                 for (int c2 = 1; c2 < 32; ++c2) d = (c2 == lane) ? dg[c2] : d;
-                sm.rn[gt] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
+                sm.rn[row] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
             }
-            tc::bar_sync(BAR_P, 128);
+            tc::bar_sync(BAR_P, GS);
             {  // A (rows 0-63) and L (rows 64-127) from the Q K^T / K K^T blocks
-                const int i = gt & 63;
+                const int i = row & 63;
                 const float Gi = sm.G[i];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                {
                     float gv[32];
                     tc::ld32(T_GRAM + lb + 64 + 32 * half, gv);
-                    if (gt < 64) {
+                    if (row < 64) {
                         const float fi = p.scale * sm.rn[i];
                         float a[32];
 #pragma unroll
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                             *reinterpret_cast<uint4*>(&sm.Aqk[s][tc::sw128_chunk(64, i, 4 * half + c8)]) =
                                 pack8(&a[8 * c8]);
                     } else {
-                        const float fi = sm.beta[i] * sm.rn[gt];
+                        const float fi = sm.beta[i] * sm.rn[row];
                         float* Lrow = sm.LT + i * LDF + 32 * half;
 #pragma unroll
                         for (int c2 = 0; c2 < 32; c2 += 4) {
@@ -225,10 +228,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
             }
             tc::fence_before();
-            tc::bar_sync(BAR_P, 128);
-            unit_lower_inverse64_inplace<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, 128); });
+            tc::bar_sync(BAR_P, GS);
+            unit_lower_inverse64_inplace<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, GS); });
             // T diag(beta), T diag(beta e^G / |k|); Q~ = scale e^G Q / |q|; slot factors
-            for (int e = gt; e < 64 * 8; e += 128) {
+            for (int e = gt; e < 64 * 8; e += GS) {
                 const int i = e >> 3, c8 = e & 7;
                 const float* trow = sm.LT + i * LDF + 8 * c8;
                 float tbv[8], tbg[8];
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
             }
             if (job.write_o) {
-                for (int e = gt; e < 64 * 16; e += 128) {
+                for (int e = gt; e < 64 * 16; e += GS) {
                     const int r = e >> 4, c8 = e & 15;
                     uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
                     uint4 raw = *ptr;
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 sm.slot[s].valid = valid;
             }
             tc::fence_async_smem();
-            tc::bar_sync(BAR_P, 128);
+            tc::bar_sync(BAR_P, GS);
             // W^T = K^T Tbg^T, U^T = V^T Tb^T
             if (gt == 0) {
                 tc::fence_after();
@@ -279,21 +282,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             if (!(ok = wait_mma())) break;
             // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
-            if (c >= 1 && !(ok = tc::bar_and(BAR_P, 128, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
+            if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
             {
                 float wv[32];
-                const int dch = (gt & 63) >> 3;
+                const int dch = (row & 63) >> 3;
+                tc::ld32(T_W + lb + 32 * half, wv);
+                bf16* wb = sm.W + (row >> 6) * 64 * 64 + 32 * half * 64 + (row & 7);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tc::ld32(T_W + lb + 32 * half, wv);
-                    bf16* wb = sm.W + (gt >> 6) * 64 * 64 + 32 * half * 64 + (gt & 7);
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
-                }
+                for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
             }
             tc::fence_async_smem();
             tc::fence_before();
-            tc::bar_sync(BAR_P, 128);
+            tc::bar_sync(BAR_P, GS);
             if (gt == 0) tc::mbar_arrive(&sm.full[s]);
         }
     } else {
@@ -303,41 +303,39 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         auto wait_mma = [&]() -> bool {
             const bool done = tc::mbar_wait(&sm.mbar_s, ph, kSpin);
             ph ^= 1u;
-            const bool all = tc::bar_and(BAR_S, 128, done);
+            const bool all = tc::bar_and(BAR_S, GS, done);
             tc::fence_after();
             return all;
         };
-        // state S^T row gt (value column gt), all 128 key columns
-        float Sr[128];
+        // state S^T row `row` (value column), key columns [64 half, 64 half + 64)
+        float Sr[64];
 #pragma unroll
-        for (int d = 0; d < 128; ++d) {
+        for (int c2 = 0; c2 < 64; ++c2) {
+            const int d = 64 * half + c2;
             float s0 = 0.f;
-            if (job.identity_init) s0 = (d == job.col0 + gt) ? 1.f : 0.f;
-            else if (job.init) s0 = job.init[(int64_t)d * job.init_ld + gt];
-            Sr[d] = s0;
+            if (job.identity_init) s0 = (d == job.col0 + row) ? 1.f : 0.f;
+            else if (job.init) s0 = job.init[(int64_t)d * job.init_ld + row];
+            Sr[c2] = s0;
         }
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8)
-            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, gt, c8)]) = pack8(&Sr[8 * c8]);
+        for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
         tc::fence_async_smem();
-        tc::bar_sync(BAR_S, 128);
+        tc::bar_sync(BAR_S, GS);
         const int64_t ostride = (int64_t)p.Hv * 128;
         auto store_o = [&](int otb, int ovalid) {
             float ov[32];
+            tc::ld32(T_O + lb + 32 * half, ov);
+            bf16* ob = o + ((int64_t)(otb + 32 * half) * p.Hv + hv) * 128 + row;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tc::ld32(T_O + lb + 32 * half, ov);
-                bf16* ob = o + ((int64_t)(otb + 32 * half) * p.Hv + hv) * 128 + gt;
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2)
-                    if (32 * half + c2 < ovalid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
-            }
+            for (int c2 = 0; c2 < 32; ++c2)
+                if (32 * half + c2 < ovalid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
         };
         int o_tb = 0, o_valid = 0;
         bool o_pending = false;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
-            if (!(ok = tc::bar_and(BAR_S, 128, tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
+            if (!(ok = tc::bar_and(BAR_S, GS, tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
             tc::fence_after();
             // v_new^T = U^T - S^T W^T
             if (gt == 0) {
@@ -353,22 +351,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             {
                 const float* fac = sm.slot[s].fac;
                 float vv[32];
+                tc::ld32(T_U[s] + lb + 32 * half, vv);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tc::ld32(T_U[s] + lb + 32 * half, vv);
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float d8[8];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float d8[8];
-#pragma unroll
-                        for (int c2 = 0; c2 < 8; ++c2) d8[c2] = vv[8 * c8 + c2] * fac[32 * half + 8 * c8 + c2];
-                        *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, gt, 4 * half + c8)]) = pack8(&vv[8 * c8]);
-                        *reinterpret_cast<uint4*>(&sm.VNd[tc::sw128_chunk(128, gt, 4 * half + c8)]) = pack8(d8);
-                    }
+                    for (int c2 = 0; c2 < 8; ++c2) d8[c2] = vv[8 * c8 + c2] * fac[32 * half + 8 * c8 + c2];
+                    *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
+                    *reinterpret_cast<uint4*>(&sm.VNd[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(d8);
                 }
             }
             tc::fence_async_smem();
             tc::fence_before();
-            tc::bar_sync(BAR_S, 128);
+            tc::bar_sync(BAR_S, GS);
             // o^T = S^T Q~^T + v_new^T A^T ; dS^T = VNd K
             if (gt == 0) {
                 tc::fence_after();
@@ -391,28 +386,28 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             o_valid = sm.slot[s].valid;
             o_pending = job.write_o;
             tc::fence_before();
-            tc::bar_sync(BAR_S, 128);
+            tc::bar_sync(BAR_S, GS);
             if (gt == 0) tc::mbar_arrive(&sm.empty[s]);
             {  // S <- e^{G_last} S + dS
                 float ds[32];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    tc::ld32(T_DS + lb + 32 * q4, ds);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    tc::ld32(T_DS + lb + 64 * half + 32 * q2, ds);
 #pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) Sr[32 * q4 + c2] = fmaf(eglast, Sr[32 * q4 + c2], ds[c2]);
+                    for (int c2 = 0; c2 < 32; ++c2) Sr[32 * q2 + c2] = fmaf(eglast, Sr[32 * q2 + c2], ds[c2]);
                 }
 #pragma unroll
-                for (int c8 = 0; c8 < 16; ++c8)
-                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, gt, c8)]) = pack8(&Sr[8 * c8]);
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
             }
             tc::fence_async_smem();
             tc::fence_before();
-            tc::bar_sync(BAR_S, 128);
+            tc::bar_sync(BAR_S, GS);
         }
         if (ok && o_pending) store_o(o_tb, o_valid);
         if (ok && job.fin) {
 #pragma unroll
-            for (int d = 0; d < 128; ++d) job.fin[(int64_t)d * job.fin_ld + gt] = Sr[d];
+            for (int c2 = 0; c2 < 64; ++c2) job.fin[(int64_t)(64 * half + c2) * job.fin_ld + row] = Sr[c2];
         }
     }
     if (!ok && gt == 0) atomicAdd(&g_gdn_timeouts, 1);
