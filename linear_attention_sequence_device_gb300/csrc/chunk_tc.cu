@@ -64,6 +64,13 @@ struct SmemWS {
     SlotSmall slot[2];
     float g[64], beta[64], G[64], eG[64], eGl[64];
     float rn[128];          // 1/|q_i| (0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
+    // per-chunk factors; e^{G_i - G_j} = e^{G_i - G_r} e^{G_r - G_j} with G_r = G_31
+    float colf[64];         // e^{G_r - G_j} / |k_j|
+    float rowA[64];         // scale e^{G_i - G_r} / |q_i|
+    float rowL[64];         // beta_i e^{G_i - G_r} / |k_i|
+    float fbg[64];          // beta_j e^{G_j} / |k_j|
+    float qf[64];           // scale e^{G_i} / |q_i|
+    int factored;           // the split exponentials stay well inside fp32 range
     uint64_t mbar_p, mbar_s;  // tensor-core completion, producer / consumer
     uint64_t full[2], empty[2], wfree;
     uint32_t tmem_slot;
@@ -147,28 +154,38 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
-        for (int c = 0; c < nch; ++c) {
-            const int s = c & 1;
-            const int tb = job.t0 + 64 * c;
-            const int valid = min(64, job.t1 - tb);
-            if (c >= 2 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.empty[s], ((c >> 1) - 1) & 1, kSpin))))
-                break;
-            tc::fence_after();
-            bf16* QKs = sm.QK[s];
+        // Q/K of chunk cc into its slot, V into the single V tile (cp.async);
+        // g and beta into registers, stored to shared memory at the chunk's start
+        float g_next = 0.f, b_next = 0.f;
+        auto issue_loads = [&](int cc) {
+            const int tbn = job.t0 + 64 * cc;
+            const int vn = min(64, job.t1 - tbn);
+            bf16* QKn = sm.QK[cc & 1];
             for (int e = gt; e < 64 * 16; e += GS) {
                 const int r = e >> 4, c8 = e & 15;
-                const int64_t t = tb + (r < valid ? r : 0);
-                const int nb = r < valid ? 16 : 0;
-                cp_async16(&QKs[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
-                cp_async16(&QKs[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
+                const int64_t t = tbn + (r < vn ? r : 0);
+                const int nb = r < vn ? 16 : 0;
+                cp_async16(&QKn[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
+                cp_async16(&QKn[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
                 if (!job.value_zero)
                     cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8, nb);
             }
             cp_async_commit();
             if (gt < 64) {
-                const int64_t t = tb + gt;
-                sm.g[gt] = gt < valid ? __ldg(p.g + t * p.Hv + hv) : 0.f;
-                sm.beta[gt] = gt < valid ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
+                const int64_t t = tbn + gt;
+                g_next = gt < vn ? __ldg(p.g + t * p.Hv + hv) : 0.f;
+                b_next = gt < vn ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
+            }
+        };
+        if (nch > 0) issue_loads(0);
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            const int tb = job.t0 + 64 * c;
+            const int valid = min(64, job.t1 - tb);
+            bf16* QKs = sm.QK[s];
+            if (gt < 64) {
+                sm.g[gt] = g_next;
+                sm.beta[gt] = b_next;
             }
             cp_async_wait_all();
             tc::fence_async_smem();
@@ -181,7 +198,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     tc::mma(T_GRAM, dQK[s] + tc::koff(128, kk), dQK[s] + tc::koff(128, kk), ID_N128, kk > 0);
                 tc::commit(&sm.mbar_p);
             }
-            if (warp == 0) gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
+            if (warp == 0) {
+                gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
+                __syncwarp();
+                const float Gr = sm.G[31];
+                float dev = fmaxf(fabsf(sm.G[2 * lane] - Gr), fabsf(sm.G[2 * lane + 1] - Gr));
+#pragma unroll
+                for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
+                if (lane == 0) sm.factored = dev < 60.f;
+            }
             if (!(ok = wait_mma())) break;
             if (half == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
                 float dg[32];
@@ -189,42 +214,58 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 float d = dg[0];
 #pragma unroll
                 for (int c2 = 1; c2 < 32; ++c2) d = (c2 == lane) ? dg[c2] : d;
-                sm.rn[row] = l2 ? rsqrtf(d + 1e-6f) : 1.f;
+                const float r = l2 ? rsqrtf(d + 1e-6f) : 1.f;
+                sm.rn[row] = r;
+                const int i = row & 63;
+                const float Gi = sm.G[i], Gr = sm.G[31];
+                if (row < 64) {
+                    sm.rowA[i] = p.scale * r * __expf(Gi - Gr);
+                    sm.qf[i] = p.scale * sm.eG[i] * r;
+                } else {
+                    sm.colf[i] = r * __expf(Gr - Gi);
+                    sm.rowL[i] = sm.beta[i] * r * __expf(Gi - Gr);
+                    sm.fbg[i] = sm.beta[i] * sm.eG[i] * r;
+                }
             }
             tc::bar_sync(BAR_P, GS);
             {  // A (rows 0-63) and L (rows 64-127) from the Q K^T / K K^T blocks
                 const int i = row & 63;
-                const float Gi = sm.G[i];
-                {
-                    float gv[32];
-                    tc::ld32(T_GRAM + lb + 64 + 32 * half, gv);
-                    if (row < 64) {
-                        const float fi = p.scale * sm.rn[i];
-                        float a[32];
+                float gv[32];
+                tc::ld32(T_GRAM + lb + 64 + 32 * half, gv);
+                float a[32];
+                if (sm.factored) {
+                    const float fi = row < 64 ? sm.rowA[i] : sm.rowL[i];
+                    const int lim = row < 64 ? i : i - 1;  // A keeps the diagonal, L does not
+                    const float4* cf = reinterpret_cast<const float4*>(sm.colf + 32 * half);
 #pragma unroll
-                        for (int c2 = 0; c2 < 32; ++c2) {
-                            const int j = 32 * half + c2;
-                            a[c2] = (j <= i) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
-                        }
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 f4 = cf[c4];
+                        const float fc[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8)
-                            *reinterpret_cast<uint4*>(&sm.Aqk[s][tc::sw128_chunk(64, i, 4 * half + c8)]) =
-                                pack8(&a[8 * c8]);
-                    } else {
-                        const float fi = sm.beta[i] * sm.rn[row];
-                        float* Lrow = sm.LT + i * LDF + 32 * half;
-#pragma unroll
-                        for (int c2 = 0; c2 < 32; c2 += 4) {
-                            float4 l4;
-                            float* lv = &l4.x;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = 32 * half + c2 + e;
-                                lv[e] = (j < i) ? fi * sm.rn[64 + j] * gv[c2 + e] * __expf(Gi - sm.G[j]) : 0.f;
-                            }
-                            *reinterpret_cast<float4*>(Lrow + c2) = l4;
+                        for (int e = 0; e < 4; ++e) {
+                            const int c2 = 4 * c4 + e;
+                            a[c2] = (32 * half + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
                         }
                     }
+                } else {  // wide gate range: one exponential per element
+                    const float Gi = sm.G[i];
+                    const float fi = row < 64 ? p.scale * sm.rn[i] : sm.beta[i] * sm.rn[row];
+                    const int lim = row < 64 ? i : i - 1;
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) {
+                        const int j = 32 * half + c2;
+                        a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
+                    }
+                }
+                if (row < 64) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4*>(&sm.Aqk[s][tc::sw128_chunk(64, i, 4 * half + c8)]) = pack8(&a[8 * c8]);
+                } else {
+                    float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * half);
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
                 }
             }
             tc::fence_before();
@@ -233,13 +274,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             // T diag(beta), T diag(beta e^G / |k|); Q~ = scale e^G Q / |q|; slot factors
             for (int e = gt; e < 64 * 8; e += GS) {
                 const int i = e >> 3, c8 = e & 7;
-                const float* trow = sm.LT + i * LDF + 8 * c8;
+                const float4* trow = reinterpret_cast<const float4*>(sm.LT + i * LDF + 8 * c8);
+                const float4* bj = reinterpret_cast<const float4*>(sm.beta + 8 * c8);
+                const float4* fj = reinterpret_cast<const float4*>(sm.fbg + 8 * c8);
                 float tbv[8], tbg[8];
 #pragma unroll
-                for (int c2 = 0; c2 < 8; ++c2) {
-                    const int j = 8 * c8 + c2;
-                    tbv[c2] = trow[c2] * sm.beta[j];
-                    tbg[c2] = tbv[c2] * sm.eG[j] * sm.rn[64 + j];
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const float4 t4 = trow[h2], b4 = bj[h2], f4 = fj[h2];
+                    tbv[4 * h2] = t4.x * b4.x; tbv[4 * h2 + 1] = t4.y * b4.y;
+                    tbv[4 * h2 + 2] = t4.z * b4.z; tbv[4 * h2 + 3] = t4.w * b4.w;
+                    tbg[4 * h2] = t4.x * f4.x; tbg[4 * h2 + 1] = t4.y * f4.y;
+                    tbg[4 * h2 + 2] = t4.z * f4.z; tbg[4 * h2 + 3] = t4.w * f4.w;
                 }
                 *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
                 *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
@@ -250,7 +295,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
                     uint4 raw = *ptr;
                     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                    const float f = p.scale * sm.eG[r] * sm.rn[r];
+                    const float f = sm.qf[r];
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -281,6 +326,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::commit(&sm.mbar_p);
             }
             if (!(ok = wait_mma())) break;
+            // prefetch chunk c+1: its slot must have been released by the consumer
+            // (chunk c-1), and V is free now that U has been formed
+            if (c + 1 < nch) {
+                if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.empty[s ^ 1], ((c - 1) >> 1) & 1, kSpin))))
+                    break;
+                tc::fence_after();
+                issue_loads(c + 1);
+            }
             // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
             if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
             {
