@@ -208,3 +208,135 @@ __device__ __forceinline__ void unit_lower_inverse64_inplace(float* Ls, int gtid
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// acc (16x16, two m16n8 accumulators) += A (16x16 block at Ab) * B (16x16 block
+// at Bb), both fp32 in shared memory with row stride LD, as tf32 products.
+template <int LD>
+__device__ __forceinline__ void mma_block16_tf32(float (&acc)[2][4], const float* Ab, const float* Bb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 16; kk += 8) {
+        const float* Ar = Ab + g * LD + kk + t;
+        uint32_t af[4] = {to_tf32(Ar[0]), to_tf32(Ar[8 * LD]), to_tf32(Ar[4]), to_tf32(Ar[8 * LD + 4])};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float* Br = Bb + (kk + t) * LD + 8 * nt + g;
+            mma_tf32(acc[nt], af, to_tf32(Br[0]), to_tf32(Br[4 * LD]));
+        }
+    }
+}
+// Write -acc (16x16) to the block at Cb.
+template <int LD>
+__device__ __forceinline__ void store_block16_neg(const float (&acc)[2][4], float* Cb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        float* Cr = Cb + g * LD + 8 * nt + 2 * t;
+        *reinterpret_cast<float2*>(Cr) = make_float2(-acc[nt][0], -acc[nt][1]);
+        *reinterpret_cast<float2*>(Cr + 8 * LD) = make_float2(-acc[nt][2], -acc[nt][3]);
+    }
+}
+template <int LD>
+__device__ __forceinline__ void store_block16(const float (&acc)[2][4], float* Cb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        float* Cr = Cb + g * LD + 8 * nt + 2 * t;
+        *reinterpret_cast<float2*>(Cr) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(Cr + 8 * LD) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+}
+
+// In place: Ls holds a strictly lower 64x64 L on entry and T = (I + L)^-1 on
+// exit, by 2x2 recursion on 32x32 blocks.  With A = I + L[0:32,0:32],
+// B = I + L[32:64,32:64], C = L[32:64,0:32]:
+//   T = [[A^-1, 0], [-B^-1 C A^-1, B^-1]],
+// each 32x32 inverse itself from 16x16 blocks: D_a = (I + L_aa)^-1 by
+// forward substitution, T10 = -D1 L10 D0, T32 = -D3 L32 D2.  Then
+// X = C A^-1 (four 16x16 blocks) and T_lowerleft = -B^-1 X, every product a
+// tf32 mma.sync on one warp; each stage is computed in registers before it
+// overwrites the blocks it no longer needs.  gtid: thread index in a group of
+// >= 128 threads (warps 0-3 work); sync: the group barrier.
+template <int LD, class Sync>
+__device__ __forceinline__ void unit_lower_inverse64_rec(float* Ls, int gtid, Sync sync) {
+    const int gw = gtid >> 5;
+    auto blk = [&](int a, int b) { return Ls + 16 * a * LD + 16 * b; };
+    // diagonal blocks
+    float x[16];
+    const int da = gtid >> 4, dc = gtid & 15;
+    if (gtid < 64) {
+        const float* L = blk(da, da);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float acc = (i == dc) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) acc = fmaf(-L[i * LD + m], (m >= dc) ? x[m] : 0.f, acc);
+            x[i] = (i >= dc) ? acc : 0.f;
+        }
+    }
+    sync();
+    if (gtid < 64) {
+        float* L = blk(da, da);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) L[i * LD + dc] = x[i];
+    }
+    sync();
+    // T10 = -D1 (L10 D0)  (warp 0),  T32 = -D3 (L32 D2)  (warp 1); the
+    // intermediate goes through the block it replaces
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (gw < 2) {
+        const int a = gw ? 3 : 1, b = a - 1;
+        mma_block16_tf32<LD>(acc, blk(a, b), blk(b, b));
+    }
+    sync();
+    if (gw < 2) store_block16<LD>(acc, blk(gw ? 3 : 1, gw ? 2 : 0));
+    sync();
+    if (gw < 2) {
+        const int a = gw ? 3 : 1, b = a - 1;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        mma_block16_tf32<LD>(acc, blk(a, a), blk(a, b));
+    }
+    sync();
+    if (gw < 2) store_block16_neg<LD>(acc, blk(gw ? 3 : 1, gw ? 2 : 0));
+    sync();
+    // X = C A^-1: X_a0 = L_a0 D0 + L_a1 T10, X_a1 = L_a1 D1   (a = 2, 3; warps 0-3)
+    const int xa = 2 + (gw >> 1), xb = gw & 1;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    if (gw < 4) {
+        if (xb == 0) {
+            mma_block16_tf32<LD>(acc, blk(xa, 0), blk(0, 0));
+            mma_block16_tf32<LD>(acc, blk(xa, 1), blk(1, 0));
+        } else {
+            mma_block16_tf32<LD>(acc, blk(xa, 1), blk(1, 1));
+        }
+    }
+    sync();
+    if (gw < 4) store_block16<LD>(acc, blk(xa, xb));
+    sync();
+    // T_2b = -D2 X_2b ;  T_3b = -(T32 X_2b + D3 X_3b)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    if (gw < 4) {
+        if (xa == 2) {
+            mma_block16_tf32<LD>(acc, blk(2, 2), blk(2, xb));
+        } else {
+            mma_block16_tf32<LD>(acc, blk(3, 2), blk(2, xb));
+            mma_block16_tf32<LD>(acc, blk(3, 3), blk(3, xb));
+        }
+    }
+    sync();
+    if (gw < 4) store_block16_neg<LD>(acc, blk(xa, xb));
+    sync();
+}
+
+}  // namespace gdn

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         // Q/K of chunk cc into its slot, V into the single V tile (cp.async);
         // g and beta into registers, stored to shared memory at the chunk's start
         float g_next = 0.f, b_next = 0.f;
-        auto issue_loads = [&](int cc) {
+        auto issue_qk = [&](int cc) {
             const int tbn = job.t0 + 64 * cc;
             const int vn = min(64, job.t1 - tbn);
             bf16* QKn = sm.QK[cc & 1];
@@ -167,17 +167,30 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 const int nb = r < vn ? 16 : 0;
                 cp_async16(&QKn[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
                 cp_async16(&QKn[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
-                if (!job.value_zero)
-                    cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8, nb);
             }
-            cp_async_commit();
             if (gt < 64) {
                 const int64_t t = tbn + gt;
                 g_next = gt < vn ? __ldg(p.g + t * p.Hv + hv) : 0.f;
                 b_next = gt < vn ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
             }
         };
-        if (nch > 0) issue_loads(0);
+        auto issue_v = [&](int cc) {
+            const int tbn = job.t0 + 64 * cc;
+            const int vn = min(64, job.t1 - tbn);
+            if (!job.value_zero) {
+                for (int e = gt; e < 64 * 16; e += GS) {
+                    const int r = e >> 4, c8 = e & 15;
+                    const int64_t t = tbn + (r < vn ? r : 0);
+                    cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8,
+                               r < vn ? 16 : 0);
+                }
+            }
+            cp_async_commit();
+        };
+        if (nch > 0) {
+            issue_qk(0);
+            issue_v(0);
+        }
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             const int tb = job.t0 + 64 * c;
@@ -270,7 +283,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_before();
             tc::bar_sync(BAR_P, GS);
-            unit_lower_inverse64_inplace<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, GS); });
+            unit_lower_inverse64_rec<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, GS); });
             // T diag(beta), T diag(beta e^G / |k|); Q~ = scale e^G Q / |q|; slot factors
             for (int e = gt; e < 64 * 8; e += GS) {
                 const int i = e >> 3, c8 = e & 7;
@@ -325,15 +338,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
                 tc::commit(&sm.mbar_p);
             }
-            if (!(ok = wait_mma())) break;
-            // prefetch chunk c+1: its slot must have been released by the consumer
-            // (chunk c-1), and V is free now that U has been formed
+            // prefetch chunk c+1 while W and U form: its Q/K slot once the
+            // consumer has released it (chunk c-1); V once U no longer reads it
             if (c + 1 < nch) {
                 if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.empty[s ^ 1], ((c - 1) >> 1) & 1, kSpin))))
                     break;
                 tc::fence_after();
-                issue_loads(c + 1);
+                issue_qk(c + 1);
             }
+            if (!(ok = wait_mma())) break;
+            if (c + 1 < nch) issue_v(c + 1);
             // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
             if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
             {
