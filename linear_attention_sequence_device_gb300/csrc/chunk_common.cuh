@@ -27,6 +27,8 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 // ---- gate prefix -------------------------------------------------------------
 // Warp 0: G = inclusive cumsum of g over the chunk (2 values per lane), then

@@ -7,14 +7,20 @@
 // window of the last conv_k - 1 input rows down the strip, so every input
 // element is read once (plus conv_k - 1 halo rows per strip).  A warp covers
 // 256 contiguous channels of a row: fully coalesced 512-byte transactions.
+// Input rows stream through a per-thread ring of NSTAGE batches of RB rows in
+// shared memory, filled by cp.async: the bytes in flight are bounded by
+// shared memory rather than registers, and since every thread only reads
+// what it copied itself, no block-level synchronisation is needed.
 // Grid: (channel blocks, strips per shard, shards).
-#include "gdn_internal.cuh"
+#include "chunk_common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int NT = 128;
-constexpr int R = 32;  // rows per strip
+constexpr int R = 128;     // rows per strip
+constexpr int RB = 8;      // rows per batch
+constexpr int NSTAGE = 4;  // batches in the shared-memory ring
 
 struct ConvParams {
     const void* x; int64_t ldx;
@@ -80,7 +86,7 @@ template <> struct Vec8<float> {
 };
 
 template <typename T, int KC>
-__global__ void __launch_bounds__(NT, 3) conv_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
     const int c0 = (blockIdx.x * NT + threadIdx.x) * 8;
     if (c0 >= p.C) return;
     int part, rs;
@@ -147,18 +153,34 @@ __global__ void __launch_bounds__(NT, 3) conv_kernel(const ConvParams p) {
             for (int c = 0; c < 8; ++c) win[j][c] = 0.f;
         }
     }
-    // rows in groups of RB: all loads of a group are issued before any compute,
-    // so each thread keeps RB 16-byte loads in flight
-    constexpr int RB = 8;
-    for (int t0 = lt0; t0 < lt1; t0 += RB) {
-        typename Vec8<T>::Raw raw[RB];
+    // ring of NSTAGE batches: stage b holds rows [lt0 + RB b, lt0 + RB (b + 1))
+    constexpr int VEC = sizeof(T) * 8 / 16;  // 16-byte vectors per row and thread
+    extern __shared__ uint4 ring[];          // [NSTAGE][RB][VEC][NT]
+    const int nb = (lt1 - lt0 + RB - 1) / RB;
+    auto issue = [&](int b) {
+        if (b < nb) {
+            uint4* st = ring + (size_t)(b % NSTAGE) * RB * VEC * NT;
 #pragma unroll
-        for (int u = 0; u < RB; ++u) {
-            if (t0 + u < lt1) raw[u] = Vec8<T>::load_raw(x + (int64_t)(rs + t0 + u) * p.ldx + c0);
+            for (int u = 0; u < RB; ++u) {
+                const int t = lt0 + RB * b + u;
+                const T* src = x + (int64_t)(rs + (t < lt1 ? t : lt0)) * p.ldx + c0;
+#pragma unroll
+                for (int v = 0; v < VEC; ++v)
+                    cp_async16(st + (u * VEC + v) * NT + threadIdx.x, reinterpret_cast<const uint4*>(src) + v,
+                               t < lt1 ? 16 : 0);
+            }
         }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int b = 0; b < NSTAGE - 1; ++b) issue(b);
+    for (int b = 0; b < nb; ++b) {
+        issue(b + NSTAGE - 1);
+        cp_async_wait<NSTAGE - 1>();
+        const uint4* st = ring + (size_t)(b % NSTAGE) * RB * VEC * NT;
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
-            const int t = t0 + u;
+            const int t = lt0 + RB * b + u;
             if (t >= lt1) break;
             while (t == next) {  // a new sequence starts: no history
 #pragma unroll
@@ -169,14 +191,19 @@ __global__ void __launch_bounds__(NT, 3) conv_kernel(const ConvParams p) {
                 next = seg + 1 <= nloc ? lc[seg + 1] : part;
             }
             float cur[8], out[8];
-            Vec8<T>::unpack(raw[u], cur);
+            uint4 rv[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) rv[v] = st[(u * VEC + v) * NT + threadIdx.x];
+            Vec8<T>::unpack(*reinterpret_cast<const typename Vec8<T>::Raw*>(rv), cur);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float acc = br[c];
 #pragma unroll
                 for (int j = 0; j < KC - 1; ++j) acc = fmaf(wr[j][c], win[j][c], acc);
                 acc = fmaf(wr[KC - 1][c], cur[c], acc);
-                out[c] = acc / (1.f + expf(-acc));
+                // silu(a) = a / (1 + e^-a); the exponent is capped so that the
+                // fast divide stays in range (silu(a) ~ 0 below that)
+                out[c] = __fdividef(acc, 1.f + __expf(fminf(-acc, 80.f)));
             }
             Vec8<T>::store(y + (int64_t)(rs + t) * p.ldy + c0, out);
 #pragma unroll
@@ -191,16 +218,30 @@ __global__ void __launch_bounds__(NT, 3) conv_kernel(const ConvParams p) {
     }
 }
 
+}  // namespace
+
+gdn_status set_smem_attr(const void* func, size_t bytes);
+
+namespace {
+
+template <typename T, int KC>
+gdn_status launch_tk(const ConvParams& p, dim3 grid, cudaStream_t s) {
+    const size_t smem = (size_t)NSTAGE * RB * (sizeof(T) * 8 / 16) * NT * 16;
+    gdn_status st = set_smem_attr((const void*)conv_kernel<T, KC>, smem);
+    if (st != GDN_OK) return st;
+    conv_kernel<T, KC><<<grid, NT, smem, s>>>(p);
+    return check_launch("conv_kernel");
+}
+
 template <typename T>
 gdn_status launch_t(const ConvParams& p, dim3 grid, cudaStream_t s) {
     switch (p.Kc) {
-        case 1: conv_kernel<T, 1><<<grid, NT, 0, s>>>(p); break;
-        case 2: conv_kernel<T, 2><<<grid, NT, 0, s>>>(p); break;
-        case 3: conv_kernel<T, 3><<<grid, NT, 0, s>>>(p); break;
-        case 4: conv_kernel<T, 4><<<grid, NT, 0, s>>>(p); break;
-        default: return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", p.Kc);
+        case 1: return launch_tk<T, 1>(p, grid, s);
+        case 2: return launch_tk<T, 2>(p, grid, s);
+        case 3: return launch_tk<T, 3>(p, grid, s);
+        case 4: return launch_tk<T, 4>(p, grid, s);
     }
-    return check_launch("conv_kernel");
+    return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", p.Kc);
 }
 
 }  // namespace
