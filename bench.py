@@ -107,6 +107,18 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(self.samples)}
 
 
+KERNEL_SOURCES = ["chunk_tc.cu", "chunk_common.cuh", "tc_util.cuh", "gdn_internal.cuh"]
+
+
+def kernel_sources_sha256():
+    """Hash of the dominant kernel's sources (ties stored ncu counters to them)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "linear_attention_sequence_device_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def time_loop(fn, n, stream):
     import torch
     start = torch.cuda.Event(enable_timing=True)
@@ -310,7 +322,10 @@ def run_ours(args, rank, world, local_rank):
     traffic = None
     tp = os.path.join(ROOT, "profiles", f"chunk_traffic_{w.name}.json")
     if os.path.exists(tp):
-        traffic = json.load(open(tp)).get("bytes_per_launch")
+        rec = json.load(open(tp))
+        # counters are only valid for the kernel sources they were taken on
+        if rec.get("kernel_sources_sha256") == kernel_sources_sha256():
+            traffic = rec.get("bytes_per_launch")
     if t_bytes >= t_flops:
         ach = chunk_bytes / (chunk_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
@@ -319,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         ach = flops / (chunk_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tfl, "unit": "TFLOP/s",
                 "frac": ach / tfl, "traffic": traffic}
-    roof.update({"kernel": "chunk_bf16_kernel" if w.dtype == "bf16" else "chunk_f32_kernel",
+    roof.update({"kernel": ("chunk_tc_kernel" if (w.dtype == "bf16" and w.dk == 128 and w.dv == 128)
+                            else "chunk_bf16_kernel" if w.dtype == "bf16" else "chunk_f32_kernel"),
                  "kernel_ms": chunk_ms, "peak_source": peak_src + " (burst)",
                  "algorithmic_bytes": chunk_bytes, "algorithmic_flops": flops,
                  "tensor_frac": (flops / (chunk_ms * 1e-3) / 1e12) / tfl,

@@ -123,18 +123,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
     const uint32_t T_GRAM = tmem, T_W = tmem + 128, T_O = tmem + 320, T_DS = tmem + 384;
-    const uint32_t T_U[2] = {tmem + 192, tmem + 256};
-    const uint32_t aQK[2] = {tc::smem_addr(sm.QK[0]), tc::smem_addr(sm.QK[1])};
-    const uint32_t aA[2] = {tc::smem_addr(sm.Aqk[0]), tc::smem_addr(sm.Aqk[1])};
+    // per-slot values are picked with selects (a runtime-indexed array would live in local memory)
+    const uint32_t T_U0 = tmem + 192, T_U1 = tmem + 256;
+    const uint32_t aQK0 = tc::smem_addr(sm.QK[0]), aQK1 = tc::smem_addr(sm.QK[1]);
+    const uint32_t aA0 = tc::smem_addr(sm.Aqk[0]), aA1 = tc::smem_addr(sm.Aqk[1]);
     const uint32_t aW = tc::smem_addr(sm.W), aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S);
     const uint32_t aVN = tc::smem_addr(sm.VN), aVNd = tc::smem_addr(sm.VNd);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
     const int nch = (job.t1 - job.t0 + 63) / 64;
     bool ok = true;
     // base descriptors; a K step adds a constant to the start-address field
-    const uint64_t dQK[2] = {tc::desc(aQK[0], 16, 1024), tc::desc(aQK[1], 16, 1024)};
-    const uint64_t dKmn[2] = {tc::desc(aQK[0] + 64 * 128, 128 * 128, 1024), tc::desc(aQK[1] + 64 * 128, 128 * 128, 1024)};
-    const uint64_t dA[2] = {tc::desc(aA[0], 16, 1024), tc::desc(aA[1], 16, 1024)};
+    const uint64_t dQK0 = tc::desc(aQK0, 16, 1024), dQK1 = tc::desc(aQK1, 16, 1024);
+    const uint64_t dKmn0 = tc::desc(aQK0 + 64 * 128, 128 * 128, 1024), dKmn1 = tc::desc(aQK1 + 64 * 128, 128 * 128, 1024);
+    const uint64_t dA0 = tc::desc(aA0, 16, 1024), dA1 = tc::desc(aA1, 16, 1024);
     const uint64_t dW = tc::desc(aW, 16, 1024), dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024);
     const uint64_t dVN = tc::desc(aVN, 16, 1024), dVNd = tc::desc(aVNd, 16, 1024);
     const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_GRAM, dQK[s] + tc::koff(128, kk), dQK[s] + tc::koff(128, kk), ID_N128, kk > 0);
+                    tc::mma(T_GRAM, (s ? dQK1 : dQK0) + tc::koff(128, kk), (s ? dQK1 : dQK0) + tc::koff(128, kk), ID_N128, kk > 0);
                 tc::commit(&sm.mbar_p);
             }
             if (warp == 0) {
@@ -332,9 +333,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    tc::mma(T_W, dKmn[s] + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                    tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                     if (!job.value_zero)
-                        tc::mma(T_U[s], dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        tc::mma((s ? T_U1 : T_U0), dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                 }
                 tc::commit(&sm.mbar_p);
             }
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             if (gt == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_U[s], dS + tc::koff(128, kk), dW + tc::koff(64, kk), ID_N64_NEG,
+                    tc::mma((s ? T_U1 : T_U0), dS + tc::koff(128, kk), dW + tc::koff(64, kk), ID_N64_NEG,
                             (!job.value_zero) || kk > 0);
                 tc::commit(&sm.mbar_s);
             }
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             {
                 const float* fac = sm.slot[s].fac;
                 float vv[32];
-                tc::ld32(T_U[s] + lb + 32 * half, vv);
+                tc::ld32((s ? T_U1 : T_U0) + lb + 32 * half, vv);
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     float d8[8];
@@ -437,14 +438,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (job.write_o) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma(T_O, dS + tc::koff(128, kk), dQK[s] + tc::koff(128, kk), ID_N64, kk > 0);
+                        tc::mma(T_O, dS + tc::koff(128, kk), (s ? dQK1 : dQK0) + tc::koff(128, kk), ID_N64, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma(T_O, dVN + tc::koff(128, kk), dA[s] + tc::koff(64, kk), ID_N64, 1);
+                        tc::mma(T_O, dVN + tc::koff(128, kk), (s ? dA1 : dA0) + tc::koff(64, kk), ID_N64, 1);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma(T_DS, dVNd + tc::koff(128, kk), dKmn[s] + tc::mnoff(kk), ID_N128_BMN, kk > 0);
+                    tc::mma(T_DS, dVNd + tc::koff(128, kk), (s ? dKmn1 : dKmn0) + tc::mnoff(kk), ID_N128_BMN, kk > 0);
                 tc::commit(&sm.mbar_s);
             }
             if (!(ok = wait_mma())) break;
