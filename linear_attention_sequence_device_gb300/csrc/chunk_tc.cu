@@ -27,6 +27,9 @@
 // buffered ("slots"); W is single buffered with its own release barrier.
 // Every wait is bounded: on expiry the kernel counts a timeout, both groups
 // leave their loops, and the tensor memory is freed.
+#include <cuda.h>
+#include <string.h>
+
 #include "chunk_common.cuh"
 #include "tc_util.cuh"
 
@@ -40,8 +43,13 @@ constexpr int NT = 512;
 constexpr int GS = 256;  // threads per role (two warpgroups)
 constexpr int LDF = 68;
 constexpr uint32_t kSpin = 1u << 20;  // try_wait polls before a wait is declared stuck
-constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two warpgroups
+constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two roles
+constexpr int BAR_PA = 3;             // producer warps 0-3 (the UT inverse)
 typedef __nv_bfloat16 bf16;
+
+struct TmaMaps {
+    CUtensorMap q, k, v;  // [T rows x heads*128 columns] bf16 views, 64x64 boxes, 128-byte swizzle
+};
 
 struct SlotSmall {
     float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of dS
@@ -73,6 +81,7 @@ struct SmemWS {
     int factored;           // the split exponentials stay well inside fp32 range
     uint64_t mbar_p, mbar_s;  // tensor-core completion, producer / consumer
     uint64_t full[2], empty[2], wfree;
+    uint64_t ld_qk[2], ld_v;   // TMA arrivals (transaction bytes)
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
     int lpt_pick;
@@ -92,7 +101,8 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return r;
 }
 
-__global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src) {
+__global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src,
+                                                        const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     SmemWS& sm = *reinterpret_cast<SmemWS*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
     ChunkJob job;
@@ -116,6 +126,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::mbar_init(&sm.empty[0], 1);
         tc::mbar_init(&sm.empty[1], 1);
         tc::mbar_init(&sm.wfree, 1);
+        tc::mbar_init(&sm.ld_qk[0], 1);
+        tc::mbar_init(&sm.ld_qk[1], 1);
+        tc::mbar_init(&sm.ld_v, 1);
     }
     if (warp == 0) tc::tmem_alloc(&sm.tmem_slot, 512);
     tc::fence_before();
@@ -142,9 +155,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 
     if (producer) {
         // ====================== producer warpgroup ======================
-        const bf16* __restrict__ q = static_cast<const bf16*>(p.q);
-        const bf16* __restrict__ k = static_cast<const bf16*>(p.k);
-        const bf16* __restrict__ v = static_cast<const bf16*>(p.v);
         const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
         uint32_t ph = 0;
@@ -155,19 +165,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
-        // Q/K of chunk cc into its slot, V into the single V tile (cp.async);
+        // TMA loads: Q/K of chunk cc into its slot (four 64x64 boxes, 128-byte
+        // swizzle = the operand layout), V into the single V tile (two boxes);
         // g and beta into registers, stored to shared memory at the chunk's start
         float g_next = 0.f, b_next = 0.f;
         auto issue_qk = [&](int cc) {
             const int tbn = job.t0 + 64 * cc;
             const int vn = min(64, job.t1 - tbn);
-            bf16* QKn = sm.QK[cc & 1];
-            for (int e = gt; e < 64 * 16; e += GS) {
-                const int r = e >> 4, c8 = e & 15;
-                const int64_t t = tbn + (r < vn ? r : 0);
-                const int nb = r < vn ? 16 : 0;
-                cp_async16(&QKn[tc::sw128_chunk(128, r, c8)], q + t * p.ldq + (int64_t)hk * 128 + c8 * 8, nb);
-                cp_async16(&QKn[tc::sw128_chunk(128, 64 + r, c8)], k + t * p.ldk + (int64_t)hk * 128 + c8 * 8, nb);
+            if (gt == 0) {
+                bf16* QKn = sm.QK[cc & 1];
+                uint64_t* bar = &sm.ld_qk[cc & 1];
+                tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
+                tc::tma_load_2d(QKn, &maps.q, hk * 128, tbn, bar);
+                tc::tma_load_2d(QKn + 128 * 64, &maps.q, hk * 128 + 64, tbn, bar);
+                tc::tma_load_2d(QKn + 64 * 64, &maps.k, hk * 128, tbn, bar);
+                tc::tma_load_2d(QKn + 128 * 64 + 64 * 64, &maps.k, hk * 128 + 64, tbn, bar);
             }
             if (gt < 64) {
                 const int64_t t = tbn + gt;
@@ -176,23 +188,35 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
         };
         auto issue_v = [&](int cc) {
-            const int tbn = job.t0 + 64 * cc;
-            const int vn = min(64, job.t1 - tbn);
-            if (!job.value_zero) {
-                for (int e = gt; e < 64 * 16; e += GS) {
-                    const int r = e >> 4, c8 = e & 15;
-                    const int64_t t = tbn + (r < vn ? r : 0);
-                    cp_async16(&sm.V[tc::sw128_chunk(64, r, c8)], v + t * p.ldv + (int64_t)hv * 128 + c8 * 8,
-                               r < vn ? 16 : 0);
-                }
+            if (gt == 0 && !job.value_zero) {
+                const int tbn = job.t0 + 64 * cc;
+                tc::mbar_expect_tx(&sm.ld_v, 2 * 64 * 64 * 2);
+                tc::tma_load_2d(sm.V, &maps.v, hv * 128, tbn, &sm.ld_v);
+                tc::tma_load_2d(sm.V + 64 * 64, &maps.v, hv * 128 + 64, tbn, &sm.ld_v);
             }
-            cp_async_commit();
+        };
+        auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool all = tc::bar_and(BAR_P, GS, tc::mbar_wait(bar, parity, kSpin));
+            tc::fence_after();
+            return all;
+        };
+        // the Gram product [Q;K][Q;K]^T of the chunk in slot ss (diagonal: the L2 norms)
+        auto issue_gram = [&](int ss) {
+            if (gt == 0) {
+                tc::fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma(T_GRAM, (ss ? dQK1 : dQK0) + tc::koff(128, kk), (ss ? dQK1 : dQK0) + tc::koff(128, kk),
+                            ID_N128, kk > 0);
+                tc::commit(&sm.mbar_p);
+            }
         };
         if (nch > 0) {
             issue_qk(0);
             issue_v(0);
+            if ((ok = wait_bar(&sm.ld_qk[0], 0))) issue_gram(0);
         }
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
             const int tb = job.t0 + 64 * c;
             const int valid = min(64, job.t1 - tb);
@@ -201,17 +225,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 sm.g[gt] = g_next;
                 sm.beta[gt] = b_next;
             }
-            cp_async_wait_all();
-            tc::fence_async_smem();
             tc::bar_sync(BAR_P, GS);
-            // Gram [Q;K][Q;K]^T; the gate prefix meanwhile
-            if (gt == 0) {
-                tc::fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_GRAM, (s ? dQK1 : dQK0) + tc::koff(128, kk), (s ? dQK1 : dQK0) + tc::koff(128, kk), ID_N128, kk > 0);
-                tc::commit(&sm.mbar_p);
-            }
             if (warp == 0) {
                 gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
                 __syncwarp();
@@ -221,7 +235,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
                 if (lane == 0) sm.factored = dev < 60.f;
             }
-            if (!(ok = wait_mma())) break;
+            if (!(ok = wait_mma())) break;  // the Gram product of this chunk
             if (half == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
                 float dg[32];
                 tc::ld32(T_GRAM + lb + (row & ~31), dg);
@@ -284,8 +298,28 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_before();
             tc::bar_sync(BAR_P, GS);
-            unit_lower_inverse64_rec<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_P, GS); });
-            // T diag(beta), T diag(beta e^G / |k|); Q~ = scale e^G Q / |q|; slot factors
+            // the UT inverse on warps 0-3; warps 4-7 rescale Q meanwhile
+            if (gt < 128) {
+                unit_lower_inverse64_rec<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_PA, 128); });
+            } else if (job.write_o) {
+                for (int e = gt - 128; e < 64 * 16; e += 128) {
+                    const int r = e >> 4, c8 = e & 15;
+                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
+                    uint4 raw = *ptr;
+                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+                    const float f = sm.qf[r];
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 t2 = __bfloat1622float2(h[i]);
+                        x[2 * i] = t2.x * f;
+                        x[2 * i + 1] = t2.y * f;
+                    }
+                    *ptr = pack8(x);
+                }
+            }
+            tc::bar_sync(BAR_P, GS);
+            // T diag(beta), T diag(beta e^G / |k|); slot factors
             for (int e = gt; e < 64 * 8; e += GS) {
                 const int i = e >> 3, c8 = e & 7;
                 const float4* trow = reinterpret_cast<const float4*>(sm.LT + i * LDF + 8 * c8);
@@ -303,23 +337,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
                 *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
             }
-            if (job.write_o) {
-                for (int e = gt; e < 64 * 16; e += GS) {
-                    const int r = e >> 4, c8 = e & 15;
-                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
-                    uint4 raw = *ptr;
-                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                    const float f = sm.qf[r];
-                    float x[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 t2 = __bfloat1622float2(h[i]);
-                        x[2 * i] = t2.x * f;
-                        x[2 * i + 1] = t2.y * f;
-                    }
-                    *ptr = pack8(x);
-                }
-            }
             if (gt < 64) sm.slot[s].fac[gt] = sm.eGl[gt] * sm.rn[64 + gt];
             if (gt == 0) {
                 sm.slot[s].eglast = sm.eG[63];
@@ -328,7 +345,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_async_smem();
             tc::bar_sync(BAR_P, GS);
-            // W^T = K^T Tbg^T, U^T = V^T Tb^T
+            // W^T = K^T Tbg^T, U^T = V^T Tb^T (V of this chunk must have landed)
+            if (!job.value_zero && !(ok = wait_bar(&sm.ld_v, c & 1))) break;
             if (gt == 0) {
                 tc::fence_after();
 #pragma unroll
@@ -342,15 +360,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             // prefetch chunk c+1 while W and U form: its Q/K slot once the
             // consumer has released it (chunk c-1); V once U no longer reads it
             if (c + 1 < nch) {
-                if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.empty[s ^ 1], ((c - 1) >> 1) & 1, kSpin))))
-                    break;
-                tc::fence_after();
+                if (c >= 1 && !(ok = wait_bar(&sm.empty[s ^ 1], ((c - 1) >> 1) & 1))) break;
                 issue_qk(c + 1);
             }
             if (!(ok = wait_mma())) break;
             if (c + 1 < nch) issue_v(c + 1);
             // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
-            if (c >= 1 && !(ok = tc::bar_and(BAR_P, GS, tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin)))) break;
+            if (c >= 1 && !(ok = wait_bar(&sm.wfree, (c - 1) & 1))) break;
             {
                 float wv[32];
                 const int dch = (row & 63) >> 3;
@@ -363,6 +379,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_before();
             tc::bar_sync(BAR_P, GS);
             if (gt == 0) tc::mbar_arrive(&sm.full[s]);
+            // the next chunk's Gram product starts as soon as its Q/K are in
+            if (c + 1 < nch) {
+                if (!(ok = wait_bar(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1))) break;
+                issue_gram(s ^ 1);
+            }
         }
     } else {
         // ====================== consumer warpgroup ======================
@@ -490,11 +511,50 @@ gdn_status set_smem_attr(const void* func, size_t bytes);
 
 bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv) { return dt == GDN_BF16 && dk == 128 && dv == 128; }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [rows x cols] bf16 view with row stride ld (elements), 64x64 boxes, 128B swizzle;
+// rows past the end read as zero.
+static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t cols, int64_t rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, 64}, es[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return GDN_OK;
+}
+
 gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_t s) {
     const size_t smem = sizeof(SmemWS) + 1024;
     gdn_status st = set_smem_attr((const void*)chunk_tc_kernel, smem);
     if (st != GDN_OK) return st;
-    chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src);
+    TmaMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (p.T > 0) {
+        if ((st = make_map(&maps.q, p.q, p.ldq, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
+        if ((st = make_map(&maps.k, p.k, p.ldk, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
+        if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
+    }
+    chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src, maps);
     return check_launch("chunk_tc_kernel");
 }
 

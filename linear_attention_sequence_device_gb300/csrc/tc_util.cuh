@@ -138,3 +138,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
 
 }  // namespace tc
 }  // namespace gdn
+
+namespace gdn {
+namespace tc {
+
+// Arrive on an mbarrier and add `bytes` to its expected transaction count.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)), "r"(bytes)
+                 : "memory");
+}
+// 2D tiled TMA load of one box (coordinates x = innermost element, y = row)
+// into shared memory; completion is counted on `mbar` in bytes.  `tmap` is
+// the generic address of a CUtensorMap kernel parameter.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(mbar))
+        : "memory");
+}
+
+}  // namespace tc
+}  // namespace gdn
