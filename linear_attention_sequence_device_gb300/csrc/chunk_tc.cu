@@ -93,6 +93,36 @@ constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
 constexpr uint32_t ID_N64_NEG = tc::idesc_bf16(128, 64, false, false, true);
 constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 
+// One warp: the chunk's gate prefix from per-token values held by lanes
+// (lane l holds g of tokens 2l and 2l+1; beta likewise), written to shared
+// memory with e^G, e^{G_last - G}, beta, and whether split exponentials
+// around G_31 stay within fp32 range.
+template <class Sm>
+__device__ __forceinline__ void gate_prefix_fast(Sm& sm, float g0, float g1, float b0, float b1) {
+    const int lane = threadIdx.x & 31;
+    float s = g0 + g1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += t;
+    }
+    const float G1 = s, G0 = s - g1;
+    const float Gl = __shfl_sync(0xffffffffu, s, 31);
+    const float Gr = __shfl_sync(0xffffffffu, s, 15);  // G_31 = inclusive sum through token 31
+    sm.G[2 * lane] = G0;
+    sm.G[2 * lane + 1] = G1;
+    sm.eG[2 * lane] = __expf(G0);
+    sm.eG[2 * lane + 1] = __expf(G1);
+    sm.eGl[2 * lane] = __expf(Gl - G0);
+    sm.eGl[2 * lane + 1] = __expf(Gl - G1);
+    sm.beta[2 * lane] = b0;
+    sm.beta[2 * lane + 1] = b1;
+    float dev = fmaxf(fabsf(G0 - Gr), fabsf(G1 - Gr));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
+    if (lane == 0) sm.factored = dev < 60.f;
+}
+
 __device__ __forceinline__ uint4 pack8(const float* f) {
     uint4 r;
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
@@ -168,7 +198,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         // TMA loads: Q/K of chunk cc into its slot (four 64x64 boxes, 128-byte
         // swizzle = the operand layout), V into the single V tile (two boxes);
         // g and beta into registers, stored to shared memory at the chunk's start
-        float g_next = 0.f, b_next = 0.f;
+        float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
         auto issue_qk = [&](int cc) {
             const int tbn = job.t0 + 64 * cc;
             const int vn = min(64, job.t1 - tbn);
@@ -181,10 +211,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::tma_load_2d(QKn + 64 * 64, &maps.k, hk * 128, tbn, bar);
                 tc::tma_load_2d(QKn + 128 * 64 + 64 * 64, &maps.k, hk * 128 + 64, tbn, bar);
             }
-            if (gt < 64) {
-                const int64_t t = tbn + gt;
-                g_next = gt < vn ? __ldg(p.g + t * p.Hv + hv) : 0.f;
-                b_next = gt < vn ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
+            if (warp == 0) {  // lane l: tokens 2l, 2l+1
+                const int r0 = 2 * lane, r1 = 2 * lane + 1;
+                const int64_t t0 = tbn + r0, t1 = tbn + r1;
+                g_next0 = r0 < vn ? __ldg(p.g + t0 * p.Hv + hv) : 0.f;
+                g_next1 = r1 < vn ? __ldg(p.g + t1 * p.Hv + hv) : 0.f;
+                b_next0 = r0 < vn ? __bfloat162float(beta[t0 * p.Hv + hv]) : 0.f;
+                b_next1 = r1 < vn ? __bfloat162float(beta[t1 * p.Hv + hv]) : 0.f;
             }
         };
         auto issue_v = [&](int cc) {
@@ -215,26 +248,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             issue_qk(0);
             issue_v(0);
             if ((ok = wait_bar(&sm.ld_qk[0], 0))) issue_gram(0);
+            if (warp == 0) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
         }
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
             const int tb = job.t0 + 64 * c;
             const int valid = min(64, job.t1 - tb);
             bf16* QKs = sm.QK[s];
-            if (gt < 64) {
-                sm.g[gt] = g_next;
-                sm.beta[gt] = b_next;
-            }
-            tc::bar_sync(BAR_P, GS);
-            if (warp == 0) {
-                gate_prefix_warp0(sm.g, sm.G, sm.eG, sm.eGl);
-                __syncwarp();
-                const float Gr = sm.G[31];
-                float dev = fmaxf(fabsf(sm.G[2 * lane] - Gr), fabsf(sm.G[2 * lane + 1] - Gr));
-#pragma unroll
-                for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
-                if (lane == 0) sm.factored = dev < 60.f;
-            }
+            // the gate prefix of this chunk was formed at the end of the previous one
             if (!(ok = wait_mma())) break;  // the Gram product of this chunk
             if (half == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
                 float dg[32];
@@ -379,10 +400,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_before();
             tc::bar_sync(BAR_P, GS);
             if (gt == 0) tc::mbar_arrive(&sm.full[s]);
-            // the next chunk's Gram product starts as soon as its Q/K are in
+            // the next chunk's Gram product starts as soon as its Q/K are in,
+            // and its gate prefix is formed meanwhile (this chunk no longer reads G)
             if (c + 1 < nch) {
                 if (!(ok = wait_bar(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1))) break;
                 issue_gram(s ^ 1);
+                if (warp == 0) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
             }
         }
     } else {
