@@ -113,7 +113,7 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* Ls, float* Ts,
 
 namespace gdn {
 
-// ---- in-place unit-lower inverse on tensor cores (tf32) ---------------------
+// ---- tf32 tensor-core block products (m16n8k8 mma.sync) -------------------
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -125,88 +125,6 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, uint32_t b
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Ls (fp32, 64 x 64, row stride LD) holds a strictly lower L on entry and
-// T = (I + L)^-1 on exit.  16x16 blocks: the diagonal blocks D_a = (I + L_aa)^-1
-// by forward substitution (64 threads, one column each); then block row
-// a = 1..3, block b < a by warp b:
-//   T_ab = -D_a sum_{m=b}^{a-1} L_am T_mb       (T_bb = D_b)
-// with m16n8k8 tf32 products; every block of a row is computed before any
-// is written over the L blocks it replaces, which later rows no longer read.
-// `gtid` is the thread index inside the participating group (>= 128
-// threads: warps 0..3 of the group do the work); `sync` is the group barrier.
-template <int LD, class Sync>
-__device__ __forceinline__ void unit_lower_inverse64_inplace(float* Ls, int gtid, Sync sync) {
-    const int gw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t = lane & 3;
-    float x[16];
-    const int da = gtid >> 4, dc = gtid & 15;
-    if (gtid < 64) {
-        const float* L = Ls + 16 * da * LD + 16 * da;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == dc) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) acc = fmaf(-L[i * LD + m], (m >= dc) ? x[m] : 0.f, acc);
-            x[i] = (i >= dc) ? acc : 0.f;
-        }
-    }
-    sync();
-    if (gtid < 64) {
-        float* L = Ls + 16 * da * LD + 16 * da;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) L[i * LD + dc] = x[i];
-    }
-    sync();
-#pragma unroll 1
-    for (int a = 1; a < 4; ++a) {
-        const int b = gw;
-        const bool active = gw < a;
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (active) {
-            float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int m = b; m < a; ++m) {
-#pragma unroll
-                for (int kk = 0; kk < 16; kk += 8) {
-                    const float* Ar = Ls + (16 * a + g) * LD + 16 * m + kk + t;
-                    uint32_t af[4] = {to_tf32(Ar[0]), to_tf32(Ar[8 * LD]), to_tf32(Ar[4]), to_tf32(Ar[8 * LD + 4])};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const float* Br = Ls + (16 * m + kk + t) * LD + 16 * b + 8 * nt + g;
-                        mma_tf32(xa[nt], af, to_tf32(Br[0]), to_tf32(Br[4 * LD]));
-                    }
-                }
-            }
-            // y = D_a x: x moves from accumulator to B-operand layout by shuffles
-#pragma unroll
-            for (int kk = 0; kk < 16; kk += 8) {
-                const float* Ar = Ls + (16 * a + g) * LD + 16 * a + kk + t;
-                uint32_t af[4] = {to_tf32(Ar[0]), to_tf32(Ar[8 * LD]), to_tf32(Ar[4]), to_tf32(Ar[8 * LD + 4])};
-                const int e0 = kk ? 2 : 0;
-                const int src0 = 4 * t + (g >> 1), src1 = 4 * (t + 4) + (g >> 1);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const float p0 = __shfl_sync(0xffffffffu, xa[nt][e0], src0);
-                    const float p1 = __shfl_sync(0xffffffffu, xa[nt][e0 + 1], src0);
-                    const float q0 = __shfl_sync(0xffffffffu, xa[nt][e0], src1);
-                    const float q1 = __shfl_sync(0xffffffffu, xa[nt][e0 + 1], src1);
-                    const float b0 = (g & 1) ? p1 : p0;
-                    const float b1 = (g & 1) ? q1 : q0;
-                    mma_tf32(y[nt], af, to_tf32(b0), to_tf32(b1));
-                }
-            }
-        }
-        sync();
-        if (active) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float* Cr = Ls + (16 * a + g) * LD + 16 * b + 8 * nt + 2 * t;
-                *reinterpret_cast<float2*>(Cr) = make_float2(-y[nt][0], -y[nt][1]);
-                *reinterpret_cast<float2*>(Cr + 8 * LD) = make_float2(-y[nt][2], -y[nt][3]);
-            }
-        }
-        sync();
-    }
 }
 
 }  // namespace gdn
@@ -249,96 +167,6 @@ __device__ __forceinline__ void store_block16(const float (&acc)[2][4], float* C
         *reinterpret_cast<float2*>(Cr) = make_float2(acc[nt][0], acc[nt][1]);
         *reinterpret_cast<float2*>(Cr + 8 * LD) = make_float2(acc[nt][2], acc[nt][3]);
     }
-}
-
-// In place: Ls holds a strictly lower 64x64 L on entry and T = (I + L)^-1 on
-// exit, by 2x2 recursion on 32x32 blocks.  With A = I + L[0:32,0:32],
-// B = I + L[32:64,32:64], C = L[32:64,0:32]:
-//   T = [[A^-1, 0], [-B^-1 C A^-1, B^-1]],
-// each 32x32 inverse itself from 16x16 blocks: D_a = (I + L_aa)^-1 by
-// forward substitution, T10 = -D1 L10 D0, T32 = -D3 L32 D2.  Then
-// X = C A^-1 (four 16x16 blocks) and T_lowerleft = -B^-1 X, every product a
-// tf32 mma.sync on one warp; each stage is computed in registers before it
-// overwrites the blocks it no longer needs.  gtid: thread index in a group of
-// >= 128 threads (warps 0-3 work); sync: the group barrier.
-template <int LD, class Sync>
-__device__ __forceinline__ void unit_lower_inverse64_rec(float* Ls, int gtid, Sync sync) {
-    const int gw = gtid >> 5;
-    auto blk = [&](int a, int b) { return Ls + 16 * a * LD + 16 * b; };
-    // diagonal blocks
-    float x[16];
-    const int da = gtid >> 4, dc = gtid & 15;
-    if (gtid < 64) {
-        const float* L = blk(da, da);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == dc) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) acc = fmaf(-L[i * LD + m], (m >= dc) ? x[m] : 0.f, acc);
-            x[i] = (i >= dc) ? acc : 0.f;
-        }
-    }
-    sync();
-    if (gtid < 64) {
-        float* L = blk(da, da);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) L[i * LD + dc] = x[i];
-    }
-    sync();
-    // T10 = -D1 (L10 D0)  (warp 0),  T32 = -D3 (L32 D2)  (warp 1); the
-    // intermediate goes through the block it replaces
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if (gw < 2) {
-        const int a = gw ? 3 : 1, b = a - 1;
-        mma_block16_tf32<LD>(acc, blk(a, b), blk(b, b));
-    }
-    sync();
-    if (gw < 2) store_block16<LD>(acc, blk(gw ? 3 : 1, gw ? 2 : 0));
-    sync();
-    if (gw < 2) {
-        const int a = gw ? 3 : 1, b = a - 1;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-        mma_block16_tf32<LD>(acc, blk(a, a), blk(a, b));
-    }
-    sync();
-    if (gw < 2) store_block16_neg<LD>(acc, blk(gw ? 3 : 1, gw ? 2 : 0));
-    sync();
-    // X = C A^-1: X_a0 = L_a0 D0 + L_a1 T10, X_a1 = L_a1 D1   (a = 2, 3; warps 0-3)
-    const int xa = 2 + (gw >> 1), xb = gw & 1;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    if (gw < 4) {
-        if (xb == 0) {
-            mma_block16_tf32<LD>(acc, blk(xa, 0), blk(0, 0));
-            mma_block16_tf32<LD>(acc, blk(xa, 1), blk(1, 0));
-        } else {
-            mma_block16_tf32<LD>(acc, blk(xa, 1), blk(1, 1));
-        }
-    }
-    sync();
-    if (gw < 4) store_block16<LD>(acc, blk(xa, xb));
-    sync();
-    // T_2b = -D2 X_2b ;  T_3b = -(T32 X_2b + D3 X_3b)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    if (gw < 4) {
-        if (xa == 2) {
-            mma_block16_tf32<LD>(acc, blk(2, 2), blk(2, xb));
-        } else {
-            mma_block16_tf32<LD>(acc, blk(3, 2), blk(2, xb));
-            mma_block16_tf32<LD>(acc, blk(3, 3), blk(3, xb));
-        }
-    }
-    sync();
-    if (gw < 4) store_block16_neg<LD>(acc, blk(xa, xb));
-    sync();
 }
 
 }  // namespace gdn

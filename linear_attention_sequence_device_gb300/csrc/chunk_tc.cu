@@ -2,31 +2,41 @@
 // (tcgen05.mma, accumulators in tensor memory).
 //
 // One CTA runs one job: a token range of one value head with the full
-// 128-column state, chunk after chunk (C = 64).  Every product is written
-// transposed so that its M dimension is 128 (a head dimension):
-//   Gram     [Q;K] [Q;K]^T              -> [128 x 128] (Q K^T and K K^T blocks, norms on the diagonal)
-//   W^T      K^T (T diag(beta e^G/|k|))^T -> [128 x 64]
-//   U^T      V^T (T diag(beta))^T        -> [128 x 64]
-//   v_new^T  U^T - S^T W^T               -> [128 x 64]   (negated-A accumulate)
-//   o^T      S^T Q~^T + v_new^T A^T      -> [128 x 64]   (Q~ = scale e^G Q / |q|)
-//   dS^T     (v_new o e^{G_last-G}/|k|)^T K -> [128 x 128]
-// Operands sit in shared memory in the 128-byte-swizzled canonical layout;
-// one tile serves as K-major operand of one product and MN-major operand of
-// another.
+// 128-column state, chunk after chunk (C = 64).  Every product has M = 128
+// (a head dimension).  A tensor-core instruction (K = 16) takes about the
+// same time for N = 64 and N = 256, so products that share their A operand
+// are concatenated along N:
+//   producer, per chunk
+//     [K;Q] K^T or [Q;K] K^T          -> [128 x 64]   the K K^T and Q K^T blocks
+//     W^T = K^T Tbg^T                 -> [128 x 64]   Tbg = T diag(beta e^G / |k|)
+//     U^T = V^T Tb^T                  -> [128 x 64]   Tb  = T diag(beta)
+//   consumer, per chunk
+//     [v_new^T | o^T]  = [U^T | 0] - S^T [W ; -Q~]^T      N = 128, negated A
+//     [o^T | S^T]     += v_new^T [A ; K~^T]^T              N = 192, onto e^{G_last} S^T
+// with Q~ = scale e^G Q / |q|, K~ = diag(e^{G_last - G} / |k|) K and
+// A = scale Q^ K^T o Gamma (lower, diagonal included); the state update
+// S <- e^{G_last} S + K~^T v_new is the last 128 columns of the second product.
+// The row order of the concatenated operands alternates with the chunk's slot
+// so that both slots' outputs sit next to the one state region in tensor memory:
+//   columns  0-63 [Q;K]K^T | 64-127 W^T | 128-191 v_new (slot 0) | 192-255 o (slot 0)
+//          | 256-383 S^T | 384-447 o (slot 1) | 448-511 v_new (slot 1)
+//   slot 0: Q/K tile rows [K -> W ; Q -> -Q~], second operand rows [A ; K~^T]
+//   slot 1: Q/K tile rows [Q -> -Q~ ; K -> W], second operand rows [K~^T ; A]
+// Operands sit in shared memory in the 128-byte-swizzled canonical layout.
 //
-// Two roles of two warpgroups each work on different chunks at once (the
-// two warpgroups of a role split the columns of every elementwise step):
-//   producer (warps 0-7): everything that does not depend on the state --
-//     loads, the Gram product, the L2 norms (from the Gram diagonal, folded
-//     into scale factors), A and L, the in-place UT inverse (tf32 mma.sync
-//     block products), W and U -- for chunk c+1 while
-//   consumer (warps 8-15) runs the state chain of chunk c: v_new, then o and
-//     dS, then S <- e^{G_last} S + dS with the fp32 state in registers
-//     (thread = value row, half the key columns) and a bf16 copy in shared memory as the A operand.
-// Q/K, A, the per-chunk scale factors and U (in tensor memory) are double
-// buffered ("slots"); W is single buffered with its own release barrier.
-// Every wait is bounded: on expiry the kernel counts a timeout, both groups
-// leave their loops, and the tensor memory is freed.
+// Two roles of two warpgroups each work on different chunks at once:
+//   producer (warps 0-7): loads, [Q;K] K^T, the L2 norms (sums of squares while
+//     that product runs, folded into per-row factors), A and L, the UT inverse
+//     (tf32 mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg),
+//     -Q~ and K~^T, and the W and U products -- for chunk c+1 while
+//   consumer (warps 8-15) runs the state chain of chunk c: W to shared memory,
+//     the two products above, the output, and the state (fp32 in registers,
+//     thread = value row and half the key columns, bf16 copy in shared memory).
+// Q/K tiles, A/K~ tiles, v_new/o columns and per-chunk values are double
+// buffered ("slots"); the consumer refills a slot with the Q/K of chunk c+2
+// as soon as it is done with chunk c.  Every wait is bounded: on expiry the
+// kernel counts a timeout, both roles leave their loops, outstanding copies
+// and products are waited for (bounded), and the tensor memory is freed.
 #include <cuda.h>
 #include <string.h>
 
@@ -52,46 +62,48 @@ struct TmaMaps {
 };
 
 struct SlotSmall {
-    float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of dS
+    float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of K~
     float eglast;   // e^{G_last}
     int tb, valid;  // first token and valid rows of the chunk
     int pad;
 };
 
 struct SmemWS {
-    bf16 QK[2][128 * 128];  // per slot: rows 0-63 Q (then Q~), rows 64-127 K
-    bf16 Aqk[2][64 * 64];   // per slot: scale Q^ K^T o Gamma, lower incl. diagonal
-    bf16 W[64 * 128];       // [token][key column]
+    bf16 QK[2][128 * 128];  // per slot: Q/K rows (order above); K rows become W, Q rows -Q~
+    bf16 B2[2][192 * 64];   // per slot: A (64 rows) and K~^T (128 rows), order above
     bf16 V[64 * 128];       // [token][value column]
     bf16 S[128 * 128];      // S^T [value column][key column] (bf16 copy of the state)
     bf16 VN[128 * 64];      // v_new^T [value column][token]
-    bf16 VNd[128 * 64];     // v_new^T scaled by the dS token factor
     bf16 Tb[64 * 64];       // T diag(beta)
     bf16 Tbg[64 * 64];      // T diag(beta e^G / |k|)
-    float LT[64 * LDF];     // L, then T = (I + L)^-1 in place
+    __align__(16) float LT[64 * LDF];  // L; the inverse's blocks replace it block by block
     SlotSmall slot[2];
-    float g[64], beta[64], G[64], eG[64], eGl[64];
-    float rn[128];          // 1/|q_i| (0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
+    __align__(16) float beta[64];
+    __align__(16) float G[64];
+    __align__(16) float eG[64];
+    __align__(16) float eGl[64];
+    __align__(16) float rn[128];  // 1/|q_i| (0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
     // per-chunk factors; e^{G_i - G_j} = e^{G_i - G_r} e^{G_r - G_j} with G_r = G_31
-    float colf[64];         // e^{G_r - G_j} / |k_j|
-    float rowA[64];         // scale e^{G_i - G_r} / |q_i|
-    float rowL[64];         // beta_i e^{G_i - G_r} / |k_i|
-    float fbg[64];          // beta_j e^{G_j} / |k_j|
-    float qf[64];           // scale e^{G_i} / |q_i|
-    int factored;           // the split exponentials stay well inside fp32 range
-    uint64_t mbar_p, mbar_s;  // tensor-core completion, producer / consumer
-    uint64_t full[2], empty[2], wfree;
-    uint64_t ld_qk[2], ld_v;   // TMA arrivals (transaction bytes)
+    __align__(16) float colf[64];  // e^{G_r - G_j} / |k_j|
+    __align__(16) float rowA[64];  // scale e^{G_i - G_r} / |q_i|
+    __align__(16) float rowL[64];  // beta_i e^{G_i - G_r} / |k_i|
+    __align__(16) float fbg[64];   // beta_j e^{G_j} / |k_j|
+    __align__(16) float qf[64];    // scale e^{G_i} / |q_i|
+    int factored;                  // the split exponentials stay well inside fp32 range
+    uint64_t mbar_p, mbar_s;       // tensor-core completion, producer / consumer
+    uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
+    uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
+    uint64_t fin_p, fin_s;         // end-of-job drain of each role's products
+    int qk_issued[2], qk_waited[2], v_issued, v_waited;
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
     int lpt_pick;
 };
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
-constexpr uint32_t ID_N128 = tc::idesc_bf16(128, 128, false, false, false);
 constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
-constexpr uint32_t ID_N64_NEG = tc::idesc_bf16(128, 64, false, false, true);
-constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
+constexpr uint32_t ID_N128_NEG = tc::idesc_bf16(128, 128, false, false, true);
+constexpr uint32_t ID_N192 = tc::idesc_bf16(128, 192, false, false, false);
 
 // One warp: the chunk's gate prefix from per-token values held by lanes
 // (lane l holds g of tokens 2l and 2l+1; beta likewise), written to shared
@@ -131,6 +143,118 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return r;
 }
 
+// bf16 copies of -acc (a 16x16 block at block position (bi, bj) of T) into
+// Tb = T diag(beta) and Tbg = T diag(fbg).
+__device__ __forceinline__ void store_tb16_neg(const float (&acc)[2][4], bf16* Tb, bf16* Tbg, const float* beta,
+                                               const float* fbg, int bi, int bj) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int J = 16 * bj + 8 * nt + 2 * t;
+        const float2 b2 = *reinterpret_cast<const float2*>(beta + J), f2 = *reinterpret_cast<const float2*>(fbg + J);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = tc::sw128(64, 16 * bi + g + 8 * h, J);
+            const float v0 = -acc[nt][2 * h], v1 = -acc[nt][2 * h + 1];
+            *reinterpret_cast<__nv_bfloat162*>(Tb + e) = __floats2bfloat162_rn(v0 * b2.x, v1 * b2.y);
+            *reinterpret_cast<__nv_bfloat162*>(Tbg + e) = __floats2bfloat162_rn(v0 * f2.x, v1 * f2.y);
+        }
+    }
+}
+
+// Tb = T diag(beta) and Tbg = T diag(fbg) (bf16, 128-byte-swizzled K-major
+// 64x64) for T = (I + L)^-1, the strictly lower L in Ls (fp32, row stride
+// LDF), on 128 threads (gtid 0-127; `sync` is their barrier).  16x16 blocks:
+// the diagonal blocks D_a = (I + L_aa)^-1 by forward substitution, one column
+// per thread; then warps 0 and 1 form T10 = -D1 (L10 D0) and T32 = -D3 (L32 D2)
+// while warps 2 and 3 start X = C A0^-1 for the lower-left 32x32 block C
+// (X_a0 = L_a0 D0 + L_a1 T10, X_a1 = L_a1 D1); finally the lower-left blocks
+// T_2b = -D2 X_2b and T_3b = -(T32 X_2b + D3 X_3b).  Block products are tf32
+// mma.sync; each result replaces the L block that only its own warp still
+// reads.  Blocks above the diagonal are never written: Tb and Tbg hold zeros
+// there from the start.
+template <class Sync>
+__device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, const float* beta, const float* fbg,
+                                              int gtid, Sync sync) {
+    const int gw = gtid >> 5;
+    auto blk = [&](int a, int b) { return Ls + 16 * a * LDF + 16 * b; };
+    if (gtid < 64) {
+        const int da = gtid >> 4, dc = gtid & 15;
+        float* Lb = blk(da, da);
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float acc = (i == dc) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) acc = fmaf(-Lb[i * LDF + m], (m >= dc) ? x[m] : 0.f, acc);
+            x[i] = (i >= dc) ? acc : 0.f;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Lb[i * LDF + dc] = x[i];
+    }
+    sync();
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (gw < 2) {
+        const int a = gw ? 3 : 1, b = a - 1;
+        mma_block16_tf32<LDF>(acc, blk(a, b), blk(b, b));
+        __syncwarp();
+        store_block16<LDF>(acc, blk(a, b));
+        __syncwarp();
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        mma_block16_tf32<LDF>(acc, blk(a, a), blk(a, b));
+        __syncwarp();
+        store_block16_neg<LDF>(acc, blk(a, b));
+    } else {
+        mma_block16_tf32<LDF>(acc, blk(gw, 0), blk(0, 0));
+        mma_block16_tf32<LDF>(acc2, blk(gw, 1), blk(1, 1));
+    }
+    sync();
+    if (gw >= 2) {
+        mma_block16_tf32<LDF>(acc, blk(gw, 1), blk(1, 0));
+        __syncwarp();
+        store_block16<LDF>(acc, blk(gw, 0));
+        store_block16<LDF>(acc2, blk(gw, 1));
+    } else {
+        // D0-D3, T10 and T32 are final: their bf16 copies, 8 columns per step
+        for (int t = gtid; t < 192; t += 64) {
+            const int bk = t >> 5, r = (t >> 1) & 15, h = t & 1;
+            const int bi = bk < 4 ? bk : (bk == 4 ? 1 : 3), bj = bk < 4 ? bk : (bk == 4 ? 0 : 2);
+            const int J = 16 * bj + 8 * h;
+            const float* src = Ls + (16 * bi + r) * LDF + J;
+            const float4 v0 = *reinterpret_cast<const float4*>(src), v1 = *reinterpret_cast<const float4*>(src + 4);
+            const float4 b0 = *reinterpret_cast<const float4*>(beta + J), b1 = *reinterpret_cast<const float4*>(beta + J + 4);
+            const float4 f0 = *reinterpret_cast<const float4*>(fbg + J), f1 = *reinterpret_cast<const float4*>(fbg + J + 4);
+            const float tb[8] = {v0.x * b0.x, v0.y * b0.y, v0.z * b0.z, v0.w * b0.w,
+                                 v1.x * b1.x, v1.y * b1.y, v1.z * b1.z, v1.w * b1.w};
+            const float tg[8] = {v0.x * f0.x, v0.y * f0.y, v0.z * f0.z, v0.w * f0.w,
+                                 v1.x * f1.x, v1.y * f1.y, v1.z * f1.z, v1.w * f1.w};
+            const int e = tc::sw128_chunk(64, 16 * bi + r, J >> 3);
+            *reinterpret_cast<uint4*>(Tb + e) = pack8(tb);
+            *reinterpret_cast<uint4*>(Tbg + e) = pack8(tg);
+        }
+    }
+    sync();
+    {
+        const int a = 2 + (gw >> 1), b = gw & 1;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        if (a == 2) {
+            mma_block16_tf32<LDF>(acc, blk(2, 2), blk(2, b));
+        } else {
+            mma_block16_tf32<LDF>(acc, blk(3, 2), blk(2, b));
+            mma_block16_tf32<LDF>(acc, blk(3, 3), blk(3, b));
+        }
+        store_tb16_neg(acc, Tb, Tbg, beta, fbg, a, b);
+    }
+}
+
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src,
                                                         const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -151,40 +275,57 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     if (tid == 0) {
         tc::mbar_init(&sm.mbar_p, 1);
         tc::mbar_init(&sm.mbar_s, 1);
-        tc::mbar_init(&sm.full[0], 1);
-        tc::mbar_init(&sm.full[1], 1);
-        tc::mbar_init(&sm.empty[0], 1);
-        tc::mbar_init(&sm.empty[1], 1);
+        tc::mbar_init(&sm.full[0], 2);  // the W/U products' commit and a producer thread
+        tc::mbar_init(&sm.full[1], 2);
         tc::mbar_init(&sm.wfree, 1);
         tc::mbar_init(&sm.ld_qk[0], 1);
         tc::mbar_init(&sm.ld_qk[1], 1);
         tc::mbar_init(&sm.ld_v, 1);
+        tc::mbar_init(&sm.fin_p, 1);
+        tc::mbar_init(&sm.fin_s, 1);
+        sm.qk_issued[0] = sm.qk_issued[1] = sm.qk_waited[0] = sm.qk_waited[1] = 0;
+        sm.v_issued = sm.v_waited = 0;
     }
     if (warp == 0) tc::tmem_alloc(&sm.tmem_slot, 512);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
-    const uint32_t T_GRAM = tmem, T_W = tmem + 128, T_O = tmem + 320, T_DS = tmem + 384;
-    // per-slot values are picked with selects (a runtime-indexed array would live in local memory)
-    const uint32_t T_U0 = tmem + 192, T_U1 = tmem + 256;
+    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_S = tmem + 256;
+    // per-slot columns are picked with selects (a runtime-indexed array would live in local memory)
+    const uint32_t T_VN0 = tmem + 128, T_O0 = tmem + 192, T_O1 = tmem + 384, T_VN1 = tmem + 448;
     const uint32_t aQK0 = tc::smem_addr(sm.QK[0]), aQK1 = tc::smem_addr(sm.QK[1]);
-    const uint32_t aA0 = tc::smem_addr(sm.Aqk[0]), aA1 = tc::smem_addr(sm.Aqk[1]);
-    const uint32_t aW = tc::smem_addr(sm.W), aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S);
-    const uint32_t aVN = tc::smem_addr(sm.VN), aVNd = tc::smem_addr(sm.VNd);
+    const uint32_t aB20 = tc::smem_addr(sm.B2[0]), aB21 = tc::smem_addr(sm.B2[1]);
+    const uint32_t aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S), aVN = tc::smem_addr(sm.VN);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
     const int nch = (job.t1 - job.t0 + 63) / 64;
     bool ok = true;
     // base descriptors; a K step adds a constant to the start-address field
     const uint64_t dQK0 = tc::desc(aQK0, 16, 1024), dQK1 = tc::desc(aQK1, 16, 1024);
-    const uint64_t dKmn0 = tc::desc(aQK0 + 64 * 128, 128 * 128, 1024), dKmn1 = tc::desc(aQK1 + 64 * 128, 128 * 128, 1024);
-    const uint64_t dA0 = tc::desc(aA0, 16, 1024), dA1 = tc::desc(aA1, 16, 1024);
-    const uint64_t dW = tc::desc(aW, 16, 1024), dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024);
-    const uint64_t dVN = tc::desc(aVN, 16, 1024), dVNd = tc::desc(aVNd, 16, 1024);
+    // K rows as the MN-major A operand of W^T: slot 0 rows 0-63, slot 1 rows 64-127
+    const uint64_t dKmn0 = tc::desc(aQK0, 128 * 128, 1024), dKmn1 = tc::desc(aQK1 + 64 * 128, 128 * 128, 1024);
+    const uint64_t dB20 = tc::desc(aB20, 16, 1024), dB21 = tc::desc(aB21, 16, 1024);
+    const uint64_t dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024), dVN = tc::desc(aVN, 16, 1024);
     const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
 
+    // Q/K of chunk cc into its slot: four 64x64 boxes (128-byte swizzle = the
+    // operand layout); one thread
+    auto issue_qk = [&](int cc) {
+        const int tbn = job.t0 + 64 * cc;
+        const int ss = cc & 1;
+        bf16* qd = sm.QK[ss] + (ss ? 0 : 64 * 64);
+        bf16* kd = sm.QK[ss] + (ss ? 64 * 64 : 0);
+        uint64_t* bar = &sm.ld_qk[ss];
+        tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
+        tc::tma_load_2d(qd, &maps.q, hk * 128, tbn, bar);
+        tc::tma_load_2d(qd + 128 * 64, &maps.q, hk * 128 + 64, tbn, bar);
+        tc::tma_load_2d(kd, &maps.k, hk * 128, tbn, bar);
+        tc::tma_load_2d(kd + 128 * 64, &maps.k, hk * 128 + 64, tbn, bar);
+        sm.qk_issued[ss] += 1;
+    };
+
     if (producer) {
-        // ====================== producer warpgroup ======================
+        // ====================== producer warpgroups ======================
         const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
         uint32_t ph = 0;
@@ -195,23 +336,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
-        // TMA loads: Q/K of chunk cc into its slot (four 64x64 boxes, 128-byte
-        // swizzle = the operand layout), V into the single V tile (two boxes);
-        // g and beta into registers, stored to shared memory at the chunk's start
+        auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool all = tc::bar_and(BAR_P, GS, tc::mbar_wait(bar, parity, kSpin));
+            tc::fence_after();
+            return all;
+        };
+        // g and beta of chunk cc into warp 1's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
-        auto issue_qk = [&](int cc) {
-            const int tbn = job.t0 + 64 * cc;
-            const int vn = min(64, job.t1 - tbn);
-            if (gt == 0) {
-                bf16* QKn = sm.QK[cc & 1];
-                uint64_t* bar = &sm.ld_qk[cc & 1];
-                tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
-                tc::tma_load_2d(QKn, &maps.q, hk * 128, tbn, bar);
-                tc::tma_load_2d(QKn + 128 * 64, &maps.q, hk * 128 + 64, tbn, bar);
-                tc::tma_load_2d(QKn + 64 * 64, &maps.k, hk * 128, tbn, bar);
-                tc::tma_load_2d(QKn + 128 * 64 + 64 * 64, &maps.k, hk * 128 + 64, tbn, bar);
-            }
-            if (warp == 0) {  // lane l: tokens 2l, 2l+1
+        auto load_gb = [&](int cc) {
+            if (warp == 1) {
+                const int tbn = job.t0 + 64 * cc;
+                const int vn = min(64, job.t1 - tbn);
                 const int r0 = 2 * lane, r1 = 2 * lane + 1;
                 const int64_t t0 = tbn + r0, t1 = tbn + r1;
                 g_next0 = r0 < vn ? __ldg(p.g + t0 * p.Hv + hv) : 0.f;
@@ -220,71 +355,103 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 b_next1 = r1 < vn ? __bfloat162float(beta[t1 * p.Hv + hv]) : 0.f;
             }
         };
-        auto issue_v = [&](int cc) {
-            if (gt == 0 && !job.value_zero) {
+        auto issue_v = [&](int cc) {  // one thread
+            if (!job.value_zero) {
                 const int tbn = job.t0 + 64 * cc;
                 tc::mbar_expect_tx(&sm.ld_v, 2 * 64 * 64 * 2);
                 tc::tma_load_2d(sm.V, &maps.v, hv * 128, tbn, &sm.ld_v);
                 tc::tma_load_2d(sm.V + 64 * 64, &maps.v, hv * 128 + 64, tbn, &sm.ld_v);
+                sm.v_issued += 1;
             }
         };
-        auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool all = tc::bar_and(BAR_P, GS, tc::mbar_wait(bar, parity, kSpin));
-            tc::fence_after();
-            return all;
-        };
-        // the Gram product [Q;K][Q;K]^T of the chunk in slot ss (diagonal: the L2 norms)
-        auto issue_gram = [&](int ss) {
+        // Once Q/K of chunk cc have landed: [rows] K^T on the tensor cores;
+        // meanwhile the gate prefix (warp 1) and the L2 norms of the 128 rows
+        // (two threads per row); then the per-row factors and the slot values.
+        auto prep = [&](int cc) {
+            const int ss = cc & 1;
             if (gt == 0) {
+                sm.qk_waited[ss] += 1;
                 tc::fence_after();
+                const uint64_t dA = ss ? dQK1 : dQK0, dB = ss ? dQK1 + (uint64_t)((64 * 128) >> 4) : dQK0;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_GRAM, (ss ? dQK1 : dQK0) + tc::koff(128, kk), (ss ? dQK1 : dQK0) + tc::koff(128, kk),
-                            ID_N128, kk > 0);
+                    tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
                 tc::commit(&sm.mbar_p);
             }
-        };
-        if (nch > 0) {
-            issue_qk(0);
-            issue_v(0);
-            if ((ok = wait_bar(&sm.ld_qk[0], 0))) issue_gram(0);
-            if (warp == 0) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
-        }
-        for (int c = 0; c < nch && ok; ++c) {
-            const int s = c & 1;
-            const int tb = job.t0 + 64 * c;
-            const int valid = min(64, job.t1 - tb);
-            bf16* QKs = sm.QK[s];
-            // the gate prefix of this chunk was formed at the end of the previous one
-            if (!(ok = wait_mma())) break;  // the Gram product of this chunk
-            if (half == 0) {  // 1 / sqrt(|x|^2 + 1e-6) from the diagonal
-                float dg[32];
-                tc::ld32(T_GRAM + lb + (row & ~31), dg);
-                float d = dg[0];
+            if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
+            {  // 1 / sqrt(|x|^2 + 1e-6); rn[0-63] for the Q rows, rn[64-127] for the K rows
+                const int r = gt >> 1, hh = gt & 1;
+                float acc = 0.f;
+                if (l2) {
+                    const bf16* QKn = sm.QK[ss];
 #pragma unroll
-                for (int c2 = 1; c2 < 32; ++c2) d = (c2 == lane) ? dg[c2] : d;
-                const float r = l2 ? rsqrtf(d + 1e-6f) : 1.f;
-                sm.rn[row] = r;
-                const int i = row & 63;
-                const float Gi = sm.G[i], Gr = sm.G[31];
-                if (row < 64) {
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, 8 * hh + ch)]);
+                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 f = __bfloat1622float2(h2[i]);
+                            acc = fmaf(f.x, f.x, acc);
+                            acc = fmaf(f.y, f.y, acc);
+                        }
+                    }
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                const bool qrow = ss ? (r < 64) : (r >= 64);
+                if (hh == 0) sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc + 1e-6f) : 1.f;
+            }
+            tc::bar_sync(BAR_P, GS);
+            if (gt < 128) {
+                const int i = gt & 63;
+                const float r = sm.rn[gt], Gi = sm.G[i], Gr = sm.G[31];
+                if (gt < 64) {
                     sm.rowA[i] = p.scale * r * __expf(Gi - Gr);
                     sm.qf[i] = p.scale * sm.eG[i] * r;
                 } else {
                     sm.colf[i] = r * __expf(Gr - Gi);
                     sm.rowL[i] = sm.beta[i] * r * __expf(Gi - Gr);
                     sm.fbg[i] = sm.beta[i] * sm.eG[i] * r;
+                    sm.slot[ss].fac[i] = sm.eGl[i] * r;
+                }
+                if (gt == 0) {
+                    const int tbn = job.t0 + 64 * cc;
+                    sm.slot[ss].eglast = sm.eG[63];
+                    sm.slot[ss].tb = tbn;
+                    sm.slot[ss].valid = min(64, job.t1 - tbn);
                 }
             }
-            tc::bar_sync(BAR_P, GS);
-            {  // A (rows 0-63) and L (rows 64-127) from the Q K^T / K K^T blocks
+        };
+        // blocks above the diagonal of Tb and Tbg stay zero
+        for (int e = gt; e < 64 * 64 / 8; e += GS) {
+            reinterpret_cast<uint4*>(sm.Tb)[e] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (nch > 0) {
+            if (gt == 32) {
+                issue_qk(0);
+                if (nch > 1) issue_qk(1);
+                issue_v(0);
+            }
+            load_gb(0);
+            if ((ok = wait_bar(&sm.ld_qk[0], 0))) prep(0);
+        }
+        for (int c = 0; c < nch && ok; ++c) {
+            const int s = c & 1;
+            bf16* QKs = sm.QK[s];
+            bf16* B2s = sm.B2[s];
+            const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
+            if (!(ok = wait_mma())) break;  // [rows] K^T of this chunk, and every product issued before it
+            if (gt == 0 && c >= 1) issue_v(c);  // U of the previous chunk has read V
+            if (c + 1 < nch) load_gb(c + 1);
+            {  // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks
+                const bool isq = s ? (row < 64) : (row >= 64);
                 const int i = row & 63;
                 float gv[32];
-                tc::ld32(T_GRAM + lb + 64 + 32 * half, gv);
+                tc::ld32(T_GRAM + lb + 32 * half, gv);
                 float a[32];
+                const int lim = isq ? i : i - 1;  // A keeps the diagonal, L does not
                 if (sm.factored) {
-                    const float fi = row < 64 ? sm.rowA[i] : sm.rowL[i];
-                    const int lim = row < 64 ? i : i - 1;  // A keeps the diagonal, L does not
+                    const float fi = isq ? sm.rowA[i] : sm.rowL[i];
                     const float4* cf = reinterpret_cast<const float4*>(sm.colf + 32 * half);
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
@@ -298,18 +465,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     }
                 } else {  // wide gate range: one exponential per element
                     const float Gi = sm.G[i];
-                    const float fi = row < 64 ? p.scale * sm.rn[i] : sm.beta[i] * sm.rn[row];
-                    const int lim = row < 64 ? i : i - 1;
+                    const float fi = isq ? p.scale * sm.rn[i] : sm.beta[i] * sm.rn[64 + i];
 #pragma unroll
                     for (int c2 = 0; c2 < 32; ++c2) {
                         const int j = 32 * half + c2;
                         a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
                     }
                 }
-                if (row < 64) {
+                if (isq) {
+                    const int arow = (s ? 128 : 0) + i;
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(&sm.Aqk[s][tc::sw128_chunk(64, i, 4 * half + c8)]) = pack8(&a[8 * c8]);
+                        *reinterpret_cast<uint4*>(&B2s[tc::sw128_chunk(192, arow, 4 * half + c8)]) = pack8(&a[8 * c8]);
                 } else {
                     float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * half);
 #pragma unroll
@@ -319,97 +486,81 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_before();
             tc::bar_sync(BAR_P, GS);
-            // the UT inverse on warps 0-3; warps 4-7 rescale Q meanwhile
-            if (gt < 128) {
-                unit_lower_inverse64_rec<LDF>(sm.LT, gt, [] { tc::bar_sync(BAR_PA, 128); });
-            } else if (job.write_o) {
-                for (int e = gt - 128; e < 64 * 16; e += 128) {
-                    const int r = e >> 4, c8 = e & 15;
-                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, r, c8)]);
-                    uint4 raw = *ptr;
-                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-                    const float f = sm.qf[r];
-                    float x[8];
+            if (gt < 128) {  // the UT inverse, straight into Tb and Tbg
+                ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
+            } else {
+                const int g2 = gt - 128;
+                if (job.write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
+                    for (int e = g2; e < 64 * 16; e += 128) {
+                        const int r = e >> 4, c8 = e & 15;
+                        uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
+                        uint4 raw = *ptr;
+                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                        const float f = -sm.qf[r];
+                        float x[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 t2 = __bfloat1622float2(h[i]);
+                            x[2 * i] = t2.x * f;
+                            x[2 * i + 1] = t2.y * f;
+                        }
+                        *ptr = pack8(x);
+                    }
+                }
+                // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
+                const float* fac = sm.slot[s].fac;
+                const int ktrow0 = s ? 0 : 64;
+                for (int t = g2; t < 512; t += 128) {
+                    const int j0 = 2 * (t & 31), ch = t >> 5;
+                    const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
+                    const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
+                    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
+                    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
+                    const float f0 = fac[j0], f1 = fac[j0 + 1];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float2 t2 = __bfloat1622float2(h[i]);
-                        x[2 * i] = t2.x * f;
-                        x[2 * i + 1] = t2.y * f;
+                        const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
+                        const int d = 8 * ch + 2 * i;
+                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
+                            __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
+                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
+                            __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
                     }
-                    *ptr = pack8(x);
                 }
-            }
-            tc::bar_sync(BAR_P, GS);
-            // T diag(beta), T diag(beta e^G / |k|); slot factors
-            for (int e = gt; e < 64 * 8; e += GS) {
-                const int i = e >> 3, c8 = e & 7;
-                const float4* trow = reinterpret_cast<const float4*>(sm.LT + i * LDF + 8 * c8);
-                const float4* bj = reinterpret_cast<const float4*>(sm.beta + 8 * c8);
-                const float4* fj = reinterpret_cast<const float4*>(sm.fbg + 8 * c8);
-                float tbv[8], tbg[8];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const float4 t4 = trow[h2], b4 = bj[h2], f4 = fj[h2];
-                    tbv[4 * h2] = t4.x * b4.x; tbv[4 * h2 + 1] = t4.y * b4.y;
-                    tbv[4 * h2 + 2] = t4.z * b4.z; tbv[4 * h2 + 3] = t4.w * b4.w;
-                    tbg[4 * h2] = t4.x * f4.x; tbg[4 * h2 + 1] = t4.y * f4.y;
-                    tbg[4 * h2 + 2] = t4.z * f4.z; tbg[4 * h2 + 3] = t4.w * f4.w;
-                }
-                *reinterpret_cast<uint4*>(&sm.Tb[tc::sw128_chunk(64, i, c8)]) = pack8(tbv);
-                *reinterpret_cast<uint4*>(&sm.Tbg[tc::sw128_chunk(64, i, c8)]) = pack8(tbg);
-            }
-            if (gt < 64) sm.slot[s].fac[gt] = sm.eGl[gt] * sm.rn[64 + gt];
-            if (gt == 0) {
-                sm.slot[s].eglast = sm.eG[63];
-                sm.slot[s].tb = tb;
-                sm.slot[s].valid = valid;
             }
             tc::fence_async_smem();
             tc::bar_sync(BAR_P, GS);
-            // W^T = K^T Tbg^T, U^T = V^T Tb^T (V of this chunk must have landed)
-            if (!job.value_zero && !(ok = wait_bar(&sm.ld_v, c & 1))) break;
-            if (gt == 0) {
+            // W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the consumer has read the previous W
+            {
+                bool w = true;
+                if (!job.value_zero) w = tc::mbar_wait(&sm.ld_v, c & 1, kSpin);
+                if (w && c >= 1) w = tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin);
+                if (!(ok = tc::bar_and(BAR_P, GS, w))) break;
                 tc::fence_after();
+            }
+            if (gt == 0) {
+                if (!job.value_zero) sm.v_waited += 1;
+                const uint32_t T_U = s ? T_VN1 : T_VN0;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
-                    if (!job.value_zero)
-                        tc::mma((s ? T_U1 : T_U0), dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                    if (!job.value_zero) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                 }
-                tc::commit(&sm.mbar_p);
+                tc::commit(&sm.full[s]);
+                tc::mbar_arrive(&sm.full[s]);
             }
-            // prefetch chunk c+1 while W and U form: its Q/K slot once the
-            // consumer has released it (chunk c-1); V once U no longer reads it
-            if (c + 1 < nch) {
-                if (c >= 1 && !(ok = wait_bar(&sm.empty[s ^ 1], ((c - 1) >> 1) & 1))) break;
-                issue_qk(c + 1);
-            }
-            if (!(ok = wait_mma())) break;
-            if (c + 1 < nch) issue_v(c + 1);
-            // W goes to shared memory once the consumer's v_new of chunk c-1 is done with it
-            if (c >= 1 && !(ok = wait_bar(&sm.wfree, (c - 1) & 1))) break;
-            {
-                float wv[32];
-                const int dch = (row & 63) >> 3;
-                tc::ld32(T_W + lb + 32 * half, wv);
-                bf16* wb = sm.W + (row >> 6) * 64 * 64 + 32 * half * 64 + (row & 7);
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            tc::bar_sync(BAR_P, GS);
-            if (gt == 0) tc::mbar_arrive(&sm.full[s]);
-            // the next chunk's Gram product starts as soon as its Q/K are in,
-            // and its gate prefix is formed meanwhile (this chunk no longer reads G)
+            // the next chunk's products start as soon as its Q/K are in
             if (c + 1 < nch) {
                 if (!(ok = wait_bar(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1))) break;
-                issue_gram(s ^ 1);
-                if (warp == 0) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
+                prep(c + 1);
             }
         }
+        if (tid == 0) {  // every product this thread issued has completed
+            tc::commit(&sm.fin_p);
+            tc::mbar_wait(&sm.fin_p, 0, kSpin);
+        }
     } else {
-        // ====================== consumer warpgroup ======================
+        // ====================== consumer warpgroups ======================
         bf16* __restrict__ o = static_cast<bf16*>(p.o);
         uint32_t ph = 0;
         auto wait_mma = [&]() -> bool {
@@ -432,98 +583,142 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8)
             *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
+        // o columns start at zero (and v_new columns too when no U product writes them)
+        float zero[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2) zero[c2] = 0.f;
+        tc::st32(T_O0 + lb + 32 * half, zero);
+        tc::st32(T_O1 + lb + 32 * half, zero);
+        if (job.value_zero) {
+            tc::st32(T_VN0 + lb + 32 * half, zero);
+            tc::st32(T_VN1 + lb + 32 * half, zero);
+        }
+        tc::wait_st();
         tc::fence_async_smem();
+        tc::fence_before();
         tc::bar_sync(BAR_S, GS);
         const int64_t ostride = (int64_t)p.Hv * 128;
-        auto store_o = [&](int otb, int ovalid) {
-            float ov[32];
-            tc::ld32(T_O + lb + 32 * half, ov);
-            bf16* ob = o + ((int64_t)(otb + 32 * half) * p.Hv + hv) * 128 + row;
-#pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)
-                if (32 * half + c2 < ovalid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
-        };
-        int o_tb = 0, o_valid = 0;
+        int o_tb = 0, o_valid = 0, o_slot = 0;
         bool o_pending = false;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             if (!(ok = tc::bar_and(BAR_S, GS, tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
             tc::fence_after();
-            // v_new^T = U^T - S^T W^T
-            if (gt == 0) {
+            const float eglast = sm.slot[s].eglast;
+            const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
+            bf16* QKs = sm.QK[s];
+            {  // W [token][key column] into the K rows of the slot's Q/K tile
+                float wv[32];
+                tc::ld32(T_W + lb + 32 * half, wv);
+                const int d = row, wrow0 = s ? 64 : 0;
+                bf16* wb = QKs + (d >> 6) * 128 * 64 + (wrow0 + 32 * half) * 64 + (d & 7);
+                const int dch = (d & 63) >> 3;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma((s ? T_U1 : T_U0), dS + tc::koff(128, kk), dW + tc::koff(64, kk), ID_N64_NEG,
-                            (!job.value_zero) || kk > 0);
-                tc::commit(&sm.mbar_s);
-            }
-            if (o_pending) store_o(o_tb, o_valid);  // previous chunk's output, while the MMA runs
-            if (!(ok = wait_mma())) break;
-            if (gt == 0) tc::mbar_arrive(&sm.wfree);
-            {
-                const float* fac = sm.slot[s].fac;
-                float vv[32];
-                tc::ld32((s ? T_U1 : T_U0) + lb + 32 * half, vv);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float d8[8];
-#pragma unroll
-                    for (int c2 = 0; c2 < 8; ++c2) d8[c2] = vv[8 * c8 + c2] * fac[32 * half + 8 * c8 + c2];
-                    *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
-                    *reinterpret_cast<uint4*>(&sm.VNd[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(d8);
-                }
+                for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
             }
             tc::fence_async_smem();
             tc::fence_before();
             tc::bar_sync(BAR_S, GS);
-            // o^T = S^T Q~^T + v_new^T A^T ; dS^T = VNd K
+            if (gt == 0) {
+                tc::mbar_arrive(&sm.wfree);
+                tc::fence_after();
+                // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T  (row order of the slot)
+                const uint32_t D1 = s ? T_O1 : T_VN0;
+                const uint64_t dB = s ? dQK1 : dQK0;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma(D1, dS + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N128_NEG, 1u);
+                tc::commit(&sm.mbar_s);
+            }
+            // while it runs: the previous chunk's output, its o columns back to
+            // zero, and e^{G_last} S^T into the state columns
+            if (o_pending) {
+                float ov[32];
+                const uint32_t T_Op = o_slot ? T_O1 : T_O0;
+                tc::ld32(T_Op + lb + 32 * half, ov);
+                bf16* ob = o + ((int64_t)(o_tb + 32 * half) * p.Hv + hv) * 128 + row;
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2)
+                    if (32 * half + c2 < o_valid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
+            }
+            if (c >= 1) {
+                tc::st32((s ? T_O0 : T_O1) + lb + 32 * half, zero);
+                if (job.value_zero) tc::st32((s ? T_VN0 : T_VN1) + lb + 32 * half, zero);
+            }
+            {
+                float es[32];
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) es[c2] = eglast * Sr[32 * q2 + c2];
+                    tc::st32(T_S + lb + 64 * half + 32 * q2, es);
+                }
+            }
+            tc::wait_st();
+            tc::fence_before();
+            if (!(ok = wait_mma())) break;
+            {  // v_new^T [value column][token] as the A operand of the second product
+                float vv[32];
+                tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::bar_sync(BAR_S, GS);
             if (gt == 0) {
                 tc::fence_after();
-                if (job.write_o) {
+                // [o^T | S^T] += v_new^T [A ; K~^T]^T  (row order of the slot)
+                const uint32_t D2 = s ? T_S : T_O0;
+                const uint64_t dB = s ? dB21 : dB20;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma(T_O, dS + tc::koff(128, kk), (s ? dQK1 : dQK0) + tc::koff(128, kk), ID_N64, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma(T_O, dVN + tc::koff(128, kk), (s ? dA1 : dA0) + tc::koff(64, kk), ID_N64, 1);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc::mma(T_DS, dVNd + tc::koff(128, kk), (s ? dKmn1 : dKmn0) + tc::mnoff(kk), ID_N128_BMN, kk > 0);
+                for (int kk = 0; kk < 4; ++kk) tc::mma(D2, dVN + tc::koff(128, kk), dB + tc::koff(192, kk), ID_N192, 1u);
                 tc::commit(&sm.mbar_s);
             }
             if (!(ok = wait_mma())) break;
-            const float eglast = sm.slot[s].eglast;
-            o_tb = sm.slot[s].tb;
-            o_valid = sm.slot[s].valid;
-            o_pending = job.write_o;
-            tc::fence_before();
-            tc::bar_sync(BAR_S, GS);
-            if (gt == 0) tc::mbar_arrive(&sm.empty[s]);
-            {  // S <- e^{G_last} S + dS
-                float ds[32];
+            // the slot is free: refill it with the Q/K of chunk c + 2
+            if (gt == 0 && c + 2 < nch) issue_qk(c + 2);
+            {  // S <- e^{G_last} S + K~^T v_new, from the state columns
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    tc::ld32(T_DS + lb + 64 * half + 32 * q2, ds);
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) Sr[32 * q2 + c2] = fmaf(eglast, Sr[32 * q2 + c2], ds[c2]);
-                }
+                for (int q2 = 0; q2 < 2; ++q2) tc::ld32(T_S + lb + 64 * half + 32 * q2, &Sr[32 * q2]);
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
                     *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
             }
+            o_tb = tb;
+            o_valid = valid;
+            o_slot = s;
+            o_pending = job.write_o;
             tc::fence_async_smem();
             tc::fence_before();
             tc::bar_sync(BAR_S, GS);
         }
-        if (ok && o_pending) store_o(o_tb, o_valid);
+        if (ok && o_pending) {
+            float ov[32];
+            tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
+            bf16* ob = o + ((int64_t)(o_tb + 32 * half) * p.Hv + hv) * 128 + row;
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2)
+                if (32 * half + c2 < o_valid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
+        }
         if (ok && job.fin) {
 #pragma unroll
             for (int c2 = 0; c2 < 64; ++c2) job.fin[(int64_t)(64 * half + c2) * job.fin_ld + row] = Sr[c2];
         }
+        if (tid == GS) {  // every product this thread issued has completed
+            tc::commit(&sm.fin_s);
+            tc::mbar_wait(&sm.fin_s, 0, kSpin);
+        }
     }
     if (!ok && gt == 0) atomicAdd(&g_gdn_timeouts, 1);
     tc::fence_before();
+    __syncthreads();
+    if (tid == 0) {  // copies still in flight after an early exit land before the memory is released
+        for (int ss = 0; ss < 2; ++ss)
+            if (sm.qk_issued[ss] > sm.qk_waited[ss]) tc::mbar_wait(&sm.ld_qk[ss], (sm.qk_issued[ss] - 1) & 1, kSpin);
+        if (sm.v_issued > sm.v_waited) tc::mbar_wait(&sm.ld_v, (sm.v_issued - 1) & 1, kSpin);
+    }
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
