@@ -92,8 +92,9 @@ struct SmemWS {
     int factored;                  // the split exponentials stay well inside fp32 range
     uint64_t mbar_p, mbar_s;       // tensor-core completion, producer / consumer
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
+    uint64_t gfree;                // the producer has read this chunk's [rows] K^T columns
     uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
-    uint64_t fin_p, fin_s;         // end-of-job drain of each role's products
+    uint64_t fin_p, fin_s, fin_s2; // end-of-job drains of the issuing threads' products
     int qk_issued[2], qk_waited[2], v_issued, v_waited;
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
@@ -181,12 +182,18 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
     if (gtid < 64) {
         const int da = gtid >> 4, dc = gtid & 15;
         float* Lb = blk(da, da);
-        float x[16];
+        float x[16];  // column dc of D_a; rows above dc are exactly zero
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float acc = (i == dc) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc = fmaf(-Lb[i * LDF + m], (m >= dc) ? x[m] : 0.f, acc);
+            for (int m4 = 0; m4 < i; m4 += 4) {
+                const float4 l = *reinterpret_cast<const float4*>(Lb + i * LDF + m4);
+                acc = fmaf(-l.x, x[m4], acc);
+                if (m4 + 1 < i) acc = fmaf(-l.y, x[m4 + 1], acc);
+                if (m4 + 2 < i) acc = fmaf(-l.z, x[m4 + 2], acc);
+                if (m4 + 3 < i) acc = fmaf(-l.w, x[m4 + 3], acc);
+            }
             x[i] = (i >= dc) ? acc : 0.f;
         }
         __syncwarp();
@@ -278,11 +285,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::mbar_init(&sm.full[0], 2);  // the W/U products' commit and a producer thread
         tc::mbar_init(&sm.full[1], 2);
         tc::mbar_init(&sm.wfree, 1);
+        tc::mbar_init(&sm.gfree, 1);
         tc::mbar_init(&sm.ld_qk[0], 1);
         tc::mbar_init(&sm.ld_qk[1], 1);
         tc::mbar_init(&sm.ld_v, 1);
         tc::mbar_init(&sm.fin_p, 1);
         tc::mbar_init(&sm.fin_s, 1);
+        tc::mbar_init(&sm.fin_s2, 1);
         sm.qk_issued[0] = sm.qk_issued[1] = sm.qk_waited[0] = sm.qk_waited[1] = 0;
         sm.v_issued = sm.v_waited = 0;
     }
@@ -336,11 +345,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
-        auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool all = tc::bar_and(BAR_P, GS, tc::mbar_wait(bar, parity, kSpin));
-            tc::fence_after();
-            return all;
-        };
         // g and beta of chunk cc into warp 1's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
         auto load_gb = [&](int cc) {
@@ -364,43 +368,51 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 sm.v_issued += 1;
             }
         };
-        // Once Q/K of chunk cc have landed: [rows] K^T on the tensor cores;
-        // meanwhile the gate prefix (warp 1) and the L2 norms of the 128 rows
-        // (two threads per row); then the per-row factors and the slot values.
-        auto prep = [&](int cc) {
+        // Once chunk cc's Q/K have landed: [rows] K^T on the tensor cores
+        // (thread 224), and the L2 norms of the 128 rows (warps 4-7, one
+        // thread per row; rn[0-63] Q rows, rn[64-127] K rows).  True when the
+        // load arrived.
+        auto issue_gram = [&](int cc) -> bool {
             const int ss = cc & 1;
-            if (gt == 0) {
-                sm.qk_waited[ss] += 1;
-                tc::fence_after();
-                const uint64_t dA = ss ? dQK1 : dQK0, dB = ss ? dQK1 + (uint64_t)((64 * 128) >> 4) : dQK0;
+            if (!tc::mbar_wait(&sm.ld_qk[ss], (cc >> 1) & 1, kSpin)) return false;
+            sm.qk_waited[ss] += 1;
+            tc::fence_after();
+            const uint64_t dA = ss ? dQK1 : dQK0, dB = ss ? dQK1 + (uint64_t)((64 * 128) >> 4) : dQK0;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
-                tc::commit(&sm.mbar_p);
-            }
-            if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
-            {  // 1 / sqrt(|x|^2 + 1e-6); rn[0-63] for the Q rows, rn[64-127] for the K rows
-                const int r = gt >> 1, hh = gt & 1;
-                float acc = 0.f;
-                if (l2) {
-                    const bf16* QKn = sm.QK[ss];
+            for (int kk = 0; kk < 8; ++kk) tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
+            tc::commit(&sm.mbar_p);
+            return true;
+        };
+        auto norms = [&](int cc) -> bool {
+            const int ss = cc & 1;
+            if (!tc::mbar_wait(&sm.ld_qk[ss], (cc >> 1) & 1, kSpin)) return false;
+            const int r = gt - 128;
+            float acc0 = 0.f, acc1 = 0.f;
+            if (l2) {
+                const bf16* QKn = sm.QK[ss];
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, 8 * hh + ch)]);
-                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                for (int ch = 0; ch < 16; ++ch) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, ch)]);
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 f = __bfloat1622float2(h2[i]);
-                            acc = fmaf(f.x, f.x, acc);
-                            acc = fmaf(f.y, f.y, acc);
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __bfloat1622float2(h2[i]);
+                        acc0 = fmaf(f.x, f.x, acc0);
+                        acc1 = fmaf(f.y, f.y, acc1);
                     }
                 }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                const bool qrow = ss ? (r < 64) : (r >= 64);
-                if (hh == 0) sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc + 1e-6f) : 1.f;
             }
-            tc::bar_sync(BAR_P, GS);
+            const bool qrow = ss ? (r < 64) : (r >= 64);
+            sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
+            return true;
+        };
+        // Chunk cc's per-row factors and slot values (its norms are in rn):
+        // the gate prefix on warp 1, then the factors on threads 0-127.
+        // `extra` carries earlier waits into the group's verdict.
+        auto prep = [&](int cc, bool extra) -> bool {
+            const int ss = cc & 1;
+            if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
+            if (!tc::bar_and(BAR_P, GS, extra)) return false;
             if (gt < 128) {
                 const int i = gt & 63;
                 const float r = sm.rn[gt], Gi = sm.G[i], Gr = sm.G[31];
@@ -420,6 +432,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     sm.slot[ss].valid = min(64, job.t1 - tbn);
                 }
             }
+            return true;
         };
         // blocks above the diagonal of Tb and Tbg stay zero
         for (int e = gt; e < 64 * 64 / 8; e += GS) {
@@ -433,15 +446,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 issue_v(0);
             }
             load_gb(0);
-            if ((ok = wait_bar(&sm.ld_qk[0], 0))) prep(0);
+            bool in = true;
+            if (gt >= 128) in = norms(0);
+            if (gt == 224 && in) in = issue_gram(0);
+            ok = prep(0, in);
         }
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
             bf16* QKs = sm.QK[s];
             bf16* B2s = sm.B2[s];
             const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
-            if (!(ok = wait_mma())) break;  // [rows] K^T of this chunk, and every product issued before it
-            if (gt == 0 && c >= 1) issue_v(c);  // U of the previous chunk has read V
+            if (!(ok = wait_mma())) break;  // [rows] K^T of this chunk
+            bool vok = true;
+            if (gt == 0 && c >= 1) {  // V of this chunk once U of the previous one has read V
+                vok = tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
+                if (vok) issue_v(c);
+            }
             if (c + 1 < nch) load_gb(c + 1);
             {  // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks
                 const bool isq = s ? (row < 64) : (row >= 64);
@@ -485,8 +505,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
             }
             tc::fence_before();
-            tc::bar_sync(BAR_P, GS);
-            if (gt < 128) {  // the UT inverse, straight into Tb and Tbg
+            if (!(ok = tc::bar_and(BAR_P, GS, vok))) break;
+            if (gt == 0) tc::mbar_arrive(&sm.gfree);
+            // the UT inverse (warps 0-3, straight into Tb and Tbg); warps 4-7:
+            // -Q~ and K~^T of this chunk and the next chunk's norms (the
+            // consumer issues the next chunk's [rows] K^T once told that its
+            // columns are free)
+            bool nok = true;
+            if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
             } else {
                 const int g2 = gt - 128;
@@ -527,37 +553,41 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                             __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
                     }
                 }
+                if (c + 1 < nch) nok = norms(c + 1);
             }
             tc::fence_async_smem();
-            tc::bar_sync(BAR_P, GS);
-            // W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the consumer has read the previous W
-            {
-                bool w = true;
+            if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
+            // W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the consumer
+            // has read the previous W (thread 0 alone; the others go on to the
+            // next chunk's set-up)
+            bool w = true;
+            if (gt == 0) {
                 if (!job.value_zero) w = tc::mbar_wait(&sm.ld_v, c & 1, kSpin);
                 if (w && c >= 1) w = tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin);
-                if (!(ok = tc::bar_and(BAR_P, GS, w))) break;
-                tc::fence_after();
-            }
-            if (gt == 0) {
-                if (!job.value_zero) sm.v_waited += 1;
-                const uint32_t T_U = s ? T_VN1 : T_VN0;
+                if (w) {
+                    if (!job.value_zero) sm.v_waited += 1;
+                    tc::fence_after();
+                    const uint32_t T_U = s ? T_VN1 : T_VN0;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
-                    if (!job.value_zero) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        if (!job.value_zero)
+                            tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                    }
+                    tc::commit(&sm.full[s]);
+                    tc::mbar_arrive(&sm.full[s]);
                 }
-                tc::commit(&sm.full[s]);
-                tc::mbar_arrive(&sm.full[s]);
             }
-            // the next chunk's products start as soon as its Q/K are in
             if (c + 1 < nch) {
-                if (!(ok = wait_bar(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1))) break;
-                prep(c + 1);
+                if (!(ok = prep(c + 1, w))) break;
+            } else if (!(ok = tc::bar_and(BAR_P, GS, w))) {
+                break;
             }
         }
-        if (tid == 0) {  // every product this thread issued has completed
-            tc::commit(&sm.fin_p);
-            tc::mbar_wait(&sm.fin_p, 0, kSpin);
+        if (gt == 0 || gt == 224) {  // every product these threads issued has completed
+            uint64_t* fb = gt ? &sm.fin_s2 : &sm.fin_p;
+            tc::commit(fb);
+            tc::mbar_wait(fb, 0, kSpin);
         }
     } else {
         // ====================== consumer warpgroups ======================
@@ -597,12 +627,26 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::fence_async_smem();
         tc::fence_before();
         tc::bar_sync(BAR_S, GS);
-        const int64_t ostride = (int64_t)p.Hv * 128;
         int o_tb = 0, o_valid = 0, o_slot = 0;
         bool o_pending = false;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
-            if (!(ok = tc::bar_and(BAR_S, GS, tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
+            // [rows] K^T of chunk c + 1 as soon as its Q/K are in and the producer
+            // has read chunk c's columns (the producer's first wait of chunk c + 1)
+            bool gok = true;
+            if (gt == 0 && c + 1 < nch) {
+                gok = tc::mbar_wait(&sm.gfree, c & 1, kSpin) && tc::mbar_wait(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1, kSpin);
+                if (gok) {
+                    sm.qk_waited[s ^ 1] += 1;
+                    tc::fence_after();
+                    const uint64_t dA = s ? dQK0 : dQK1, dB = s ? dQK0 : dQK1 + (uint64_t)((64 * 128) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
+                    tc::commit(&sm.mbar_p);
+                }
+            }
+            if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
             tc::fence_after();
             const float eglast = sm.slot[s].eglast;
             const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
@@ -630,16 +674,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     tc::mma(D1, dS + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N128_NEG, 1u);
                 tc::commit(&sm.mbar_s);
             }
-            // while it runs: the previous chunk's output, its o columns back to
-            // zero, and e^{G_last} S^T into the state columns
+            // while it runs: the previous chunk's output (through the v_new tile,
+            // free until this chunk's v_new, as [token][value column] rows), its
+            // o columns back to zero, and e^{G_last} S^T into the state columns
             if (o_pending) {
                 float ov[32];
-                const uint32_t T_Op = o_slot ? T_O1 : T_O0;
-                tc::ld32(T_Op + lb + 32 * half, ov);
-                bf16* ob = o + ((int64_t)(o_tb + 32 * half) * p.Hv + hv) * 128 + row;
+                tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
+                bf16* ot = sm.VN + (32 * half) * 128 + row;
 #pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2)
-                    if (32 * half + c2 < o_valid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
+                for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
             }
             if (c >= 1) {
                 tc::st32((s ? T_O0 : T_O1) + lb + 32 * half, zero);
@@ -655,6 +698,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
             }
             tc::wait_st();
+            if (o_pending) {  // 16-byte stores of the staged rows
+                tc::bar_sync(BAR_S, GS);
+                for (int e = gt; e < 64 * 16; e += GS) {
+                    const int t = e >> 4, ch = e & 15;
+                    if (t < o_valid)
+                        *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + hv) * 128 + 8 * ch) =
+                            *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
+                }
+            }
             tc::fence_before();
             if (!(ok = wait_mma())) break;
             {  // v_new^T [value column][token] as the A operand of the second product
@@ -694,13 +746,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_before();
             tc::bar_sync(BAR_S, GS);
         }
-        if (ok && o_pending) {
+        if (ok && o_pending) {  // the last chunk's output, the same way
             float ov[32];
             tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
-            bf16* ob = o + ((int64_t)(o_tb + 32 * half) * p.Hv + hv) * 128 + row;
+            bf16* ot = sm.VN + (32 * half) * 128 + row;
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)
-                if (32 * half + c2 < o_valid) ob[c2 * ostride] = __float2bfloat16_rn(ov[c2]);
+            for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
+            tc::bar_sync(BAR_S, GS);
+            for (int e = gt; e < 64 * 16; e += GS) {
+                const int t = e >> 4, ch = e & 15;
+                if (t < o_valid)
+                    *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + hv) * 128 + 8 * ch) =
+                        *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
+            }
         }
         if (ok && job.fin) {
 #pragma unroll
