@@ -457,11 +457,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             bf16* B2s = sm.B2[s];
             const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
             if (!(ok = wait_mma())) break;  // [rows] K^T of this chunk
-            bool vok = true;
-            if (gt == 0 && c >= 1) {  // V of this chunk once U of the previous one has read V
-                vok = tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
-                if (vok) issue_v(c);
-            }
             if (c + 1 < nch) load_gb(c + 1);
             {  // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks
                 const bool isq = s ? (row < 64) : (row >= 64);
@@ -505,17 +500,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
             }
             tc::fence_before();
-            if (!(ok = tc::bar_and(BAR_P, GS, vok))) break;
+            tc::bar_sync(BAR_P, GS);
             if (gt == 0) tc::mbar_arrive(&sm.gfree);
             // the UT inverse (warps 0-3, straight into Tb and Tbg); warps 4-7:
-            // -Q~ and K~^T of this chunk and the next chunk's norms (the
-            // consumer issues the next chunk's [rows] K^T once told that its
-            // columns are free)
+            // V and -Q~ and K~^T of this chunk
             bool nok = true;
             if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
             } else {
                 const int g2 = gt - 128;
+                if (gt == 224 && c >= 1) {  // V of this chunk once U of the previous one has read V
+                    nok = tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
+                    if (nok) issue_v(c);
+                }
                 if (job.write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
                     for (int e = g2; e < 64 * 16; e += 128) {
                         const int r = e >> 4, c8 = e & 15;
@@ -536,8 +533,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
                 const float* fac = sm.slot[s].fac;
                 const int ktrow0 = s ? 0 : 64;
-                for (int t = g2; t < 512; t += 128) {
-                    const int j0 = 2 * (t & 31), ch = t >> 5;
+                for (int t = g2; t < 512; t += 128) {  // a warp: 16 token pairs x 2 column chunks
+                    const int w4 = t >> 5, ln = t & 31;
+                    const int j0 = 2 * (16 * (w4 >> 3) + (ln & 15)), ch = 2 * (w4 & 7) + (ln >> 4);
                     const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
                     const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
                     const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
@@ -553,7 +551,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                             __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
                     }
                 }
-                if (c + 1 < nch) nok = norms(c + 1);
+
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
@@ -578,7 +576,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     tc::mbar_arrive(&sm.full[s]);
                 }
             }
-            if (c + 1 < nch) {
+            if (c + 1 < nch) {  // the next chunk's norms (warps 4-7) while thread 0 issues
+                if (gt >= 128) w = norms(c + 1);
                 if (!(ok = prep(c + 1, w))) break;
             } else if (!(ok = tc::bar_and(BAR_P, GS, w))) {
                 break;
