@@ -55,6 +55,7 @@ constexpr int LDF = 68;
 constexpr uint32_t kSpin = 1u << 20;  // try_wait polls before a wait is declared stuck
 constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two roles
 constexpr int BAR_PA = 3;             // producer warps 0-3 (the UT inverse)
+constexpr int BAR_Q = 4;              // producer warps 1-7 (while thread 0 issues W and U)
 typedef __nv_bfloat16 bf16;
 
 struct TmaMaps {
@@ -337,14 +338,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         // ====================== producer warpgroups ======================
         const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
-        uint32_t ph = 0;
-        auto wait_mma = [&]() -> bool {
-            const bool done = tc::mbar_wait(&sm.mbar_p, ph, kSpin);
-            ph ^= 1u;
-            const bool all = tc::bar_and(BAR_P, GS, done);
-            tc::fence_after();
-            return all;
-        };
+        uint32_t ph = 0;  // phase of the [rows] K^T completions
         // g and beta of chunk cc into warp 1's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
         auto load_gb = [&](int cc) {
@@ -406,17 +400,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
             return true;
         };
-        // Chunk cc's per-row factors and slot values (its norms are in rn):
-        // the gate prefix on warp 1, then the factors on threads 0-127.
-        // `extra` carries earlier waits into the group's verdict.
+        // Chunk cc's per-row factors and slot values (its norms are in rn), on
+        // warps 1-7 (thread 0 is issuing the previous chunk's W and U): the gate
+        // prefix on warp 1, then the factors on threads 32-159.
         auto prep = [&](int cc, bool extra) -> bool {
             const int ss = cc & 1;
             if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
-            if (!tc::bar_and(BAR_P, GS, extra)) return false;
-            if (gt < 128) {
-                const int i = gt & 63;
-                const float r = sm.rn[gt], Gi = sm.G[i], Gr = sm.G[31];
-                if (gt < 64) {
+            if (!tc::bar_and(BAR_Q, GS - 32, extra)) return false;
+            if (gt >= 32 && gt < 160) {
+                const int f = gt - 32, i = f & 63;
+                const float r = sm.rn[f], Gi = sm.G[i], Gr = sm.G[31];
+                if (f < 64) {
                     sm.rowA[i] = p.scale * r * __expf(Gi - Gr);
                     sm.qf[i] = p.scale * sm.eG[i] * r;
                 } else {
@@ -425,7 +419,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     sm.fbg[i] = sm.beta[i] * sm.eG[i] * r;
                     sm.slot[ss].fac[i] = sm.eGl[i] * r;
                 }
-                if (gt == 0) {
+                if (f == 0) {
                     const int tbn = job.t0 + 64 * cc;
                     sm.slot[ss].eglast = sm.eG[63];
                     sm.slot[ss].tb = tbn;
@@ -439,6 +433,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             reinterpret_cast<uint4*>(sm.Tb)[e] = make_uint4(0u, 0u, 0u, 0u);
             reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
         }
+        bool pend = true;  // this thread's verdict on work whose barrier is still ahead
         if (nch > 0) {
             if (gt == 32) {
                 issue_qk(0);
@@ -446,28 +441,30 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 issue_v(0);
             }
             load_gb(0);
-            bool in = true;
-            if (gt >= 128) in = norms(0);
-            if (gt == 224 && in) in = issue_gram(0);
-            ok = prep(0, in);
+            if (warp != 0) {
+                bool in = true;
+                if (gt >= 128) in = norms(0);
+                if (gt == 224 && in) in = issue_gram(0);
+                pend = prep(0, in);
+            }
         }
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
             bf16* QKs = sm.QK[s];
             bf16* B2s = sm.B2[s];
             const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
-            if (!(ok = wait_mma())) break;  // [rows] K^T of this chunk
-            if (c + 1 < nch) load_gb(c + 1);
-            {  // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks
+            // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks: this
+            // thread's lane, columns [32 hh, 32 hh + 32)
+            auto al_readout = [&](int hh) {
                 const bool isq = s ? (row < 64) : (row >= 64);
                 const int i = row & 63;
                 float gv[32];
-                tc::ld32(T_GRAM + lb + 32 * half, gv);
+                tc::ld32(T_GRAM + lb + 32 * hh, gv);
                 float a[32];
                 const int lim = isq ? i : i - 1;  // A keeps the diagonal, L does not
                 if (sm.factored) {
                     const float fi = isq ? sm.rowA[i] : sm.rowL[i];
-                    const float4* cf = reinterpret_cast<const float4*>(sm.colf + 32 * half);
+                    const float4* cf = reinterpret_cast<const float4*>(sm.colf + 32 * hh);
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 f4 = cf[c4];
@@ -475,7 +472,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int c2 = 4 * c4 + e;
-                            a[c2] = (32 * half + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
+                            a[c2] = (32 * hh + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
                         }
                     }
                 } else {  // wide gate range: one exponential per element
@@ -483,7 +480,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     const float fi = isq ? p.scale * sm.rn[i] : sm.beta[i] * sm.rn[64 + i];
 #pragma unroll
                     for (int c2 = 0; c2 < 32; ++c2) {
-                        const int j = 32 * half + c2;
+                        const int j = 32 * hh + c2;
                         a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
                     }
                 }
@@ -491,17 +488,37 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     const int arow = (s ? 128 : 0) + i;
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(&B2s[tc::sw128_chunk(192, arow, 4 * half + c8)]) = pack8(&a[8 * c8]);
+                        *reinterpret_cast<uint4*>(&B2s[tc::sw128_chunk(192, arow, 4 * hh + c8)]) = pack8(&a[8 * c8]);
                 } else {
-                    float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * half);
+                    float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * hh);
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4)
                         Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
                 }
+            };
+            // warps 1-7: chunk c's [rows] K^T, then A and L (warp 4 also takes
+            // warp 0's lanes); thread 0 meanwhile finishes the previous chunk's
+            // W and U, which must have read Tb and Tbg before the inverse below
+            // rewrites them
+            if (warp != 0) {
+                bool a = pend && tc::mbar_wait(&sm.mbar_p, ph, kSpin);
+                a = tc::bar_and(BAR_Q, GS - 32, a);
+                tc::fence_after();
+                if (a) {
+                    if (c + 1 < nch) load_gb(c + 1);
+                    al_readout(half);
+                    if (warp == 4) al_readout(0);
+                }
+                tc::fence_before();
+                pend = tc::bar_and(BAR_Q, GS - 32, a);
+                if (gt == 32 && pend) tc::mbar_arrive(&sm.gfree);
+            } else if (gt == 0 && c >= 1) {
+                pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
             }
+            ph ^= 1u;
             tc::fence_before();
-            tc::bar_sync(BAR_P, GS);
-            if (gt == 0) tc::mbar_arrive(&sm.gfree);
+            if (!(ok = tc::bar_and(BAR_P, GS, pend))) break;
+            tc::fence_after();
             // the UT inverse (warps 0-3, straight into Tb and Tbg); warps 4-7:
             // V and -Q~ and K~^T of this chunk
             bool nok = true;
@@ -555,12 +572,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
-            // W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the consumer
-            // has read the previous W (thread 0 alone; the others go on to the
-            // next chunk's set-up)
-            bool w = true;
+            // thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the
+            // consumer has read the previous W; warps 1-7: the next chunk's norms
+            // (warps 4-7), gate prefix and factors
             if (gt == 0) {
-                if (!job.value_zero) w = tc::mbar_wait(&sm.ld_v, c & 1, kSpin);
+                bool w = job.value_zero || tc::mbar_wait(&sm.ld_v, c & 1, kSpin);
                 if (w && c >= 1) w = tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin);
                 if (w) {
                     if (!job.value_zero) sm.v_waited += 1;
@@ -575,14 +591,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     tc::commit(&sm.full[s]);
                     tc::mbar_arrive(&sm.full[s]);
                 }
-            }
-            if (c + 1 < nch) {  // the next chunk's norms (warps 4-7) while thread 0 issues
-                if (gt >= 128) w = norms(c + 1);
-                if (!(ok = prep(c + 1, w))) break;
-            } else if (!(ok = tc::bar_and(BAR_P, GS, w))) {
-                break;
+                pend = w;
+            } else if (warp != 0 && c + 1 < nch) {
+                bool in = true;
+                if (gt >= 128) in = norms(c + 1);
+                pend = prep(c + 1, in);
             }
         }
+        if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
         if (gt == 0 || gt == 224) {  // every product these threads issued has completed
             uint64_t* fb = gt ? &sm.fin_s2 : &sm.fin_p;
             tc::commit(fb);
@@ -708,6 +724,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
             tc::fence_before();
             if (!(ok = wait_mma())) break;
+            // the first product was the last reader of the slot's Q/K tile: refill
+            // it with the Q/K of chunk c + 2 (the second product reads only A and K~^T)
+            if (gt == 0 && c + 2 < nch) issue_qk(c + 2);
             {  // v_new^T [value column][token] as the A operand of the second product
                 float vv[32];
                 tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
@@ -728,8 +747,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::commit(&sm.mbar_s);
             }
             if (!(ok = wait_mma())) break;
-            // the slot is free: refill it with the Q/K of chunk c + 2
-            if (gt == 0 && c + 2 < nch) issue_qk(c + 2);
             {  // S <- e^{G_last} S + K~^T v_new, from the state columns
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) tc::ld32(T_S + lb + 64 * half + 32 * q2, &Sr[32 * q2]);
