@@ -64,6 +64,7 @@ struct TmaMaps {
 
 struct SlotSmall {
     float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of K~
+    float qf[64];   // scale e^{G_i} / |q_i|: row factor of Q~
     float eglast;   // e^{G_last}
     int tb, valid;  // first token and valid rows of the chunk
     int pad;
@@ -89,7 +90,6 @@ struct SmemWS {
     __align__(16) float rowA[64];  // scale e^{G_i - G_r} / |q_i|
     __align__(16) float rowL[64];  // beta_i e^{G_i - G_r} / |k_i|
     __align__(16) float fbg[64];   // beta_j e^{G_j} / |k_j|
-    __align__(16) float qf[64];    // scale e^{G_i} / |q_i|
     int factored;                  // the split exponentials stay well inside fp32 range
     uint64_t mbar_p, mbar_s;       // tensor-core completion, producer / consumer
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 const float r = sm.rn[f], Gi = sm.G[i], Gr = sm.G[31];
                 if (f < 64) {
                     sm.rowA[i] = p.scale * r * __expf(Gi - Gr);
-                    sm.qf[i] = p.scale * sm.eG[i] * r;
+                    sm.slot[ss].qf[i] = p.scale * sm.eG[i] * r;
                 } else {
                     sm.colf[i] = r * __expf(Gr - Gi);
                     sm.rowL[i] = sm.beta[i] * r * __expf(Gi - Gr);
@@ -450,9 +450,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         }
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
-            bf16* QKs = sm.QK[s];
             bf16* B2s = sm.B2[s];
-            const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
             // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks: this
             // thread's lane, columns [32 hh, 32 hh + 32)
             auto al_readout = [&](int hh) {
@@ -519,56 +517,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_before();
             if (!(ok = tc::bar_and(BAR_P, GS, pend))) break;
             tc::fence_after();
-            // the UT inverse (warps 0-3, straight into Tb and Tbg); warps 4-7:
-            // V and -Q~ and K~^T of this chunk
+            // the UT inverse (warps 0-3, straight into Tb and Tbg); thread 224:
+            // V of this chunk
             bool nok = true;
             if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
             } else {
-                const int g2 = gt - 128;
                 if (gt == 224 && c >= 1) {  // V of this chunk once U of the previous one has read V
                     nok = tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
                     if (nok) issue_v(c);
                 }
-                if (job.write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
-                    for (int e = g2; e < 64 * 16; e += 128) {
-                        const int r = e >> 4, c8 = e & 15;
-                        uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
-                        uint4 raw = *ptr;
-                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                        const float f = -sm.qf[r];
-                        float x[8];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 t2 = __bfloat1622float2(h[i]);
-                            x[2 * i] = t2.x * f;
-                            x[2 * i + 1] = t2.y * f;
-                        }
-                        *ptr = pack8(x);
-                    }
-                }
-                // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
-                const float* fac = sm.slot[s].fac;
-                const int ktrow0 = s ? 0 : 64;
-                for (int t = g2; t < 512; t += 128) {  // a warp: 16 token pairs x 2 column chunks
-                    const int w4 = t >> 5, ln = t & 31;
-                    const int j0 = 2 * (16 * (w4 >> 3) + (ln & 15)), ch = 2 * (w4 & 7) + (ln >> 4);
-                    const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
-                    const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
-                    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
-                    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
-                    const float f0 = fac[j0], f1 = fac[j0 + 1];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
-                        const int d = 8 * ch + 2 * i;
-                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
-                            __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
-                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
-                            __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
-                    }
-                }
-
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
@@ -666,6 +624,48 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             const float eglast = sm.slot[s].eglast;
             const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
             bf16* QKs = sm.QK[s];
+            bf16* B2s = sm.B2[s];
+            const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
+            // -Q~ in place and K~^T (the K rows are overwritten by W next)
+            if (job.write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
+                for (int e = gt; e < 64 * 16; e += GS) {
+                    const int r = e >> 4, c8 = e & 15;
+                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
+                    uint4 raw = *ptr;
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                    const float f = -sm.slot[s].qf[r];
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 t2 = __bfloat1622float2(h[i]);
+                        x[2 * i] = t2.x * f;
+                        x[2 * i + 1] = t2.y * f;
+                    }
+                    *ptr = pack8(x);
+                }
+            }
+            // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
+            const float* fac = sm.slot[s].fac;
+            const int ktrow0 = s ? 0 : 64;
+            for (int t = gt; t < 512; t += GS) {  // a warp: 16 token pairs x 2 column chunks
+                const int w4 = t >> 5, ln = t & 31;
+                const int j0 = 2 * (16 * (w4 >> 3) + (ln & 15)), ch = 2 * (w4 & 7) + (ln >> 4);
+                const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
+                const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
+                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
+                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
+                const float f0 = fac[j0], f1 = fac[j0 + 1];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
+                    const int d = 8 * ch + 2 * i;
+                    *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
+                        __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
+                    *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
+                        __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
+                }
+            }
+            tc::bar_sync(BAR_S, GS);
             {  // W [token][key column] into the K rows of the slot's Q/K tile
                 float wv[32];
                 tc::ld32(T_W + lb + 32 * half, wv);
