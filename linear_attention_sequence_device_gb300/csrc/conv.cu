@@ -11,14 +11,14 @@
 // shared memory, filled by cp.async: the bytes in flight are bounded by
 // shared memory rather than registers, and since every thread only reads
 // what it copied itself, no block-level synchronisation is needed.
-// Grid: (channel blocks, strips per shard, shards).
+// Grid: (channel blocks, strips per shard, shards), with the strip length
+// chosen at launch so that all CTAs fit in one wave of resident blocks.
 #include "chunk_common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int NT = 128;
-constexpr int R = 128;     // rows per strip
 constexpr int RB = 8;      // rows per batch
 constexpr int NSTAGE = 4;  // batches in the shared-memory ring
 
@@ -30,6 +30,7 @@ struct ConvParams {
     const int32_t* cu; int num_seqs;   // explicit mode (plan == null)
     const void* halo; int halo_len;    // explicit mode
     const int32_t* plan; int P;        // shard mode
+    int rows;                          // rows per strip (a multiple of RB)
 };
 
 template <typename T> struct Vec8;
@@ -109,9 +110,9 @@ __global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
         nloc = p.num_seqs;
         hlen = p.halo_len;
     }
-    const int lt0 = blockIdx.y * R;
+    const int lt0 = blockIdx.y * p.rows;
     if (lt0 >= part) return;
-    const int lt1 = min(part, lt0 + R);
+    const int lt1 = min(part, lt0 + p.rows);
     const T* __restrict__ x = static_cast<const T*>(p.x);
     T* __restrict__ y = static_cast<T*>(p.y);
 
@@ -224,11 +225,35 @@ gdn_status set_smem_attr(const void* func, size_t bytes);
 
 namespace {
 
+// Resident CTAs of the instance on the current device (cached per device).
 template <typename T, int KC>
-gdn_status launch_tk(const ConvParams& p, dim3 grid, cudaStream_t s) {
+int resident_slots(size_t smem) {
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] > 0) return cache[dev];
+    int sms = 0, per = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, conv_kernel<T, KC>, NT, smem) != cudaSuccess)
+        return 0;
+    return cache[dev] = sms * per;
+}
+
+template <typename T, int KC>
+gdn_status launch_tk(ConvParams p, dim3 grid, cudaStream_t s) {
     const size_t smem = (size_t)NSTAGE * RB * (sizeof(T) * 8 / 16) * NT * 16;
     gdn_status st = set_smem_attr((const void*)conv_kernel<T, KC>, smem);
     if (st != GDN_OK) return st;
+    // strips per shard: one wave of resident CTAs over (channel blocks x shards),
+    // strips of at least 64 rows so that the K-1 halo rows stay a small overhead
+    const int part = p.T / p.P;
+    const int slots = resident_slots<T, KC>(smem);
+    const int per = (int)grid.x * p.P;
+    int n = slots > 0 ? max(1, slots / per) : (part + 127) / 128;
+    n = min(n, max(1, part / 64));
+    int rows = (part + n - 1) / n;
+    p.rows = (rows + RB - 1) / RB * RB;
+    grid.y = (part + p.rows - 1) / p.rows;
     conv_kernel<T, KC><<<grid, NT, smem, s>>>(p);
     return check_launch("conv_kernel");
 }
@@ -250,10 +275,10 @@ gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, c
                        const void* b, int Kc, const int32_t* cu, int num_seqs, const void* halo,
                        int halo_len, void* y, int64_t ldy, const int32_t* plan, int P,
                        cudaStream_t s) {
-    ConvParams p{x, ldx, y, ldy, w, b, T, C, Kc, cu, num_seqs, halo, halo_len, plan, plan ? P : 1};
+    ConvParams p{x, ldx, y, ldy, w, b, T, C, Kc, cu, num_seqs, halo, halo_len, plan, plan ? P : 1, 128};
     const int part = T / p.P;
-    dim3 grid((C / 8 + NT - 1) / NT, (part + R - 1) / R, p.P);
-    if (grid.y == 0) return GDN_OK;
+    dim3 grid((C / 8 + NT - 1) / NT, 1, p.P);
+    if (part <= 0) return GDN_OK;
     return dt == GDN_BF16 ? launch_t<__nv_bfloat16>(p, grid, s) : launch_t<float>(p, grid, s);
 }
 
