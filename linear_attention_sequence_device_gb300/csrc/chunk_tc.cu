@@ -647,9 +647,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
             const float* fac = sm.slot[s].fac;
             const int ktrow0 = s ? 0 : 64;
-            for (int t = gt; t < 512; t += GS) {  // a warp: 16 token pairs x 2 column chunks
-                const int w4 = t >> 5, ln = t & 31;
-                const int j0 = 2 * (16 * (w4 >> 3) + (ln & 15)), ch = 2 * (w4 & 7) + (ln >> 4);
+            for (int t = gt; t < 512; t += GS) {
+                // a warp: 2 column chunks x 16 token pairs, the two half-warps on
+                // different token halves (distinct banks for loads and stores)
+                const int w4 = t >> 5, ln = t & 31, hw = ln >> 4;
+                const int j0 = 2 * (16 * ((w4 >> 3) ^ hw) + (ln & 15)), ch = 2 * (w4 & 7) + hw;
                 const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
                 const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
                 const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
