@@ -39,7 +39,8 @@ SIGNATURES = {
                                      _i32, _vp, _i32, _vp, _i64, _vp]),
     "gdn_chunk_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp,
                                      _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _u32,
-                                     _vp, _vp, _vp]),
+                                     _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "gdn_chunk_fwd_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, ctypes.c_int]),
     "gdn_chunk_summary": (ctypes.c_int, [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
                                          _i32, _i32, _i32, _i32, _i32, _i32, _u32, _vp, _vp,
                                          _vp]),
@@ -176,9 +177,12 @@ def gdn_conv_silu(x, w, bias, cu_seqlens, halo=None, halo_len: int = 0, out=None
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, h0=None, scale=None, l2norm=False,
-                  output_final_state=True, out=None):
+                  output_final_state=True, out=None, workspace=None):
     """q, k [T, Hk, dk]; v [T, Hv, dv] (token-strided views allowed); g [T, Hv]
-    fp32; beta [T, Hv]; h0 [N, Hv, dk, dv] fp32.  Returns (o, h_final)."""
+    fp32; beta [T, Hv]; h0 [N, Hv, dk, dv] fp32.  Returns (o, h_final).
+    workspace: a uint8 device tensor of at least chunk_fwd_workspace_size
+    bytes, reused across calls; allocated per call when None; False for none
+    (longest-first job order only)."""
     dt = q.dtype
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
         _need(t, n, dt)
@@ -192,12 +196,25 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, h0=None, scale=None, l2norm=Fals
     o = torch.empty((T, Hv, dv), dtype=dt, device=q.device) if out is None else out
     hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device) \
         if output_final_state else None
-    _check(load().gdn_chunk_fwd(_p(q), _p(k), _p(v), _row_stride(q, "q"), _row_stride(k, "k"),
-                                _row_stride(v, "v"), _dt(q), _p(g.contiguous()),
-                                _p(beta.contiguous()), _p(None if h0 is None else h0.contiguous()),
-                                _p(cu_seqlens), N, T, Hk, Hv, dk, dv, float(scale),
-                                GDN_QK_L2NORM if l2norm else 0, _p(o), _p(hf), _stream()))
+    lib = load()
+    if workspace is None:
+        ws = torch.empty(max(lib.gdn_chunk_fwd_workspace_size(N, Hv, dk, dv, _dt(q)), 16), dtype=torch.uint8,
+                         device=q.device)
+    else:
+        ws = workspace if workspace is not False else None
+    _check(lib.gdn_chunk_fwd(_p(q), _p(k), _p(v), _row_stride(q, "q"), _row_stride(k, "k"),
+                             _row_stride(v, "v"), _dt(q), _p(g.contiguous()),
+                             _p(beta.contiguous()), _p(None if h0 is None else h0.contiguous()),
+                             _p(cu_seqlens), N, T, Hk, Hv, dk, dv, float(scale),
+                             GDN_QK_L2NORM if l2norm else 0, _p(o), _p(hf), _p(ws),
+                             0 if ws is None else ws.numel(), _stream()))
     return o, hf
+
+
+def chunk_fwd_workspace_size(N, Hv, dk, dv, dtype):
+    """Bytes of the optional gdn_chunk_fwd workspace."""
+    code = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}[dtype]
+    return load().gdn_chunk_fwd_workspace_size(N, Hv, dk, dv, code)
 
 
 def gdn_chunk_summary(k, v, g, beta, cu_seqlens, l2norm=False):

@@ -163,10 +163,14 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
                          int64_t ldv, gdn_dtype dtype, const float* g, const void* beta,
                          const float* h0, const int32_t* cu_seqlens, int32_t num_seqs, int32_t T,
                          int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
-                         void* o, float* h_final, void* stream) {
+                         void* o, float* h_final, void* workspace, size_t workspace_bytes, void* stream) {
     gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
     if (st != GDN_OK) return st;
     if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    const size_t need = gdn_chunk_fwd_workspace_size(num_seqs, Hv, dk, dv, dtype);
+    if (workspace && workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace_bytes, need);
+    if (workspace && !al16(workspace)) return fail(GDN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
     if (T > 0) {
         if ((st = check_row(q, ldq, (int64_t)Hk * dk, "q")) != GDN_OK) return st;
         if ((st = check_row(k, ldk, (int64_t)Hk * dk, "k")) != GDN_OK) return st;
@@ -182,8 +186,19 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
+    if (workspace && h_final && T > 0 && chunk_tc_eligible(dtype, dk, dv)) {
+        if (cudaMemsetAsync(workspace, 0, need, (cudaStream_t)stream) != cudaSuccess)
+            return check_launch("workspace clear");
+        p.sched = static_cast<int32_t*>(workspace);
+    }
     dim3 grid(num_seqs, Hv, dv / p.col_tile);
     return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
+}
+
+size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
+    if (num_seqs < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
+    const int tiles = dv / chunk_col_tile(dtype, dk, dv);
+    return align256(sizeof(int32_t) * (2 + (size_t)num_seqs * Hv * (tiles > 0 ? tiles : 1)));
 }
 
 gdn_status gdn_chunk_summary(const void* k, const void* v, int64_t ldk, int64_t ldv, gdn_dtype dtype,
@@ -219,6 +234,12 @@ gdn_status gdn_state_combine(const float* M, const float* N, const float* S0, in
     return launch_combine(M, N, S0, P, Hv, dk, dv, S_in, nullptr, (cudaStream_t)stream);
 }
 
+// pass-1 work order: ticket, pad and one flag per (item, head, tile)
+static size_t pass1_sched_bytes(int num_seqs, int P, int Hv, int dk, int dv, gdn_dtype dtype) {
+    const int tiles = (dv + dk) / chunk_col_tile(dtype, dk, dv);
+    return align256(sizeof(int32_t) * (2 + ((size_t)num_seqs + P) * Hv * tiles));
+}
+
 size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
                                     int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
     if (T < 0 || num_seqs < 1 || n_shards < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
@@ -227,7 +248,8 @@ size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shard
     return align256(sizeof(int32_t) * (size_t)gdn_cp_plan_words(num_seqs, n_shards)) +
            align256((size_t)T * cch * esize(dtype)) +
            2 * align256(carry * dv * sizeof(float)) +  // carry N, S_in
-           align256(carry * dk * sizeof(float));       // carry M
+           align256(carry * dk * sizeof(float)) +      // carry M
+           pass1_sched_bytes(num_seqs, n_shards, Hv, dk, dv, dtype);
 }
 
 gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k,
@@ -271,6 +293,8 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     float* S_in = reinterpret_cast<float*>(ws);
     ws += align256(carry * dv * sizeof(float));
     float* carryM = reinterpret_cast<float*>(ws);
+    ws += align256(carry * dk * sizeof(float));
+    int32_t* sched = reinterpret_cast<int32_t*>(ws);
 
     // 1. plan
     if ((st = launch_plan(cu_seqlens, num_seqs, P, plan, s)) != GDN_OK) return st;
@@ -291,8 +315,14 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     p.sumN = carryN; p.sumM = carryM; p.S_in = S_in; p.plan = plan; p.n_shards = P;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
     {
+        if (chunk_tc_eligible(dtype, dk, dv)) {
+            if (cudaMemsetAsync(sched, 0, pass1_sched_bytes(num_seqs, P, Hv, dk, dv, dtype), s) != cudaSuccess)
+                return check_launch("workspace clear");
+            p.sched = sched;
+        }
         dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
+        p.sched = nullptr;
     }
     if (P > 1) {
         // 4. prefix merge of the shard carries

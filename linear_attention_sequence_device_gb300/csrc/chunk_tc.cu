@@ -137,6 +137,29 @@ __device__ __forceinline__ void gate_prefix_fast(Sm& sm, float g0, float g1, flo
     if (lane == 0) sm.factored = dev < 60.f;
 }
 
+// Flag hand-over between the two halves of a split item (global memory).
+__device__ __forceinline__ void st_release(int32_t* p, int32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Waits (at most about one second) for a released flag; false on expiry.
+__device__ __forceinline__ bool wait_flag(const int32_t* f) {
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        if (ld_acquire(f)) return true;
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > 1000000000ull) return false;
+        __nanosleep(256);
+    }
+    return false;
+}
+
 __device__ __forceinline__ uint4 pack8(const float* f) {
     uint4 r;
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
@@ -268,9 +291,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     extern __shared__ unsigned char smem_raw[];
     SmemWS& sm = *reinterpret_cast<SmemWS*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
     ChunkJob job;
-    int bx, by, bz;
-    lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
+    int bx, by, bz, part = 0, first_chunks = 0, flag = 0;
+    if (p.sched) {
+        const bool splittable = p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1));
+        if (!schedule_pick<NT>(p, src, splittable, sm.lpt_len, &sm.lpt_pick, bx, by, bz, part, first_chunks, flag))
+            return;
+    } else {
+        lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
+    }
     if (!make_job(p, src, job, bx, by, bz)) return;
+    if (part) {  // a half of a split item; its final state destination carries the hand-over
+        const int split_t = job.t0 + 64 * first_chunks;
+        if (part == 1) {
+            job.t1 = split_t;
+        } else {
+            job.t0 = split_t;
+            job.init = job.fin;
+            job.init_ld = job.fin_ld;
+        }
+    }
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp < 8;
@@ -336,6 +375,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 
     if (producer) {
         // ====================== producer warpgroups ======================
+        if (part == 2) {  // start once the first half is done (no wait below can then expire on it)
+            ok = wait_flag(p.sched + 2 + flag);
+            ok = tc::bar_and(BAR_P, GS, ok);
+        }
         const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
         uint32_t ph = 0;  // phase of the [rows] K^T completions
@@ -434,7 +477,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
         }
         bool pend = true;  // this thread's verdict on work whose barrier is still ahead
-        if (nch > 0) {
+        if (nch > 0 && ok) {
             if (gt == 32) {
                 issue_qk(0);
                 if (nch > 1) issue_qk(1);
@@ -573,6 +616,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
+        if (part == 2) {  // the first half's final state is this job's initial state
+            ok = wait_flag(p.sched + 2 + flag);
+            ok = tc::bar_and(BAR_S, GS, ok);
+        }
         // state S^T row `row` (value column), key columns [64 half, 64 half + 64)
         float Sr[64];
 #pragma unroll
@@ -602,7 +649,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::bar_sync(BAR_S, GS);
         int o_tb = 0, o_valid = 0, o_slot = 0;
         bool o_pending = false;
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 0; c < nch && ok; ++c) {
             const int s = c & 1;
             // [rows] K^T of chunk c + 1 as soon as its Q/K are in and the producer
             // has read chunk c's columns (the producer's first wait of chunk c + 1)
@@ -782,6 +829,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 #pragma unroll
             for (int c2 = 0; c2 < 64; ++c2) job.fin[(int64_t)(64 * half + c2) * job.fin_ld + row] = Sr[c2];
         }
+        if (part == 1) {  // hand the state to the second half
+            tc::bar_sync(BAR_S, GS);
+            if (gt == 0 && ok) {
+                __threadfence();
+                st_release(p.sched + 2 + flag, 1);
+            }
+        }
         if (tid == GS) {  // every product this thread issued has completed
             tc::commit(&sm.fin_s);
             tc::mbar_wait(&sm.fin_s, 0, kSpin);
@@ -837,7 +891,7 @@ static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t
     return GDN_OK;
 }
 
-gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_t s) {
+gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
     const size_t smem = sizeof(SmemWS) + 1024;
     gdn_status st = set_smem_attr((const void*)chunk_tc_kernel, smem);
     if (st != GDN_OK) return st;
@@ -847,6 +901,16 @@ gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_
         if ((st = make_map(&maps.q, p.q, p.ldq, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.k, p.k, p.ldk, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
+    }
+    if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the schedule's scratch
+    if (p.sched) {  // chained splitting: two entries per item, SM count for the schedule
+        static int sms[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+            if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+            p.num_sms = sms[dev];
+        }
+        grid.x *= 2;
     }
     chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src, maps);
     return check_launch("chunk_tc_kernel");

@@ -86,6 +86,10 @@ struct ChunkParams {
     const int32_t* plan;    // plan words (shard path)
     int n_shards;
     int col_tile;           // state columns per CTA
+    // chained splitting (tcgen05 kernel): zeroed ints [ticket, pad, flags...]
+    // or null; num_sms sizes the schedule
+    int32_t* sched;
+    int num_sms;
 };
 
 // Resolve a block index (bx = job item, by = value head, bz = state tile)
@@ -269,12 +273,91 @@ __device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* le
     bz = rem / gridDim.y;
 }
 
+// Work order with chained splitting (used when p.sched is set).  CTAs take
+// a ticket in start order.  Items are cut into chunks of C = 64 tokens; with
+// T* = max(longest item, total chunks of all heads and tiles / SMs), an item
+// whose final state has a destination and whose length L satisfies
+// T*/2 < L < 0.9 T* is split into two halves, the second starting from the
+// first's final state (handed over through that destination).  Entries (whole
+// items, first and second halves) are ordered: long wholes and first halves
+// by decreasing length, then short wholes and second halves by decreasing
+// length, each entry repeated for every (head, tile).  Every first half is
+// thus handed out before any second half waits on one.  Cooperative over the
+// CTA; len is shared scratch of kMaxLptItems ints.  Returns false when the
+// ticket has no work.  part: 0 whole, 1 first half, 2 second half;
+// first_chunks: chunks of the first half; flag: index of the item's flag.
+template <int NT>
+__device__ __forceinline__ bool schedule_pick(const ChunkParams& p, int src, bool splittable, int* len, int* pick,
+                                              int& bx, int& by, int& bz, int& part, int& first_chunks, int& flag) {
+    __shared__ int s_ticket, s_max;
+    __shared__ unsigned long long s_sum;
+    const int S = gridDim.x / 2;  // items (the grid holds two entries per item)
+    const int m = gridDim.y * gridDim.z;
+    if (threadIdx.x == 0) {
+        s_ticket = atomicAdd(p.sched, 1);
+        s_max = 0;
+        s_sum = 0ull;
+        *pick = -1;
+    }
+    __syncthreads();
+    const int nvt = p.dv / p.col_tile;
+    for (int x = threadIdx.x; x < S; x += NT) {
+        const int l = job_item_length(p, src, x);
+        const int c = l > 0 ? (l + 63) / 64 : 0;
+        len[x] = c;
+        atomicMax(&s_max, c);
+        atomicAdd(&s_sum, (unsigned long long)c * (unsigned long long)(p.Hv * nvt));
+    }
+    __syncthreads();
+    const int sms = p.num_sms > 0 ? p.num_sms : 1;
+    const long long avg = (long long)((s_sum + sms - 1) / sms);
+    const int tstar = (int)(avg > s_max ? avg : s_max);
+    auto is_split = [&](int L) { return splittable && L >= 2 && 2 * L > tstar && 10 * L < 9 * tstar; };
+    // entry e = 2x + h: h = 0 whole item or first half, h = 1 second half
+    auto entry = [&](int e, int& grp, int& el) -> bool {
+        const int x = e >> 1, h = e & 1, L = len[x];
+        if (is_split(L)) {
+            const int a = (L + 1) / 2;
+            el = h ? L - a : a;
+            grp = h;
+            return true;
+        }
+        if (h) return false;
+        el = L;
+        grp = 2 * L > tstar ? 0 : 1;
+        return true;
+    };
+    const int r = s_ticket / m, rem = s_ticket % m;
+    for (int e = threadIdx.x; e < 2 * S; e += NT) {
+        int ge, le;
+        if (!entry(e, ge, le)) continue;
+        int rank = 0;
+        for (int f = 0; f < 2 * S; ++f) {
+            int gf, lf;
+            if (!entry(f, gf, lf)) continue;
+            rank += (gf < ge) || (gf == ge && (lf > le || (lf == le && f < e)));
+        }
+        if (rank == r) *pick = e;
+    }
+    __syncthreads();
+    const int e = *pick;
+    if (e < 0) return false;
+    bx = e >> 1;
+    by = rem % gridDim.y;
+    bz = rem / gridDim.y;
+    const int L = len[bx];
+    part = is_split(L) ? 1 + (e & 1) : 0;
+    first_chunks = (L + 1) / 2;
+    flag = bx * m + rem;
+    return true;
+}
+
 // launchers (chunk_bf16.cu / chunk_f32.cu)
 gdn_status launch_chunk_bf16(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
 gdn_status launch_chunk_f32(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
 // tcgen05 kernel (chunk_tc.cu): bf16 with d_k = d_v = 128, full-width state tiles
 bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv);
-gdn_status launch_chunk_tc(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
+gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s);
 extern __device__ int g_gdn_timeouts;
 int chunk_col_tile(gdn_dtype dt, int dk, int dv);
 

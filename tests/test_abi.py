@@ -79,7 +79,7 @@ def test_chunk_fwd_host_errors(lib):
         a.update(kw)
         return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["ldq"], a["ldk"], a["ldv"], a["dt"],
                                  FAKE, FAKE, None, FAKE, a["N"], a["T"], a["Hk"], a["Hv"], a["dk"],
-                                 a["dv"], 0.1, 0, FAKE, None, None)
+                                 a["dv"], 0.1, 0, FAKE, None, None, 0, None)
     assert call(ldq=60) == 1          # stride below Hk * dk
     assert call(ldq=68) == 1          # stride not a multiple of 8
     assert call(q=ctypes.c_void_p(4104)) == 1  # misaligned

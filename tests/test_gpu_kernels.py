@@ -177,6 +177,25 @@ def test_chunk_fwd_vs_oracle(case):
     assert_close(f64(hf), hf_ref, w.dtype, "h_final")
 
 
+@pytest.mark.gpu
+def test_chunk_fwd_split_sequences_match_unsplit():
+    """Sequences of 20, 14 and 3 chunks (bf16, d = 128): with a workspace the
+    14-chunk sequence runs as two chained halves (its length lies between half
+    and 0.9 of the longest); both orders match the oracle and no wait expires."""
+    import linear_attention_sequence_device_gb300 as g
+    w = make_chunk_workload(("bf16", 2, 4, 128, 128, (1280, 896, 150), 0.05, 0.5))
+    host, d = chunk_inputs(w)
+    o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                                       host["h0"], w.cu_seqlens(), w.scale)
+    g.binding.device_timeouts(reset=True)
+    for ws in (None, False):  # per-call workspace (splitting) / none (longest-first only)
+        o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"],
+                                workspace=ws)
+        assert_close(f64(o), o_ref, w.dtype, "o")
+        assert_close(f64(hf), hf_ref, w.dtype, "h_final")
+    assert g.binding.device_timeouts() == 0
+
+
 def test_chunk_fwd_strided_views_and_l2norm():
     """q/k/v as column slices of one fused [T, C] buffer; q/k L2-normalised in kernel."""
     import linear_attention_sequence_device_gb300 as g
