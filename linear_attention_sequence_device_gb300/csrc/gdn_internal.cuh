@@ -277,7 +277,7 @@ __device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* le
 // a ticket in start order.  Items are cut into chunks of C = 64 tokens; with
 // T* = max(longest item, total chunks of all heads and tiles / SMs), an item
 // whose final state has a destination and whose length L satisfies
-// T*/2 < L < 0.9 T* is split into two halves, the second starting from the
+// T*/2 < L < 0.7 T* is split into two halves, the second starting from the
 // first's final state (handed over through that destination).  Entries (whole
 // items, first and second halves) are ordered: long wholes and first halves
 // by decreasing length, then short wholes and second halves by decreasing
@@ -312,7 +312,7 @@ __device__ __forceinline__ bool schedule_pick(const ChunkParams& p, int src, boo
     const int sms = p.num_sms > 0 ? p.num_sms : 1;
     const long long avg = (long long)((s_sum + sms - 1) / sms);
     const int tstar = (int)(avg > s_max ? avg : s_max);
-    auto is_split = [&](int L) { return splittable && L >= 2 && 2 * L > tstar && 10 * L < 9 * tstar; };
+    auto is_split = [&](int L) { return splittable && L >= 2 && 2 * L > tstar && 10 * L < 7 * tstar; };
     // entry e = 2x + h: h = 0 whole item or first half, h = 1 second half
     auto entry = [&](int e, int& grp, int& el) -> bool {
         const int x = e >> 1, h = e & 1, L = len[x];
