@@ -19,7 +19,7 @@ namespace gdn {
 namespace {
 
 constexpr int NT = 128;
-constexpr int RB = 8;      // rows per batch
+constexpr int RB = 4;      // rows per batch
 constexpr int NSTAGE = 4;  // batches in the shared-memory ring
 
 struct ConvParams {
