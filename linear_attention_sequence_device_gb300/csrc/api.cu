@@ -186,11 +186,8 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
-    if (workspace && h_final && T > 0 && chunk_tc_eligible(dtype, dk, dv)) {
-        if (cudaMemsetAsync(workspace, 0, need, (cudaStream_t)stream) != cudaSuccess)
-            return check_launch("workspace clear");
-        p.sched = static_cast<int32_t*>(workspace);
-    }
+    if (workspace && h_final && T > 0 && chunk_tc_eligible(dtype, dk, dv))
+        p.sched = static_cast<int32_t*>(workspace);  // filled by the order kernel before the chunk kernel
     dim3 grid(num_seqs, Hv, dv / p.col_tile);
     return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
 }
@@ -198,7 +195,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
 size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
     if (num_seqs < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
     const int tiles = dv / chunk_col_tile(dtype, dk, dv);
-    return align256(sizeof(int32_t) * (2 + (size_t)num_seqs * Hv * (tiles > 0 ? tiles : 1)));
+    return align256(sizeof(int32_t) * chunk_sched_words(num_seqs, Hv * (tiles > 0 ? tiles : 1)));
 }
 
 gdn_status gdn_chunk_summary(const void* k, const void* v, int64_t ldk, int64_t ldv, gdn_dtype dtype,
@@ -234,10 +231,10 @@ gdn_status gdn_state_combine(const float* M, const float* N, const float* S0, in
     return launch_combine(M, N, S0, P, Hv, dk, dv, S_in, nullptr, (cudaStream_t)stream);
 }
 
-// pass-1 work order: ticket, pad and one flag per (item, head, tile)
+// pass-1 work order: ticket, entry count, one flag per (item, head, tile), sorted entries
 static size_t pass1_sched_bytes(int num_seqs, int P, int Hv, int dk, int dv, gdn_dtype dtype) {
     const int tiles = (dv + dk) / chunk_col_tile(dtype, dk, dv);
-    return align256(sizeof(int32_t) * (2 + ((size_t)num_seqs + P) * Hv * tiles));
+    return align256(sizeof(int32_t) * chunk_sched_words(num_seqs + P, Hv * tiles));
 }
 
 size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
@@ -315,11 +312,7 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     p.sumN = carryN; p.sumM = carryM; p.S_in = S_in; p.plan = plan; p.n_shards = P;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
     {
-        if (chunk_tc_eligible(dtype, dk, dv)) {
-            if (cudaMemsetAsync(sched, 0, pass1_sched_bytes(num_seqs, P, Hv, dk, dv, dtype), s) != cudaSuccess)
-                return check_launch("workspace clear");
-            p.sched = sched;
-        }
+        if (chunk_tc_eligible(dtype, dk, dv)) p.sched = sched;  // filled by the order kernel
         dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
         p.sched = nullptr;

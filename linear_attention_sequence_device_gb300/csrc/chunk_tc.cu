@@ -6,13 +6,11 @@
 // (a head dimension).  A tensor-core instruction (K = 16) takes about the
 // same time for N = 64 and N = 256, so products that share their A operand
 // are concatenated along N:
-//   producer, per chunk
-//     [K;Q] K^T or [Q;K] K^T          -> [128 x 64]   the K K^T and Q K^T blocks
-//     W^T = K^T Tbg^T                 -> [128 x 64]   Tbg = T diag(beta e^G / |k|)
-//     U^T = V^T Tb^T                  -> [128 x 64]   Tb  = T diag(beta)
-//   consumer, per chunk
-//     [v_new^T | o^T]  = [U^T | 0] - S^T [W ; -Q~]^T      N = 128, negated A
-//     [o^T | S^T]     += v_new^T [A ; K~^T]^T              N = 192, onto e^{G_last} S^T
+//   [K;Q] K^T or [Q;K] K^T          -> [128 x 64]   the K K^T and Q K^T blocks
+//   W^T = K^T Tbg^T                 -> [128 x 64]   Tbg = T diag(beta e^G / |k|)
+//   U^T = V^T Tb^T                  -> [128 x 64]   Tb  = T diag(beta)
+//   [v_new^T | o^T]  = [U^T | 0] - S^T [W ; -Q~]^T      N = 128, negated A
+//   [o^T | S^T]     += v_new^T [A ; K~^T]^T              N = 192, onto e^{G_last} S^T
 // with Q~ = scale e^G Q / |q|, K~ = diag(e^{G_last - G} / |k|) K and
 // A = scale Q^ K^T o Gamma (lower, diagonal included); the state update
 // S <- e^{G_last} S + K~^T v_new is the last 128 columns of the second product.
@@ -25,13 +23,16 @@
 // Operands sit in shared memory in the 128-byte-swizzled canonical layout.
 //
 // Two roles of two warpgroups each work on different chunks at once:
-//   producer (warps 0-7): loads, [Q;K] K^T, the L2 norms (sums of squares while
-//     that product runs, folded into per-row factors), A and L, the UT inverse
-//     (tf32 mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg),
-//     -Q~ and K~^T, and the W and U products -- for chunk c+1 while
-//   consumer (warps 8-15) runs the state chain of chunk c: W to shared memory,
-//     the two products above, the output, and the state (fp32 in registers,
-//     thread = value row and half the key columns, bf16 copy in shared memory).
+//   producer (warps 0-7), chunk c+1: the L2 norms (sums of squares of the
+//     loaded Q/K rows) and the gate prefix folded into per-row factors, A and L
+//     read from the [Q;K] K^T columns, the UT inverse on warps 0-3 (tf32
+//     mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg) while
+//     warp 7 loads V, then thread 0 issues W and U;
+//   consumer (warps 8-15), chunk c: issues [Q;K] K^T of chunk c+1 as soon as
+//     the producer has read chunk c's columns, builds -Q~ in place and K~^T,
+//     moves W to shared memory, runs the two products above, writes the output
+//     and keeps the state (fp32 in registers, thread = value row and half the
+//     key columns, bf16 copy in shared memory).
 // Q/K tiles, A/K~ tiles, v_new/o columns and per-chunk values are double
 // buffered ("slots"); the consumer refills a slot with the Q/K of chunk c+2
 // as soon as it is done with chunk c.  Every wait is bounded: on expiry the
@@ -292,10 +293,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     SmemWS& sm = *reinterpret_cast<SmemWS*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
     ChunkJob job;
     int bx, by, bz, part = 0, first_chunks = 0, flag = 0;
-    if (p.sched) {
-        const bool splittable = p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1));
-        if (!schedule_pick<NT>(p, src, splittable, sm.lpt_len, &sm.lpt_pick, bx, by, bz, part, first_chunks, flag))
-            return;
+    if (p.sched) {  // two grid entries per item: whole items or halves, by ticket
+        if (!schedule_pick(p, gridDim.x / 2, bx, by, bz, part, first_chunks, flag)) return;
     } else {
         lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
     }
@@ -902,14 +901,18 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         if ((st = make_map(&maps.k, p.k, p.ldk, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
     }
-    if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the schedule's scratch
-    if (p.sched) {  // chained splitting: two entries per item, SM count for the schedule
+    if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the order kernel's scratch
+    if (p.sched) {  // chained splitting: the order of the entries, two grid entries per item
         static int sms[64];
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
             if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
             p.num_sms = sms[dev];
         }
+        const bool splittable =
+            p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1));
+        if ((st = launch_chunk_order(p, src, (int)grid.x, (int)(grid.y * grid.z), splittable, s)) != GDN_OK)
+            return st;
         grid.x *= 2;
     }
     chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src, maps);

@@ -273,84 +273,50 @@ __device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* le
     bz = rem / gridDim.y;
 }
 
-// Work order with chained splitting (used when p.sched is set).  CTAs take
-// a ticket in start order.  Items are cut into chunks of C = 64 tokens; with
-// T* = max(longest item, total chunks of all heads and tiles / SMs), an item
-// whose final state has a destination and whose length L satisfies
-// T*/2 < L < 0.7 T* is split into two halves, the second starting from the
-// first's final state (handed over through that destination).  Entries (whole
-// items, first and second halves) are ordered: long wholes and first halves
-// by decreasing length, then short wholes and second halves by decreasing
-// length, each entry repeated for every (head, tile).  Every first half is
-// thus handed out before any second half waits on one.  Cooperative over the
-// CTA; len is shared scratch of kMaxLptItems ints.  Returns false when the
-// ticket has no work.  part: 0 whole, 1 first half, 2 second half;
-// first_chunks: chunks of the first half; flag: index of the item's flag.
-template <int NT>
-__device__ __forceinline__ bool schedule_pick(const ChunkParams& p, int src, bool splittable, int* len, int* pick,
-                                              int& bx, int& by, int& bz, int& part, int& first_chunks, int& flag) {
-    __shared__ int s_ticket, s_max;
-    __shared__ unsigned long long s_sum;
-    const int S = gridDim.x / 2;  // items (the grid holds two entries per item)
+// Work order with chained splitting (used when p.sched is set): the order
+// kernel (schedule.cu) has sorted the entries of the launch once; a CTA takes
+// a ticket in start order and reads the entry of rank ticket / m, for the
+// (head, tile) pair ticket % m.  Returns false when the ticket has no work.
+// part: 0 whole, 1 first half, 2 second half; first_chunks: chunks of the
+// first half; flag: index of the item's hand-over flag.
+// Offset (in words, even: the entries are read as int2) of the sorted entries.
+__host__ __device__ __forceinline__ int64_t chunk_sched_order_off(int S, int m) {
+    const int64_t o = 2 + (int64_t)S * m;
+    return o + (o & 1);
+}
+__device__ __forceinline__ bool schedule_pick(const ChunkParams& p, int S, int& bx, int& by, int& bz, int& part,
+                                              int& first_chunks, int& flag) {
+    __shared__ int s_pick[4];
     const int m = gridDim.y * gridDim.z;
     if (threadIdx.x == 0) {
-        s_ticket = atomicAdd(p.sched, 1);
-        s_max = 0;
-        s_sum = 0ull;
-        *pick = -1;
-    }
-    __syncthreads();
-    const int nvt = p.dv / p.col_tile;
-    for (int x = threadIdx.x; x < S; x += NT) {
-        const int l = job_item_length(p, src, x);
-        const int c = l > 0 ? (l + 63) / 64 : 0;
-        len[x] = c;
-        atomicMax(&s_max, c);
-        atomicAdd(&s_sum, (unsigned long long)c * (unsigned long long)(p.Hv * nvt));
-    }
-    __syncthreads();
-    const int sms = p.num_sms > 0 ? p.num_sms : 1;
-    const long long avg = (long long)((s_sum + sms - 1) / sms);
-    const int tstar = (int)(avg > s_max ? avg : s_max);
-    auto is_split = [&](int L) { return splittable && L >= 2 && 2 * L > tstar && 10 * L < 7 * tstar; };
-    // entry e = 2x + h: h = 0 whole item or first half, h = 1 second half
-    auto entry = [&](int e, int& grp, int& el) -> bool {
-        const int x = e >> 1, h = e & 1, L = len[x];
-        if (is_split(L)) {
-            const int a = (L + 1) / 2;
-            el = h ? L - a : a;
-            grp = h;
-            return true;
+        const int t = atomicAdd(p.sched, 1);
+        const int n = __ldcg(p.sched + 1);
+        const int r = t / m;
+        s_pick[0] = -1;
+        if (r < n) {
+            const int2 ent = __ldcg(reinterpret_cast<const int2*>(p.sched + chunk_sched_order_off(S, m)) + r);
+            s_pick[0] = ent.x;
+            s_pick[1] = ent.y;
+            s_pick[2] = t % m;
         }
-        if (h) return false;
-        el = L;
-        grp = 2 * L > tstar ? 0 : 1;
-        return true;
-    };
-    const int r = s_ticket / m, rem = s_ticket % m;
-    for (int e = threadIdx.x; e < 2 * S; e += NT) {
-        int ge, le;
-        if (!entry(e, ge, le)) continue;
-        int rank = 0;
-        for (int f = 0; f < 2 * S; ++f) {
-            int gf, lf;
-            if (!entry(f, gf, lf)) continue;
-            rank += (gf < ge) || (gf == ge && (lf > le || (lf == le && f < e)));
-        }
-        if (rank == r) *pick = e;
     }
     __syncthreads();
-    const int e = *pick;
-    if (e < 0) return false;
-    bx = e >> 1;
+    const int ent = s_pick[0];
+    if (ent < 0) return false;
+    const int rem = s_pick[2];
+    bx = ent & 0xffff;
+    part = ent >> 16;
+    first_chunks = s_pick[1];
     by = rem % gridDim.y;
     bz = rem / gridDim.y;
-    const int L = len[bx];
-    part = is_split(L) ? 1 + (e & 1) : 0;
-    first_chunks = (L + 1) / 2;
     flag = bx * m + rem;
     return true;
 }
+
+// schedule.cu: words of a launch's schedule (S items, m head/tile pairs) and
+// the kernel that fills them (zeroed ticket and flags, sorted entries)
+inline size_t chunk_sched_words(int S, int m) { return (size_t)chunk_sched_order_off(S, m) + 4 * (size_t)S; }
+gdn_status launch_chunk_order(const ChunkParams& p, int src, int S, int m, bool splittable, cudaStream_t s);
 
 // launchers (chunk_bf16.cu / chunk_f32.cu)
 gdn_status launch_chunk_bf16(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);

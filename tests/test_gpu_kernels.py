@@ -181,19 +181,72 @@ def test_chunk_fwd_vs_oracle(case):
 def test_chunk_fwd_split_sequences_match_unsplit():
     """Sequences of 20, 13 and 3 chunks (bf16, d = 128): with a workspace the
     13-chunk sequence runs as two chained halves (its length lies between half
-    and 0.7 of the longest); both orders match the oracle and no wait expires."""
+    and 0.7 of the longest); both orders match the oracle and no wait expires.
+    The split falls on a chunk boundary and hands over the fp32 state as is,
+    so the two orders agree bit for bit."""
     import linear_attention_sequence_device_gb300 as g
     w = make_chunk_workload(("bf16", 2, 4, 128, 128, (1280, 800, 150), 0.05, 0.5))
     host, d = chunk_inputs(w)
     o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
                                        host["h0"], w.cu_seqlens(), w.scale)
     g.binding.device_timeouts(reset=True)
+    outs = []
     for ws in (None, False):  # per-call workspace (splitting) / none (longest-first only)
         o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"],
                                 workspace=ws)
         assert_close(f64(o), o_ref, w.dtype, "o")
         assert_close(f64(hf), hf_ref, w.dtype, "h_final")
+        outs.append((o, hf))
     assert g.binding.device_timeouts() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_chunk_fwd_schedule_many_sequences():
+    """300 sequences (bf16, d = 128), most short, a few between half and 0.7 of
+    the longest: the launch's schedule words, read back, hold every item once
+    (whole, or as two halves of the right sizes), longest first within each
+    group with every first half ahead of the second halves, and every ticket
+    was taken; the outputs match the oracle."""
+    import linear_attention_sequence_device_gb300 as g
+    rng = np.random.default_rng(5)
+    lengths = [int(x) for x in rng.integers(0, 121, size=295)] + [4000, 2560, 2560, 2560, 2200]
+    rng.shuffle(lengths)
+    w = make_chunk_workload(("bf16", 1, 2, 128, 128, tuple(lengths), 0.02, 0.0))
+    host, d = chunk_inputs(w)
+    S, m = len(lengths), 2
+    ws = torch.zeros(g.binding.chunk_fwd_workspace_size(S, 2, 128, 128, torch.bfloat16), dtype=torch.uint8,
+                     device=dev())
+    g.binding.device_timeouts(reset=True)
+    o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"], workspace=ws)
+    words = ws.view(torch.int32).cpu().numpy()
+    assert g.binding.device_timeouts() == 0
+    assert words[0] == 2 * S * m                     # every CTA took a ticket
+    n = int(words[1])
+    off = 2 + S * m + ((2 + S * m) & 1)
+    ent = words[off:off + 2 * n].reshape(n, 2)
+    items, parts, first = ent[:, 0] & 0xFFFF, ent[:, 0] >> 16, ent[:, 1]
+    chunks = [(L + 63) // 64 for L in lengths]
+    seen = {}
+    for x, pt in zip(items, parts):
+        seen.setdefault(int(x), []).append(int(pt))
+    assert sorted(seen) == list(range(S))
+    split = [x for x, ps in seen.items() if sorted(ps) == [1, 2]]
+    assert all(ps == [0] or sorted(ps) == [1, 2] for ps in seen.values())
+    assert sorted(chunks[x] for x in split) == [35, 40, 40, 40]
+    size = [chunks[x] if pt == 0 else (f if pt == 1 else chunks[x] - f)
+            for x, pt, f in zip(items, parts, first)]
+    assert all(f == (chunks[x] + 1) // 2 for x, pt, f in zip(items, parts, first) if pt)
+    last_first = max(r for r in range(n) if parts[r] == 1)
+    assert all(r > last_first for r in range(n) if parts[r] == 2)
+    grp = [0 if pt == 1 or (pt == 0 and 2 * chunks[x] > 63) else 1 for x, pt in zip(items, parts)]
+    assert grp == sorted(grp)
+    for r in range(n - 1):
+        if grp[r] == grp[r + 1]:
+            assert size[r] >= size[r + 1]
+    o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                                       host["h0"], w.cu_seqlens(), w.scale)
+    assert_close(f64(o), o_ref, w.dtype, "o")
+    assert_close(f64(hf), hf_ref, w.dtype, "h_final")
 
 
 def test_chunk_fwd_strided_views_and_l2norm():
