@@ -186,8 +186,8 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
-    if (workspace && h_final && T > 0 && chunk_tc_eligible(dtype, dk, dv))
-        p.sched = static_cast<int32_t*>(workspace);  // filled by the order kernel before the chunk kernel
+    if (workspace && T > 0 && chunk_tc_eligible(dtype, dk, dv))
+        p.sched = static_cast<int32_t*>(workspace);  // work queue, filled by the order kernel before the chunk kernel
     dim3 grid(num_seqs, Hv, dv / p.col_tile);
     return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
 }

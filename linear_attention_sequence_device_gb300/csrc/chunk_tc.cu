@@ -26,16 +26,26 @@
 //   producer (warps 0-7), chunk c+1: the L2 norms (sums of squares of the
 //     loaded Q/K rows) and the gate prefix folded into per-row factors, A and L
 //     read from the [Q;K] K^T columns, the UT inverse on warps 0-3 (tf32
-//     mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg) while
-//     warp 7 loads V, then thread 0 issues W and U;
+//     mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg), then
+//     thread 0 issues W and U (it issues V as soon as the previous chunk's U
+//     has read it);
 //   consumer (warps 8-15), chunk c: issues [Q;K] K^T of chunk c+1 as soon as
 //     the producer has read chunk c's columns, builds -Q~ in place and K~^T,
-//     moves W to shared memory, runs the two products above, writes the output
-//     and keeps the state (fp32 in registers, thread = value row and half the
-//     key columns, bf16 copy in shared memory).
+//     moves W to shared memory, runs the two products above and writes the
+//     output.  The fp32 state stays in the state columns of tensor memory
+//     (scaled by e^{G_last} in place before the second product accumulates
+//     onto it); its bf16 copy in shared memory is the first product's A.
 // Q/K tiles, A/K~ tiles, v_new/o columns and per-chunk values are double
 // buffered ("slots"); the consumer refills a slot with the Q/K of chunk c+2
-// as soon as it is done with chunk c.  Every wait is bounded: on expiry the
+// as soon as it is done with chunk c.
+//
+// Work: one job is a token range of one value head.  With a work queue the
+// grid is one persistent CTA per SM; its chunks form one stream over the jobs
+// it takes (by ticket, in the order a separate kernel has sorted), so the
+// pipeline runs on across job boundaries: a job's first chunk loads its
+// initial state, its last stores the final state (a split item's first half
+// hands it to the second half through a release flag).  Without one, every
+// CTA runs the job of its block.  Every wait is bounded: on expiry the
 // kernel counts a timeout, both roles leave their loops, outstanding copies
 // and products are waited for (bounded), and the tensor memory is freed.
 #include <cuda.h>
@@ -71,6 +81,34 @@ struct SlotSmall {
     int pad;
 };
 
+// One job of a CTA's chunk stream (shared memory).  span = {global index of
+// the job's first chunk in the stream, chunks}: one 64-bit word, written
+// last, so a reader scanning the ring sees either a whole old span or the
+// whole new one.
+struct JobRec {
+    int2 span;
+    int t0, t1;        // tokens [t0, t1)
+    int hv, hk, col0;
+    int write_o, value_zero, identity_init;
+    int part, flag;    // split half (0 whole, 1 first, 2 second); hand-over flag index
+    const float* init;
+    float* fin;
+    int64_t init_ld, fin_ld;
+};
+constexpr int kRing = 8;  // jobs in flight per CTA: at most about 5 are live at once
+
+// What the roles need of one chunk of the stream, filled two chunks ahead
+// (entry gq & 7 holds chunk gq; it is overwritten when chunk gq + 8 is filled,
+// by which time both roles are past chunk gq).
+struct ChunkInfo {
+    int tb, valid;      // first token, valid rows
+    int hv, hk;         // value head, key head
+    int vz, write_o;    // value columns zero; o written
+    int first, last;    // first / last chunk of its job
+    int jr;             // ring entry of its job
+    int pad[3];
+};
+
 struct SmemWS {
     bf16 QK[2][128 * 128];  // per slot: Q/K rows (order above); K rows become W, Q rows -Q~
     bf16 B2[2][192 * 64];   // per slot: A (64 rows) and K~^T (128 rows), order above
@@ -101,6 +139,15 @@ struct SmemWS {
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
     int lpt_pick;
+    JobRec ring[kRing];
+    int jn;        // jobs pushed into the ring
+    int jdone;     // jobs the consumer has finished (their entries may be reused)
+    int chunks;    // chunks of the pushed jobs
+    int src_end;   // the job source is exhausted
+    int lpt_left;  // without a work queue: the CTA's one job is still to be pushed
+    int lpt_b[3];
+    int acq_ok;    // the first jobs were pushed without a ring timeout
+    ChunkInfo ci[8];
 };
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
@@ -287,36 +334,151 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
     }
 }
 
+// One thread: pushes jobs into the CTA's ring until the stream holds at
+// least `need` chunks or the source is exhausted.  With a work queue a job is
+// the entry of the next ticket (whole item or half, for one (head, tile)
+// pair); without one, the CTA's own block.  Jobs without work are skipped;
+// with a work queue so are jobs without tokens (their final states are
+// written by a separate kernel).  False when the ring stayed full (a bounded
+// wait for the consumer expired).
+__device__ __noinline__ bool acquire_jobs(const ChunkParams& p, int src, SmemWS& sm, int need) {
+    volatile int* vdone = &sm.jdone;
+    while (!sm.src_end && sm.chunks < need) {
+        if (sm.jn - *vdone >= kRing) {
+            for (uint32_t it = 0; it < kSpin && sm.jn - *vdone >= kRing; ++it) __nanosleep(64);
+            if (sm.jn - *vdone >= kRing) return false;
+        }
+        int bx, by, bz, part = 0, first_chunks = 0, flag = 0;
+        if (p.sched) {
+            const int m = p.sched_m;
+            const int t = atomicAdd(p.sched, 1);
+            const int r = t / m, rem = t - r * m;
+            if (r >= __ldcg(p.sched + 1)) {
+                sm.src_end = 1;
+                break;
+            }
+            const int2 ent =
+                __ldcg(reinterpret_cast<const int2*>(p.sched + chunk_sched_order_off(p.sched_items, m)) + r);
+            bx = ent.x & 0xffff;
+            part = ent.x >> 16;
+            first_chunks = ent.y;
+            by = rem % p.sched_ny;
+            bz = rem / p.sched_ny;
+            flag = bx * m + rem;
+        } else {
+            if (!sm.lpt_left) {
+                sm.src_end = 1;
+                break;
+            }
+            sm.lpt_left = 0;
+            bx = sm.lpt_b[0];
+            by = sm.lpt_b[1];
+            bz = sm.lpt_b[2];
+        }
+        ChunkJob job;
+        if (!make_job(p, src, job, bx, by, bz)) continue;
+        if (part) {  // a half of a split item; its final state destination carries the hand-over
+            const int split_t = job.t0 + 64 * first_chunks;
+            if (part == 1) {
+                job.t1 = split_t;
+            } else {
+                job.t0 = split_t;
+                job.init = job.fin;
+                job.init_ld = job.fin_ld;
+            }
+        }
+        const int nch = (job.t1 - job.t0 + 63) / 64;
+        if (nch == 0 && p.sched) continue;
+        JobRec& J = sm.ring[sm.jn % kRing];
+        J.t0 = job.t0;
+        J.t1 = job.t1;
+        J.hv = job.hv;
+        J.hk = job.hv / (p.Hv / p.Hk);
+        J.col0 = job.col0;
+        J.write_o = job.write_o;
+        J.value_zero = job.value_zero;
+        J.identity_init = job.identity_init;
+        J.part = part;
+        J.flag = flag;
+        J.init = job.init;
+        J.fin = job.fin;
+        J.init_ld = job.init_ld;
+        J.fin_ld = job.fin_ld;
+        __threadfence_block();
+        *reinterpret_cast<volatile unsigned long long*>(&J.span) =
+            ((unsigned long long)(unsigned)nch << 32) | (unsigned)sm.chunks;  // {first chunk, chunks}
+        __threadfence_block();
+        sm.chunks += nch;
+        sm.jn += 1;
+    }
+    return true;
+}
+
+// One thread: the info of chunk gq (already in the stream) from its job.
+__device__ __forceinline__ void fill_chunk_info(SmemWS& sm, int gq) {
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < kRing; ++i) {
+        const int2 sp = sm.ring[i].span;
+        if (gq >= sp.x && gq < sp.x + sp.y) r = i;
+    }
+    const JobRec& J = sm.ring[r];
+    const int c = gq - J.span.x;
+    ChunkInfo& I = sm.ci[gq & 7];
+    I.tb = J.t0 + 64 * c;
+    I.valid = min(64, J.t1 - I.tb);
+    I.hv = J.hv;
+    I.hk = J.hk;
+    I.vz = J.value_zero;
+    I.write_o = J.write_o;
+    I.first = c == 0;
+    I.last = c == J.span.y - 1;
+    I.jr = r;
+}
+
+// With a work queue, sequences without tokens are not queued: the persistent
+// CTAs share them out and write their final states (h0, or 0), all threads.
+__device__ __forceinline__ void empty_sequences_final(const ChunkParams& p, int src) {
+    if (!p.sched || src != JOBS_SEQS || !p.h_final) return;
+    const int64_t sz = (int64_t)p.Hv * p.dk * p.dv;
+    for (int n = blockIdx.x; n < p.num_seqs; n += gridDim.x) {
+        if (__ldg(p.cu + n) != __ldg(p.cu + n + 1)) continue;
+        float* hf = p.h_final + n * sz;
+        const float* h0 = p.h0 ? p.h0 + n * sz : nullptr;
+        for (int64_t e = threadIdx.x; e < sz; e += NT) hf[e] = h0 ? h0[e] : 0.f;
+    }
+}
+
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src,
                                                         const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     SmemWS& sm = *reinterpret_cast<SmemWS*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
-    ChunkJob job;
-    int bx, by, bz, part = 0, first_chunks = 0, flag = 0;
-    if (p.sched) {  // two grid entries per item: whole items or halves, by ticket
-        if (!schedule_pick(p, gridDim.x / 2, bx, by, bz, part, first_chunks, flag)) return;
-    } else {
-        lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
-    }
-    if (!make_job(p, src, job, bx, by, bz)) return;
-    if (part) {  // a half of a split item; its final state destination carries the hand-over
-        const int split_t = job.t0 + 64 * first_chunks;
-        if (part == 1) {
-            job.t1 = split_t;
-        } else {
-            job.t0 = split_t;
-            job.init = job.fin;
-            job.init_ld = job.fin_ld;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    {
+        int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z;
+        if (!p.sched) lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
+        if (tid == 0) {
+            for (int i = 0; i < kRing; ++i) sm.ring[i].span = make_int2(-1, 0);
+            sm.jn = sm.jdone = sm.chunks = sm.src_end = 0;
+            sm.lpt_left = p.sched ? 0 : 1;
+            sm.lpt_b[0] = bx;
+            sm.lpt_b[1] = by;
+            sm.lpt_b[2] = bz;
+            sm.acq_ok = acquire_jobs(p, src, sm, 2) ? 1 : 0;  // the first chunks of the stream
+            for (int gq = 0; gq < 2 && gq < sm.chunks; ++gq) fill_chunk_info(sm, gq);
+        }
+        __syncthreads();
+        if (sm.jn == 0) {  // no work for this CTA
+            empty_sequences_final(p, src);
+            return;
         }
     }
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp < 8;
     const int gt = tid & (GS - 1);  // thread index in its role
     const int row = gt & 127;       // tensor-memory lane = row of every [128 x N] product
     const int half = gt >> 7;       // which half of the columns this thread handles
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-    const int hv = job.hv, hk = hv / (p.Hv / p.Hk);
 
     if (tid == 0) {
         tc::mbar_init(&sm.mbar_p, 1);
@@ -346,8 +508,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     const uint32_t aB20 = tc::smem_addr(sm.B2[0]), aB21 = tc::smem_addr(sm.B2[1]);
     const uint32_t aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S), aVN = tc::smem_addr(sm.VN);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
-    const int nch = (job.t1 - job.t0 + 63) / 64;
-    bool ok = true;
+    bool ok = sm.acq_ok != 0;
     // base descriptors; a K step adds a constant to the start-address field
     const uint64_t dQK0 = tc::desc(aQK0, 16, 1024), dQK1 = tc::desc(aQK1, 16, 1024);
     // K rows as the MN-major A operand of W^T: slot 0 rows 0-63, slot 1 rows 64-127
@@ -356,11 +517,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     const uint64_t dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024), dVN = tc::desc(aVN, 16, 1024);
     const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
 
-    // Q/K of chunk cc into its slot: four 64x64 boxes (128-byte swizzle = the
+    // The CTA's chunks form one stream over its jobs, indexed by gq; every
+    // barrier phase and slot follows gq.  Chunk gq is in the stream once
+    // gq < chunks; the producer keeps the stream (and the chunk infos) two
+    // chunks ahead of the chunk it works on.
+    auto stream_len = [&]() -> int { return *reinterpret_cast<volatile int*>(&sm.chunks); };
+
+    // Q/K of chunk gq into its slot: four 64x64 boxes (128-byte swizzle = the
     // operand layout); one thread
-    auto issue_qk = [&](int cc) {
-        const int tbn = job.t0 + 64 * cc;
-        const int ss = cc & 1;
+    auto issue_qk = [&](int gq, int tbn, int hk) {
+        const int ss = gq & 1;
         bf16* qd = sm.QK[ss] + (ss ? 0 : 64 * 64);
         bf16* kd = sm.QK[ss] + (ss ? 64 * 64 : 0);
         uint64_t* bar = &sm.ld_qk[ss];
@@ -374,19 +540,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 
     if (producer) {
         // ====================== producer warpgroups ======================
-        if (part == 2) {  // start once the first half is done (no wait below can then expire on it)
-            ok = wait_flag(p.sched + 2 + flag);
-            ok = tc::bar_and(BAR_P, GS, ok);
-        }
         const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
         uint32_t ph = 0;  // phase of the [rows] K^T completions
-        // g and beta of chunk cc into warp 1's registers (lane l: tokens 2l, 2l+1)
+        int nvw = 0;      // thread 0: V loads waited for
+        // g and beta of chunk gq into warp 1's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
-        auto load_gb = [&](int cc) {
+        auto load_gb = [&](int gq) {
             if (warp == 1) {
-                const int tbn = job.t0 + 64 * cc;
-                const int vn = min(64, job.t1 - tbn);
+                const ChunkInfo& I = sm.ci[gq & 7];
+                const int tbn = I.tb, hv = I.hv, vn = I.valid;
                 const int r0 = 2 * lane, r1 = 2 * lane + 1;
                 const int64_t t0 = tbn + r0, t1 = tbn + r1;
                 g_next0 = r0 < vn ? __ldg(p.g + t0 * p.Hv + hv) : 0.f;
@@ -395,22 +558,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 b_next1 = r1 < vn ? __bfloat162float(beta[t1 * p.Hv + hv]) : 0.f;
             }
         };
-        auto issue_v = [&](int cc) {  // one thread
-            if (!job.value_zero) {
-                const int tbn = job.t0 + 64 * cc;
+        auto issue_v = [&](int gq) {  // one thread
+            const ChunkInfo& I = sm.ci[gq & 7];
+            if (!I.vz) {
+                const int tbn = I.tb, hv = I.hv;
                 tc::mbar_expect_tx(&sm.ld_v, 2 * 64 * 64 * 2);
                 tc::tma_load_2d(sm.V, &maps.v, hv * 128, tbn, &sm.ld_v);
                 tc::tma_load_2d(sm.V + 64 * 64, &maps.v, hv * 128 + 64, tbn, &sm.ld_v);
                 sm.v_issued += 1;
             }
         };
-        // Once chunk cc's Q/K have landed: [rows] K^T on the tensor cores
-        // (thread 224), and the L2 norms of the 128 rows (warps 4-7, one
-        // thread per row; rn[0-63] Q rows, rn[64-127] K rows).  True when the
-        // load arrived.
-        auto issue_gram = [&](int cc) -> bool {
-            const int ss = cc & 1;
-            if (!tc::mbar_wait(&sm.ld_qk[ss], (cc >> 1) & 1, kSpin)) return false;
+        // Once chunk gq's Q/K have landed: [rows] K^T on the tensor cores (one
+        // thread).  True when the load arrived.
+        auto issue_gram = [&](int gq) -> bool {
+            const int ss = gq & 1;
+            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin)) return false;
             sm.qk_waited[ss] += 1;
             tc::fence_after();
             const uint64_t dA = ss ? dQK1 : dQK0, dB = ss ? dQK1 + (uint64_t)((64 * 128) >> 4) : dQK0;
@@ -419,9 +581,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::commit(&sm.mbar_p);
             return true;
         };
-        auto norms = [&](int cc) -> bool {
-            const int ss = cc & 1;
-            if (!tc::mbar_wait(&sm.ld_qk[ss], (cc >> 1) & 1, kSpin)) return false;
+        // the L2 norms of chunk gq's 128 rows (warps 4-7, one thread per row;
+        // rn[0-63] Q rows, rn[64-127] K rows)
+        auto norms = [&](int gq) -> bool {
+            const int ss = gq & 1;
+            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin)) return false;
             const int r = gt - 128;
             float acc0 = 0.f, acc1 = 0.f;
             if (l2) {
@@ -442,11 +606,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
             return true;
         };
-        // Chunk cc's per-row factors and slot values (its norms are in rn), on
+        // Chunk gq's per-row factors and slot values (its norms are in rn), on
         // warps 1-7 (thread 0 is issuing the previous chunk's W and U): the gate
         // prefix on warp 1, then the factors on threads 32-159.
-        auto prep = [&](int cc, bool extra) -> bool {
-            const int ss = cc & 1;
+        auto prep = [&](int gq, bool extra) -> bool {
+            const int ss = gq & 1;
             if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
             if (!tc::bar_and(BAR_Q, GS - 32, extra)) return false;
             if (gt >= 32 && gt < 160) {
@@ -462,10 +626,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     sm.slot[ss].fac[i] = sm.eGl[i] * r;
                 }
                 if (f == 0) {
-                    const int tbn = job.t0 + 64 * cc;
                     sm.slot[ss].eglast = sm.eG[63];
-                    sm.slot[ss].tb = tbn;
-                    sm.slot[ss].valid = min(64, job.t1 - tbn);
+                    sm.slot[ss].tb = sm.ci[gq & 7].tb;
+                    sm.slot[ss].valid = sm.ci[gq & 7].valid;
                 }
             }
             return true;
@@ -476,10 +639,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
         }
         bool pend = true;  // this thread's verdict on work whose barrier is still ahead
-        if (nch > 0 && ok) {
+        if (stream_len() > 0 && ok) {
             if (gt == 32) {
-                issue_qk(0);
-                if (nch > 1) issue_qk(1);
+                issue_qk(0, sm.ci[0].tb, sm.ci[0].hk);
+                if (stream_len() > 1) issue_qk(1, sm.ci[1].tb, sm.ci[1].hk);
                 issue_v(0);
             }
             load_gb(0);
@@ -490,8 +653,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 pend = prep(0, in);
             }
         }
-        for (int c = 0; c < nch && ok; ++c) {
-            const int s = c & 1;
+        int len = stream_len();  // chunks in the stream as of the last top-up (or all of them)
+        for (int g = 0; g < len && ok; ++g) {
+            const int s = g & 1;
+            const bool vz = gt == 0 && sm.ci[g & 7].vz != 0;  // thread 0: no U product for this chunk
             bf16* B2s = sm.B2[s];
             // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks: this
             // thread's lane, columns [32 hh, 32 hh + 32)
@@ -536,7 +701,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                         Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
                 }
             };
-            // warps 1-7: chunk c's [rows] K^T, then A and L (warp 4 also takes
+            // warps 1-7: chunk g's [rows] K^T, then A and L (warp 4 also takes
             // warp 0's lanes); thread 0 meanwhile finishes the previous chunk's
             // W and U, which must have read Tb and Tbg before the inverse below
             // rewrites them
@@ -545,57 +710,66 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 a = tc::bar_and(BAR_Q, GS - 32, a);
                 tc::fence_after();
                 if (a) {
-                    if (c + 1 < nch) load_gb(c + 1);
+                    if (g + 1 < len) load_gb(g + 1);
                     al_readout(half);
                     if (warp == 4) al_readout(0);
                 }
                 tc::fence_before();
                 pend = tc::bar_and(BAR_Q, GS - 32, a);
                 if (gt == 32 && pend) tc::mbar_arrive(&sm.gfree);
-            } else if (gt == 0 && c >= 1) {
-                pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
+            } else if (gt == 0 && g >= 1) {
+                // the previous chunk's W and U are done: V is free for this chunk's
+                // load, issued now so that it has the A/L readout and the inverse
+                // to land (chunk 0: prologue)
+                pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((g - 1) >> 1) & 1, kSpin);
+                if (pend) issue_v(g);
             }
             ph ^= 1u;
             tc::fence_before();
             if (!(ok = tc::bar_and(BAR_P, GS, pend))) break;
             tc::fence_after();
-            // the UT inverse (warps 0-3, straight into Tb and Tbg); thread 224:
-            // V of this chunk
+            // the UT inverse (warps 0-3, straight into Tb and Tbg); thread 160:
+            // the stream two chunks ahead
             bool nok = true;
             if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
-            } else {
-                if (gt == 224 && c >= 1) {  // V of this chunk once U of the previous one has read V
-                    nok = tc::mbar_wait(&sm.full[s ^ 1], ((c - 1) >> 1) & 1, kSpin);
-                    if (nok) issue_v(c);
-                }
+            } else if (gt == 160) {
+                // the job of chunk g + 2, taken no earlier than the pipeline needs
+                // it (the consumer loads that chunk's Q/K during chunk g; out of
+                // line, once per job), and that chunk's info
+                if (!sm.src_end && sm.chunks < g + 3) nok = acquire_jobs(p, src, sm, g + 3);
+                if (g + 2 < sm.chunks) fill_chunk_info(sm, g + 2);
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
+            len = stream_len();
             // thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the
             // consumer has read the previous W; warps 1-7: the next chunk's norms
             // (warps 4-7), gate prefix and factors
             if (gt == 0) {
-                bool w = job.value_zero || tc::mbar_wait(&sm.ld_v, c & 1, kSpin);
-                if (w && c >= 1) w = tc::mbar_wait(&sm.wfree, (c - 1) & 1, kSpin);
+                bool w = true;
+                if (!vz) {
+                    w = tc::mbar_wait(&sm.ld_v, nvw & 1, kSpin);
+                    nvw += 1;
+                }
+                if (w && g >= 1) w = tc::mbar_wait(&sm.wfree, (g - 1) & 1, kSpin);
                 if (w) {
-                    if (!job.value_zero) sm.v_waited += 1;
+                    if (!vz) sm.v_waited += 1;
                     tc::fence_after();
                     const uint32_t T_U = s ? T_VN1 : T_VN0;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
-                        if (!job.value_zero)
-                            tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        if (!vz) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                     }
                     tc::commit(&sm.full[s]);
                     tc::mbar_arrive(&sm.full[s]);
                 }
                 pend = w;
-            } else if (warp != 0 && c + 1 < nch) {
+            } else if (warp != 0 && g + 1 < len) {
                 bool in = true;
-                if (gt >= 128) in = norms(c + 1);
-                pend = prep(c + 1, in);
+                if (gt >= 128) in = norms(g + 1);
+                pend = prep(g + 1, in);
             }
         }
         if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
@@ -615,200 +789,263 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             return all;
         };
-        if (part == 2) {  // the first half's final state is this job's initial state
-            ok = wait_flag(p.sched + 2 + flag);
-            ok = tc::bar_and(BAR_S, GS, ok);
-        }
-        // state S^T row `row` (value column), key columns [64 half, 64 half + 64)
-        float Sr[64];
+        // The fp32 state lives in the state columns of tensor memory: thread
+        // (row, half) holds S^T row `row` (value column), key columns
+        // [64 half, 64 half + 64), in 32-column pieces q2.
+        // A job's initial state into the state columns and its bf16 copy (the A
+        // operand of the first product) into shared memory.
+        auto load_state = [&](const JobRec& J) {
+            const float* ini = J.init;
+            const int64_t ild = J.init_ld;
+            const bool idi = J.identity_init != 0;
+            const int col0 = J.col0;
 #pragma unroll
-        for (int c2 = 0; c2 < 64; ++c2) {
-            const int d = 64 * half + c2;
-            float s0 = 0.f;
-            if (job.identity_init) s0 = (d == job.col0 + row) ? 1.f : 0.f;
-            else if (job.init) s0 = job.init[(int64_t)d * job.init_ld + row];
-            Sr[c2] = s0;
-        }
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float v[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const int d = 64 * half + 32 * q2 + c2;
+                    float s0 = 0.f;
+                    if (idi) s0 = (d == col0 + row) ? 1.f : 0.f;
+                    else if (ini) s0 = ini[(int64_t)d * ild + row];
+                    v[c2] = s0;
+                }
+                tc::st32(T_S + lb + 64 * half + 32 * q2, v);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 4 * q2 + c8)]) =
+                        pack8(&v[8 * c8]);
+            }
+            tc::wait_st();
+        };
+        auto store_state = [&](const JobRec& J) {  // the job's final state from the state columns
+            float* fin = J.fin;
+            const int64_t fld = J.fin_ld;
+            if (fin) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float v[32];
+                    tc::ld32(T_S + lb + 64 * half + 32 * q2, v);
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) fin[(int64_t)(64 * half + 32 * q2 + c2) * fld + row] = v[c2];
+                }
+            }
+        };
         // o columns start at zero (and v_new columns too when no U product writes them)
         float zero[32];
 #pragma unroll
         for (int c2 = 0; c2 < 32; ++c2) zero[c2] = 0.f;
         tc::st32(T_O0 + lb + 32 * half, zero);
         tc::st32(T_O1 + lb + 32 * half, zero);
-        if (job.value_zero) {
-            tc::st32(T_VN0 + lb + 32 * half, zero);
-            tc::st32(T_VN1 + lb + 32 * half, zero);
-        }
+        if (stream_len() > 0 && sm.ci[0].vz) tc::st32(T_VN0 + lb + 32 * half, zero);
         tc::wait_st();
+        if (stream_len() == 0 && ok) {  // a job without tokens: its final state is its initial state
+            load_state(sm.ring[0]);
+            store_state(sm.ring[0]);
+        }
         tc::fence_async_smem();
         tc::fence_before();
         tc::bar_sync(BAR_S, GS);
-        int o_tb = 0, o_valid = 0, o_slot = 0;
+        int o_tb = 0, o_valid = 0, o_slot = 0, o_hv = 0;
         bool o_pending = false;
-        for (int c = 0; c < nch && ok; ++c) {
-            const int s = c & 1;
-            // [rows] K^T of chunk c + 1 as soon as its Q/K are in and the producer
-            // has read chunk c's columns (the producer's first wait of chunk c + 1)
-            bool gok = true;
-            if (gt == 0 && c + 1 < nch) {
-                gok = tc::mbar_wait(&sm.gfree, c & 1, kSpin) && tc::mbar_wait(&sm.ld_qk[s ^ 1], ((c + 1) >> 1) & 1, kSpin);
-                if (gok) {
-                    sm.qk_waited[s ^ 1] += 1;
-                    tc::fence_after();
-                    const uint64_t dA = s ? dQK0 : dQK1, dB = s ? dQK0 : dQK1 + (uint64_t)((64 * 128) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
-                    tc::commit(&sm.mbar_p);
-                }
+        int g = 0;        // chunk of the stream
+        int len = stream_len();  // chunks in the stream when last read (at least 2 ahead, or all)
+        while (ok && g < len) {
+            // a job: its initial state (a second half waits for the first's final
+            // state), its chunks, its final state
+            const JobRec& J = sm.ring[sm.ci[g & 7].jr];
+            const int nchj = J.span.y, hvj = J.hv;
+            const bool write_o = J.write_o != 0;
+            {
+                bool fl = true;
+                if (J.part == 2) fl = wait_flag(p.sched + 2 + J.flag);
+                if (!(ok = tc::bar_and(BAR_S, GS, fl))) break;
+                load_state(J);
             }
-            if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (c >> 1) & 1, kSpin)))) break;
-            tc::fence_after();
-            const float eglast = sm.slot[s].eglast;
-            const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
-            bf16* QKs = sm.QK[s];
-            bf16* B2s = sm.B2[s];
-            const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
-            // -Q~ in place and K~^T (the K rows are overwritten by W next)
-            if (job.write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
-                for (int e = gt; e < 64 * 16; e += GS) {
-                    const int r = e >> 4, c8 = e & 15;
-                    uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
-                    uint4 raw = *ptr;
-                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                    const float f = -sm.slot[s].qf[r];
-                    float x[8];
+            for (int c = 0; c < nchj && ok; ++c, ++g) {
+                const int s = g & 1;
+                // [rows] K^T of chunk g + 1 as soon as its Q/K are in and the producer
+                // has read chunk g's columns (the producer's first wait of chunk g + 1)
+                bool gok = true;
+                if (gt == 0 && g + 1 < len) {
+                    gok = tc::mbar_wait(&sm.gfree, g & 1, kSpin) && tc::mbar_wait(&sm.ld_qk[s ^ 1], ((g + 1) >> 1) & 1, kSpin);
+                    if (gok) {
+                        sm.qk_waited[s ^ 1] += 1;
+                        tc::fence_after();
+                        const uint64_t dA = s ? dQK0 : dQK1, dB = s ? dQK0 : dQK1 + (uint64_t)((64 * 128) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
+                        tc::commit(&sm.mbar_p);
+                    }
+                }
+                if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (g >> 1) & 1, kSpin)))) break;
+                tc::fence_after();
+                // the producer has topped up the stream for chunk g + 2: what this
+                // chunk needs of the next two, read ahead of use
+                len = stream_len();
+                const bool vz_next = g + 1 < len && sm.ci[(g + 1) & 7].vz;
+                int qk_tb = 0, qk_hk = 0;
+                if (gt == 0 && g + 2 < len) {
+                    qk_tb = sm.ci[(g + 2) & 7].tb;
+                    qk_hk = sm.ci[(g + 2) & 7].hk;
+                }
+                const float eglast = sm.slot[s].eglast;
+                const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
+                bf16* QKs = sm.QK[s];
+                bf16* B2s = sm.B2[s];
+                const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
+                // -Q~ in place and K~^T (the K rows are overwritten by W next)
+                if (write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
+                    for (int e = gt; e < 64 * 16; e += GS) {
+                        const int r = e >> 4, c8 = e & 15;
+                        uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
+                        uint4 raw = *ptr;
+                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                        const float f = -sm.slot[s].qf[r];
+                        float x[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 t2 = __bfloat1622float2(h[i]);
+                            x[2 * i] = t2.x * f;
+                            x[2 * i + 1] = t2.y * f;
+                        }
+                        *ptr = pack8(x);
+                    }
+                }
+                // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
+                const float* fac = sm.slot[s].fac;
+                const int ktrow0 = s ? 0 : 64;
+                for (int t = gt; t < 512; t += GS) {
+                    // a warp: 2 column chunks x 16 token pairs, the two half-warps on
+                    // different token halves (distinct banks for loads and stores)
+                    const int w4 = t >> 5, ln = t & 31, hw = ln >> 4;
+                    const int j0 = 2 * (16 * ((w4 >> 3) ^ hw) + (ln & 15)), ch = 2 * (w4 & 7) + hw;
+                    const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
+                    const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
+                    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
+                    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
+                    const float f0 = fac[j0], f1 = fac[j0 + 1];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float2 t2 = __bfloat1622float2(h[i]);
-                        x[2 * i] = t2.x * f;
-                        x[2 * i + 1] = t2.y * f;
+                        const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
+                        const int d = 8 * ch + 2 * i;
+                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
+                            __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
+                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
+                            __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
                     }
-                    *ptr = pack8(x);
                 }
-            }
-            // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
-            const float* fac = sm.slot[s].fac;
-            const int ktrow0 = s ? 0 : 64;
-            for (int t = gt; t < 512; t += GS) {
-                // a warp: 2 column chunks x 16 token pairs, the two half-warps on
-                // different token halves (distinct banks for loads and stores)
-                const int w4 = t >> 5, ln = t & 31, hw = ln >> 4;
-                const int j0 = 2 * (16 * ((w4 >> 3) ^ hw) + (ln & 15)), ch = 2 * (w4 & 7) + hw;
-                const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
-                const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
-                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
-                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
-                const float f0 = fac[j0], f1 = fac[j0 + 1];
+                tc::bar_sync(BAR_S, GS);
+                {  // W [token][key column] into the K rows of the slot's Q/K tile
+                    float wv[32];
+                    tc::ld32(T_W + lb + 32 * half, wv);
+                    const int d = row, wrow0 = s ? 64 : 0;
+                    bf16* wb = QKs + (d >> 6) * 128 * 64 + (wrow0 + 32 * half) * 64 + (d & 7);
+                    const int dch = (d & 63) >> 3;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
-                    const int d = 8 * ch + 2 * i;
-                    *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
-                        __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
-                    *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
-                        __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
+                    for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
                 }
-            }
-            tc::bar_sync(BAR_S, GS);
-            {  // W [token][key column] into the K rows of the slot's Q/K tile
-                float wv[32];
-                tc::ld32(T_W + lb + 32 * half, wv);
-                const int d = row, wrow0 = s ? 64 : 0;
-                bf16* wb = QKs + (d >> 6) * 128 * 64 + (wrow0 + 32 * half) * 64 + (d & 7);
-                const int dch = (d & 63) >> 3;
+                tc::fence_async_smem();
+                tc::fence_before();
+                tc::bar_sync(BAR_S, GS);
+                if (gt == 0) {
+                    tc::mbar_arrive(&sm.wfree);
+                    tc::fence_after();
+                    // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T  (row order of the slot)
+                    const uint32_t D1 = s ? T_O1 : T_VN0;
+                    const uint64_t dB = s ? dQK1 : dQK0;
 #pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            tc::bar_sync(BAR_S, GS);
-            if (gt == 0) {
-                tc::mbar_arrive(&sm.wfree);
-                tc::fence_after();
-                // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T  (row order of the slot)
-                const uint32_t D1 = s ? T_O1 : T_VN0;
-                const uint64_t dB = s ? dQK1 : dQK0;
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma(D1, dS + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N128_NEG, 1u);
+                    tc::commit(&sm.mbar_s);
+                }
+                // while it runs: the previous chunk's output (through the v_new tile,
+                // free until this chunk's v_new, as [token][value column] rows), its
+                // o columns back to zero, the next chunk's v_new columns to zero when
+                // no U product writes them, and e^{G_last} S^T into the state columns
+                if (o_pending) {
+                    float ov[32];
+                    tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
+                    bf16* ot = sm.VN + (32 * half) * 128 + row;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma(D1, dS + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N128_NEG, 1u);
-                tc::commit(&sm.mbar_s);
-            }
-            // while it runs: the previous chunk's output (through the v_new tile,
-            // free until this chunk's v_new, as [token][value column] rows), its
-            // o columns back to zero, and e^{G_last} S^T into the state columns
-            if (o_pending) {
-                float ov[32];
-                tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
-                bf16* ot = sm.VN + (32 * half) * 128 + row;
+                    for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
+                }
+                if (g >= 1) tc::st32((s ? T_O0 : T_O1) + lb + 32 * half, zero);
+                if (vz_next)
+                    tc::st32((s ? T_VN0 : T_VN1) + lb + 32 * half, zero);
 #pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
-            }
-            if (c >= 1) {
-                tc::st32((s ? T_O0 : T_O1) + lb + 32 * half, zero);
-                if (job.value_zero) tc::st32((s ? T_VN0 : T_VN1) + lb + 32 * half, zero);
-            }
-            {
-                float es[32];
+                for (int q2 = 0; q2 < 2; ++q2) {  // S^T <- e^{G_last} S^T in place
+                    float es[32];
+                    tc::ld32(T_S + lb + 64 * half + 32 * q2, es);
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) es[c2] = eglast * Sr[32 * q2 + c2];
+                    for (int c2 = 0; c2 < 32; ++c2) es[c2] *= eglast;
                     tc::st32(T_S + lb + 64 * half + 32 * q2, es);
                 }
-            }
-            tc::wait_st();
-            if (o_pending) {  // 16-byte stores of the staged rows
+                tc::wait_st();
+                if (o_pending) {  // 16-byte stores of the staged rows
+                    tc::bar_sync(BAR_S, GS);
+                    for (int e = gt; e < 64 * 16; e += GS) {
+                        const int t = e >> 4, ch = e & 15;
+                        if (t < o_valid)
+                            *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + o_hv) * 128 + 8 * ch) =
+                                *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
+                    }
+                }
+                tc::fence_before();
+                if (!(ok = wait_mma())) break;
+                // the first product was the last reader of the slot's Q/K tile: refill
+                // it with the Q/K of chunk g + 2 (the second product reads only A and K~^T)
+                if (gt == 0 && g + 2 < len) issue_qk(g + 2, qk_tb, qk_hk);
+                {  // v_new^T [value column][token] as the A operand of the second product
+                    float vv[32];
+                    tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
+                }
+                tc::fence_async_smem();
+                tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
-                for (int e = gt; e < 64 * 16; e += GS) {
-                    const int t = e >> 4, ch = e & 15;
-                    if (t < o_valid)
-                        *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + hv) * 128 + 8 * ch) =
-                            *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
+                if (gt == 0) {
+                    tc::fence_after();
+                    // [o^T | S^T] += v_new^T [A ; K~^T]^T  (row order of the slot)
+                    const uint32_t D2 = s ? T_S : T_O0;
+                    const uint64_t dB = s ? dB21 : dB20;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc::mma(D2, dVN + tc::koff(128, kk), dB + tc::koff(192, kk), ID_N192, 1u);
+                    tc::commit(&sm.mbar_s);
+                }
+                if (!(ok = wait_mma())) break;
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {  // S <- e^{G_last} S + K~^T v_new: its bf16 copy
+                    float sv[32];
+                    tc::ld32(T_S + lb + 64 * half + 32 * q2, sv);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 4 * q2 + c8)]) =
+                            pack8(&sv[8 * c8]);
+                }
+                o_tb = tb;
+                o_valid = valid;
+                o_slot = s;
+                o_hv = hvj;
+                o_pending = write_o;
+                tc::fence_async_smem();
+                tc::fence_before();
+                tc::bar_sync(BAR_S, GS);
+            }
+            if (!ok) break;
+            store_state(J);
+            if (J.part == 1) {  // hand the final state to the second half
+                tc::bar_sync(BAR_S, GS);
+                if (gt == 0) {
+                    __threadfence();
+                    st_release(p.sched + 2 + J.flag, 1);
                 }
             }
-            tc::fence_before();
-            if (!(ok = wait_mma())) break;
-            // the first product was the last reader of the slot's Q/K tile: refill
-            // it with the Q/K of chunk c + 2 (the second product reads only A and K~^T)
-            if (gt == 0 && c + 2 < nch) issue_qk(c + 2);
-            {  // v_new^T [value column][token] as the A operand of the second product
-                float vv[32];
-                tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
             tc::bar_sync(BAR_S, GS);
-            if (gt == 0) {
-                tc::fence_after();
-                // [o^T | S^T] += v_new^T [A ; K~^T]^T  (row order of the slot)
-                const uint32_t D2 = s ? T_S : T_O0;
-                const uint64_t dB = s ? dB21 : dB20;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma(D2, dVN + tc::koff(128, kk), dB + tc::koff(192, kk), ID_N192, 1u);
-                tc::commit(&sm.mbar_s);
-            }
-            if (!(ok = wait_mma())) break;
-            {  // S <- e^{G_last} S + K~^T v_new, from the state columns
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) tc::ld32(T_S + lb + 64 * half + 32 * q2, &Sr[32 * q2]);
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + c8)]) = pack8(&Sr[8 * c8]);
-            }
-            o_tb = tb;
-            o_valid = valid;
-            o_slot = s;
-            o_pending = job.write_o;
-            tc::fence_async_smem();
-            tc::fence_before();
-            tc::bar_sync(BAR_S, GS);
+            if (gt == 0) *reinterpret_cast<volatile int*>(&sm.jdone) += 1;  // the job's ring entry is free
         }
         if (ok && o_pending) {  // the last chunk's output, the same way
             float ov[32];
@@ -820,19 +1057,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             for (int e = gt; e < 64 * 16; e += GS) {
                 const int t = e >> 4, ch = e & 15;
                 if (t < o_valid)
-                    *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + hv) * 128 + 8 * ch) =
+                    *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + o_hv) * 128 + 8 * ch) =
                         *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
-            }
-        }
-        if (ok && job.fin) {
-#pragma unroll
-            for (int c2 = 0; c2 < 64; ++c2) job.fin[(int64_t)(64 * half + c2) * job.fin_ld + row] = Sr[c2];
-        }
-        if (part == 1) {  // hand the state to the second half
-            tc::bar_sync(BAR_S, GS);
-            if (gt == 0 && ok) {
-                __threadfence();
-                st_release(p.sched + 2 + flag, 1);
             }
         }
         if (tid == GS) {  // every product this thread issued has completed
@@ -850,6 +1076,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     }
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
+    empty_sequences_final(p, src);
 }
 
 }  // namespace
@@ -902,18 +1129,21 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
     }
     if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the order kernel's scratch
-    if (p.sched) {  // chained splitting: the order of the entries, two grid entries per item
+    if (p.sched) {  // work queue: the order of the entries, then one persistent CTA per SM
         static int sms[64];
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
             if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
             p.num_sms = sms[dev];
         }
+        p.sched_items = (int)grid.x;
+        p.sched_m = (int)(grid.y * grid.z);
+        p.sched_ny = (int)grid.y;
         const bool splittable =
             p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1));
-        if ((st = launch_chunk_order(p, src, (int)grid.x, (int)(grid.y * grid.z), splittable, s)) != GDN_OK)
-            return st;
-        grid.x *= 2;
+        if ((st = launch_chunk_order(p, src, p.sched_items, p.sched_m, splittable, s)) != GDN_OK) return st;
+        const long long jobs = 2ll * p.sched_items * p.sched_m;
+        grid = dim3((unsigned)(jobs < p.num_sms ? jobs : (p.num_sms > 0 ? p.num_sms : 1)), 1, 1);
     }
     chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src, maps);
     return check_launch("chunk_tc_kernel");

@@ -86,9 +86,12 @@ struct ChunkParams {
     const int32_t* plan;    // plan words (shard path)
     int n_shards;
     int col_tile;           // state columns per CTA
-    // chained splitting (tcgen05 kernel): zeroed ints [ticket, pad, flags...]
-    // or null; num_sms sizes the schedule
+    // work queue of the tcgen05 kernel (schedule words filled by the order
+    // kernel, or null): the launch's items, (head, tile) pairs per item and
+    // heads (the grid it stands for is items x heads x tiles); num_sms sizes
+    // the schedule and the persistent grid
     int32_t* sched;
+    int sched_items, sched_m, sched_ny;
     int num_sms;
 };
 
@@ -273,46 +276,12 @@ __device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* le
     bz = rem / gridDim.y;
 }
 
-// Work order with chained splitting (used when p.sched is set): the order
-// kernel (schedule.cu) has sorted the entries of the launch once; a CTA takes
-// a ticket in start order and reads the entry of rank ticket / m, for the
-// (head, tile) pair ticket % m.  Returns false when the ticket has no work.
-// part: 0 whole, 1 first half, 2 second half; first_chunks: chunks of the
-// first half; flag: index of the item's hand-over flag.
-// Offset (in words, even: the entries are read as int2) of the sorted entries.
+// Offset (in words, even: the entries are read as int2) of the sorted entries
+// in the schedule words.
 __host__ __device__ __forceinline__ int64_t chunk_sched_order_off(int S, int m) {
     const int64_t o = 2 + (int64_t)S * m;
     return o + (o & 1);
 }
-__device__ __forceinline__ bool schedule_pick(const ChunkParams& p, int S, int& bx, int& by, int& bz, int& part,
-                                              int& first_chunks, int& flag) {
-    __shared__ int s_pick[4];
-    const int m = gridDim.y * gridDim.z;
-    if (threadIdx.x == 0) {
-        const int t = atomicAdd(p.sched, 1);
-        const int n = __ldcg(p.sched + 1);
-        const int r = t / m;
-        s_pick[0] = -1;
-        if (r < n) {
-            const int2 ent = __ldcg(reinterpret_cast<const int2*>(p.sched + chunk_sched_order_off(S, m)) + r);
-            s_pick[0] = ent.x;
-            s_pick[1] = ent.y;
-            s_pick[2] = t % m;
-        }
-    }
-    __syncthreads();
-    const int ent = s_pick[0];
-    if (ent < 0) return false;
-    const int rem = s_pick[2];
-    bx = ent & 0xffff;
-    part = ent >> 16;
-    first_chunks = s_pick[1];
-    by = rem % gridDim.y;
-    bz = rem / gridDim.y;
-    flag = bx * m + rem;
-    return true;
-}
-
 // schedule.cu: words of a launch's schedule (S items, m head/tile pairs) and
 // the kernel that fills them (zeroed ticket and flags, sorted entries)
 inline size_t chunk_sched_words(int S, int m) { return (size_t)chunk_sched_order_off(S, m) + 4 * (size_t)S; }

@@ -156,6 +156,8 @@ CHUNK_CASES = [
     # range inside a chunk exceeds what split exponentials can hold in fp32
     ("bf16", 2, 2, 128, 128, (300, 77), 0.05, 4.0),
     ("bf16", 1, 2, 128, 128, (190,), 0.0, 1.5),
+    # empty sequences on the tensor-core path: their final state is h0
+    ("bf16", 2, 2, 128, 128, (0, 130, 0, 70, 0), 0.05, 0.0),
 ]
 
 
@@ -170,7 +172,9 @@ def test_chunk_fwd_vs_oracle(case):
     import linear_attention_sequence_device_gb300 as g
     w = make_chunk_workload(case)
     host, d = chunk_inputs(w)
+    g.binding.device_timeouts(reset=True)
     o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"])
+    assert g.binding.device_timeouts() == 0
     o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
                                        host["h0"], w.cu_seqlens(), w.scale)
     assert_close(f64(o), o_ref, w.dtype, "o")
@@ -205,8 +209,9 @@ def test_chunk_fwd_schedule_many_sequences():
     """300 sequences (bf16, d = 128), most short, a few between half and 0.7 of
     the longest: the launch's schedule words, read back, hold every item once
     (whole, or as two halves of the right sizes), longest first within each
-    group with every first half ahead of the second halves, and every ticket
-    was taken; the outputs match the oracle."""
+    group with every first half ahead of the second halves, and each of the
+    persistent CTAs (one per SM) took every ticket it ran plus one past the
+    end; the outputs match the oracle."""
     import linear_attention_sequence_device_gb300 as g
     rng = np.random.default_rng(5)
     lengths = [int(x) for x in rng.integers(0, 121, size=295)] + [4000, 2560, 2560, 2560, 2200]
@@ -220,8 +225,9 @@ def test_chunk_fwd_schedule_many_sequences():
     o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"], workspace=ws)
     words = ws.view(torch.int32).cpu().numpy()
     assert g.binding.device_timeouts() == 0
-    assert words[0] == 2 * S * m                     # every CTA took a ticket
     n = int(words[1])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert words[0] == n * m + min(sms, 2 * S * m)   # one ticket past the end per CTA
     off = 2 + S * m + ((2 + S * m) & 1)
     ent = words[off:off + 2 * n].reshape(n, 2)
     items, parts, first = ent[:, 0] & 0xFFFF, ent[:, 0] >> 16, ent[:, 1]
