@@ -180,13 +180,15 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, int64_t ld
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of the optional gdn_chunk_fwd workspace (device, 16-byte aligned,
- * contents on entry irrelevant; the call clears it on its stream).  With a
- * workspace and h_final, the bf16 d=128 kernel may split a long sequence's
- * token range into two halves run one after the other on different SMs (the
- * second starts from the first's final state, handed over through h_final),
- * so that the work packs more evenly onto the SMs; results do not change
- * beyond rounding order.  Without one the job order is longest-first only.
- * A workspace smaller than this size is an error (GDN_ERR_WORKSPACE). */
+ * contents on entry irrelevant; the call rewrites it on its stream).  With a
+ * workspace, the bf16 d=128 kernel takes its (sequence, head) jobs from a
+ * work queue sorted longest-first, one persistent block per SM; with h_final
+ * as well it may split a long sequence's token range into two halves run one
+ * after the other (the second starts from the first's final state, handed
+ * over through h_final), so that the work packs more evenly onto the SMs.
+ * Results are bit-identical with and without a workspace.  Without one every
+ * block runs one job, longest first.  A workspace smaller than this size is
+ * an error (GDN_ERR_WORKSPACE). */
 size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int32_t Hv, int32_t dk, int32_t dv,
                                     gdn_dtype dtype);
 
