@@ -1,11 +1,12 @@
 // bf16 chunk kernel for d_k = d_v = 128 on the 5th-generation tensor cores
 // (tcgen05.mma, accumulators in tensor memory).
 //
-// One CTA runs one job: a token range of one value head with the full
+// A CTA runs jobs: a job is a token range of one value head with the full
 // 128-column state, chunk after chunk (C = 64).  Every product has M = 128
-// (a head dimension).  A tensor-core instruction (K = 16) takes about the
-// same time for N = 64 and N = 256, so products that share their A operand
-// are concatenated along N:
+// (a head dimension).  A tensor-core instruction (K = 16) costs a fixed
+// ~50 cycles to issue from one thread and ~65 cycles of pipe time at N = 64
+// against ~150 at N = 256, so products that share their A operand are
+// concatenated along N (fewer instructions for the same work):
 //   [K;Q] K^T or [Q;K] K^T          -> [128 x 64]   the K K^T and Q K^T blocks
 //   W^T = K^T Tbg^T                 -> [128 x 64]   Tbg = T diag(beta e^G / |k|)
 //   U^T = V^T Tb^T                  -> [128 x 64]   Tb  = T diag(beta)
