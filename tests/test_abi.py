@@ -87,6 +87,26 @@ def test_chunk_fwd_host_errors(lib):
     assert call(dv=96) == 2
 
 
+def test_chunk_fwd_workspace_contract(lib):
+    """The optional work-queue workspace: its size is a multiple of 256 bytes
+    that grows with the sequence count (0 for invalid arguments); a smaller or
+    misaligned workspace is rejected on the host before any launch."""
+    size = lambda n, hv=4, d=128, dt=1: lib.gdn_chunk_fwd_workspace_size(n, hv, d, d, dt)
+    assert size(0) == 0 and size(3, hv=0) == 0
+    for n in (1, 7, 300):
+        assert size(n) > 0 and size(n) % 256 == 0
+    assert size(1) <= size(7) <= size(300)
+    assert size(300, hv=8) >= size(300, hv=4)
+
+    def call(ws, ws_bytes):
+        return lib.gdn_chunk_fwd(FAKE, FAKE, FAKE, 512, 512, 512, 1, FAKE, FAKE, None, FAKE, 3, 256, 4, 4,
+                                 128, 128, 0.1, 0, FAKE, FAKE, ws, ws_bytes, None)
+    need = size(3)
+    assert call(FAKE, need - 1) == 9
+    assert "workspace" in lib.gdn_last_error().decode()
+    assert call(ctypes.c_void_p(4100), need) == 9  # not 16-byte aligned
+
+
 def test_conv_host_errors(lib):
     def call(**kw):
         a = dict(C=64, K=4, halo=None, hl=0, T=8)
