@@ -22,8 +22,9 @@
  *
  * Conventions shared by every entry point
  *   - Pointers marked "device" must be CUDA device (or managed) memory; the
- *     caller allocates and owns every buffer.  Except for the workspace of
- *     gdn_shard_fwd, no entry point needs scratch memory, and none allocates.
+ *     caller allocates and owns every buffer.  Except for the workspaces of
+ *     gdn_shard_fwd (required) and gdn_chunk_fwd (optional), no entry point
+ *     needs scratch memory, and none allocates.
  *   - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL
  *     = the legacy default stream).  No entry point synchronises the host.
  *   - Tokens are packed, batch 1: a token-major [T, ...] layout with
@@ -147,7 +148,9 @@ gdn_status gdn_cp_plan(const int32_t *cu_seqlens, int32_t num_seqs, int32_t n_sh
  *   w     device [channels, conv_k] dtype;  bias device [channels] or NULL
  *   y     device [T, channels] dtype, row stride ldy; must not overlap x
  * Needs channels % 8 == 0, ldx and ldy multiples of 8, and 16-byte aligned
- * x, y and halo.  Accumulates in fp32; bf16 output rounds to nearest even.
+ * x, y and halo.  Accumulates in fp32; bf16 output rounds to nearest even
+ * (its SiLU uses a hardware tanh, error about 5e-4, below bf16 rounding;
+ * fp32 output uses a / (1 + e^-a)).
  * ---------------------------------------------------------------------- */
 gdn_status gdn_conv_silu(const void *x, int64_t ldx, gdn_dtype dtype, int32_t T,
                          int32_t channels, const void *w, const void *bias, int32_t conv_k,
@@ -167,6 +170,9 @@ gdn_status gdn_conv_silu(const void *x, int64_t ldx, gdn_dtype dtype, int32_t T,
  *   h_final device [num_seqs, Hv, dk, dv] fp32 state after each sequence's
  *         last token (h0 or 0 for an empty sequence), or NULL
  *   scale multiplies q (1/sqrt(dk) in the pages)
+ *   workspace, workspace_bytes  optional device scratch of at least
+ *         gdn_chunk_fwd_workspace_size(...) bytes, 16-byte aligned (the work
+ *         queue described there), or NULL, 0
  * Chunks restart at every sequence start; a sequence's last chunk is padded
  * with beta = 0, g = 0 rows that are never stored.  Row strides must be
  * multiples of 8 elements and q/k/v 16-byte aligned.  o may not alias the
