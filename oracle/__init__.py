@@ -60,6 +60,10 @@ def _load():
             lib.orc_gdn_summary.restype = None
             lib.orc_state_combine.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp]
             lib.orc_state_combine.restype = None
+            lib.orc_gates.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp]
+            lib.orc_gates.restype = None
+            lib.orc_gated_rmsnorm.argtypes = [vp, vp, vp, dbl, i64, i64, vp]
+            lib.orc_gated_rmsnorm.restype = None
             lib.orc_max_threads.argtypes = []
             lib.orc_max_threads.restype = i32
             _lib = lib
@@ -167,3 +171,38 @@ def path_forward(x, conv_w, conv_b, g, beta, h0, cu_seqlens, Hk, Hv, K, V, scale
     k = y[:, Hk * K:2 * Hk * K].reshape(T, Hk, K)
     v = y[:, 2 * Hk * K:].reshape(T, Hv, V)
     return gdn_forward(q, k, v, g, beta, h0, cu_seqlens, scale, l2norm=True)
+
+
+def gates(a, b, A_log, dt_bias):
+    """The wrappers' gates from the raw projections: g = -exp(A_log) softplus(a +
+    dt_bias), beta = sigmoid(b).  a, b [T, Hv]; A_log, dt_bias [Hv]."""
+    a, b, A_log, dt_bias = map(_f64, (a, b, A_log, dt_bias))
+    T, Hv = a.shape
+    g = np.empty((T, Hv), dtype=np.float64)
+    beta = np.empty((T, Hv), dtype=np.float64)
+    _load().orc_gates(a.ctypes.data, b.ctypes.data, A_log.ctypes.data, dt_bias.ctypes.data, T, Hv,
+                      g.ctypes.data, beta.ctypes.data)
+    return g, beta
+
+
+def gated_rmsnorm(o, z, w, eps=1e-6):
+    """Gated RMS norm over the last axis: w * o / sqrt(mean(o^2) + eps) * silu(z)."""
+    o, z, w = _f64(o), _f64(z), _f64(w)
+    shape = o.shape
+    D = shape[-1]
+    rows = int(np.prod(shape[:-1]))
+    y = np.empty(shape, dtype=np.float64)
+    _load().orc_gated_rmsnorm(o.ctypes.data, z.ctypes.data, w.ctypes.data, float(eps), rows, D,
+                              y.ctypes.data)
+    return y
+
+
+def layer_forward(x, conv_w, conv_b, a, b, A_log, dt_bias, z, norm_w, h0, cu_seqlens, Hk, Hv, K, V,
+                  scale, eps=1e-6):
+    """The wrappers' forward between the projections and the output
+    projection, unsharded: gates from a and b, the path (conv + SiLU, split,
+    L2 norm, recurrence), then the gated RMS norm with z.  Returns
+    (y [T, Hv, V], h_final [N, Hv, K, V])."""
+    g, beta = gates(a, b, A_log, dt_bias)
+    o, hf = path_forward(x, conv_w, conv_b, g, beta, h0, cu_seqlens, Hk, Hv, K, V, scale)
+    return gated_rmsnorm(o, z, norm_w, eps), hf

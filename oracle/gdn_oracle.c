@@ -277,6 +277,50 @@ void orc_state_combine(const double *M, const double *N, const double *S0,
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* The steps around the path in the wrappers' forward ([HP-CP])              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gates from the raw projections, as the P2P / all-gather wrappers' forward
+ * forms them before the delta rule:
+ *   beta = sigmoid(b)
+ *   g    = -exp(A_log[h]) * softplus(a + dt_bias[h]),  softplus(x) = log(1 + e^x)
+ * a, b [T, Hv]; A_log, dt_bias [Hv]; g, beta [T, Hv].
+ */
+void orc_gates(const double *a, const double *b, const double *A_log, const double *dt_bias,
+               int64_t T, int64_t Hv, double *g, double *beta) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < Hv; ++h) {
+            const int64_t i = t * Hv + h;
+            const double x = a[i] + dt_bias[h];
+            const double sp = x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+            g[i] = -exp(A_log[h]) * sp;
+            beta[i] = 1.0 / (1.0 + exp(-b[i]));
+        }
+}
+
+/*
+ * The gated RMS norm the wrappers apply to the attention output before the
+ * output projection (base.norm(core_attn_out, z) on rows of head_v_dim):
+ * for every row r of D values,
+ *   y[r] = w * o[r] / sqrt(mean(o[r]^2) + eps) * silu(z[r]),  silu(x) = x / (1 + e^-x)
+ * o, z, y [rows, D]; w [D].
+ */
+void orc_gated_rmsnorm(const double *o, const double *z, const double *w, double eps,
+                       int64_t rows, int64_t D, double *y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t d = 0; d < D; ++d) ss += o[r * D + d] * o[r * D + d];
+        const double inv = 1.0 / sqrt(ss / (double)D + eps);
+        for (int64_t d = 0; d < D; ++d) {
+            const double zz = z[r * D + d];
+            y[r * D + d] = w[d] * (o[r * D + d] * inv) * (zz / (1.0 + exp(-zz)));
+        }
+    }
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

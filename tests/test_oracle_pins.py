@@ -356,3 +356,64 @@ def test_path_forward_composition():
                                       g[s0:s1, h], beta[s0:s1, h], None, scale=0.3)
             np.testing.assert_allclose(o[s0:s1, h], o2, atol=1e-11)
             np.testing.assert_allclose(hf[n, h], S2, atol=1e-11)
+
+
+# ----------------------------------------------------------------------------
+# gates from the raw projections and the gated RMS norm (the wrappers'
+# forward around the path)
+# ----------------------------------------------------------------------------
+
+def test_gates_closed_forms():
+    """a = -dt_bias gives softplus(0) = ln 2, so g = -exp(A_log) ln 2; b = 0
+    gives beta = 1/2; A_log = log 3 scales the decay rate by exactly 3."""
+    T, Hv = 5, 4
+    dt = rng.standard_normal(Hv)
+    A_log = rng.standard_normal(Hv)
+    g, beta = oracle.gates(-np.tile(dt, (T, 1)), np.zeros((T, Hv)), A_log, dt)
+    np.testing.assert_allclose(g, -np.exp(A_log)[None, :] * np.log(2.0) * np.ones((T, 1)), rtol=1e-15)
+    np.testing.assert_allclose(beta, 0.5, rtol=0)
+    a = rng.standard_normal((T, Hv))
+    g1, _ = oracle.gates(a, a, np.zeros(Hv), dt)
+    g3, _ = oracle.gates(a, a, np.full(Hv, np.log(3.0)), dt)
+    np.testing.assert_allclose(g3, 3.0 * g1, rtol=1e-14)
+    assert (g1 < 0).all()
+
+
+def test_gates_vs_torch():
+    """Against torch's softplus (threshold 20: identical up to e^-20 beyond
+    it) and sigmoid, over a wide range of inputs."""
+    T, Hv = 200, 6
+    a = rng.standard_normal((T, Hv)) * 8.0
+    b = rng.standard_normal((T, Hv)) * 8.0
+    A_log = rng.standard_normal(Hv)
+    dt = rng.standard_normal(Hv)
+    g, beta = oracle.gates(a, b, A_log, dt)
+    ta = torch.tensor(a, dtype=torch.float64)
+    exp_g = -torch.tensor(A_log).exp() * torch.nn.functional.softplus(ta + torch.tensor(dt))
+    np.testing.assert_allclose(g, exp_g.numpy(), rtol=1e-12, atol=1e-8)
+    np.testing.assert_allclose(beta, torch.sigmoid(torch.tensor(b)).numpy(), rtol=1e-13, atol=0)
+
+
+def test_gated_rmsnorm_vs_torch():
+    """Against torch.nn.functional.rms_norm over head_v_dim times silu(z)."""
+    o = rng.standard_normal((7, 3, 128))
+    z = rng.standard_normal((7, 3, 128)) * 3.0
+    w = 1.0 + 0.1 * rng.standard_normal(128)
+    for eps in (1e-6, 0.5):
+        y = oracle.gated_rmsnorm(o, z, w, eps)
+        exp = torch.nn.functional.rms_norm(torch.tensor(o), (128,), torch.tensor(w), eps) \
+            * torch.nn.functional.silu(torch.tensor(z))
+        np.testing.assert_allclose(y, exp.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_gated_rmsnorm_closed_forms():
+    """z = 0 closes the gate (y = 0); with eps = 0 the result does not depend
+    on the scale of o; a constant row c with unit weight gives silu(z)."""
+    o = rng.standard_normal((4, 64))
+    z = rng.standard_normal((4, 64))
+    w = rng.standard_normal(64)
+    assert np.all(oracle.gated_rmsnorm(o, np.zeros_like(z), w) == 0.0)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(37.0 * o, z, w, 0.0), oracle.gated_rmsnorm(o, z, w, 0.0),
+                               rtol=1e-13)
+    y = oracle.gated_rmsnorm(np.full((2, 64), 2.5), z[:2], np.ones(64), 0.0)
+    np.testing.assert_allclose(y, z[:2] / (1.0 + np.exp(-z[:2])), rtol=1e-14)
