@@ -4,6 +4,13 @@ One step = one gdn_shard_fwd call (plan, conv + SiLU with halo, chunked gated
 delta rule, and for P > 1 the prefix merge and second pass) over one batch of
 seeded synthetic input resident in HBM.  Prints ONE JSON line (rank 0).
 
+The default workload is the largest bf16 d = 128 configuration, the
+million-token sequence (T = 1048576, 32 heads, 64 virtual shards, h0 != 0);
+--config picks another (packed_varlen, long, ragged, tiny).  The line's
+"kernels" entry gives each phase of the step (plan + conv, chunk pass 1,
+merge, chunk pass 2, final states), timed with CUDA events recorded between
+the step's own launches; "roofline" rates the two chunk passes together.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                   [--impl ours|reference] [--no-cpu-baseline]
 
@@ -45,9 +52,11 @@ def workload(name):
     return W.CONFIGS[name]()
 
 
-def algorithmic(w):
-    """Algorithmic bytes and FLOPs of the chunk step (real tokens, C = 64);
-    the UT triangular solve is ALU work and not credited."""
+def algorithmic(w, spanning_tokens=0, n_affine=0):
+    """Algorithmic bytes and FLOPs of the chunk passes (real tokens, C = 64);
+    the UT triangular solve is ALU work and not credited.  On P > 1 shards
+    the M chain adds 4 K^2 Hv FLOPs per token of a spanning shard and the
+    merge 2 K^2 V Hv per affine shard carry."""
     e = 2 if w.dtype == "bf16" else 4
     T, Hk, Hv, K, V, C = w.T, w.Hk, w.Hv, w.dk, w.dv, 64
     chunk_bytes = T * (2 * Hk * K * e + Hv * V * e      # q, k, v in
@@ -57,8 +66,20 @@ def algorithmic(w):
     if w.h0_std:
         chunk_bytes += w.N * Hv * K * V * 4
     flops = T * (4 * C * K * Hk + (2 * C * K + 4 * C * V + 6 * K * V) * Hv)
+    flops += spanning_tokens * 4 * K * K * Hv + n_affine * 2 * K * K * V * Hv
     conv_bytes = 2 * T * w.Cch * e
     return chunk_bytes, flops, conv_bytes
+
+
+def shard_extras(recs):
+    """Tokens of spanning shards and affine carries, from the device plan."""
+    part_tokens, span, aff = 0, 0, 0
+    for r in recs:
+        part_tokens = r["local_cu"][-1]
+        if r["local_num_seqs"] == 1 and not r["is_first_rank"] and r["post_num_ranks"] > 0:
+            span += part_tokens
+            aff += 1
+    return span, aff
 
 
 class ClockSampler:
@@ -245,11 +266,12 @@ def run_ours(args, rank, world, local_rank):
     # plan, conv, pass 1, empty-seq final (+ merge, pass 2); the tensor-core
     # chunk path (bf16, d = 128) sorts pass 1's work queue first (order kernel)
     tc_path = w.dtype == "bf16" and w.dk == 128 and w.dv == 128
-    launches_per_step = 4 + (1 if tc_path else 0) + (2 if P > 1 else 0)
+    launches_per_step = 4 + (1 if tc_path else 0) + (2 if P > 1 else 0)  # plan, conv, [order], pass 1, final
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    g.binding.device_timeouts(reset=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -336,34 +358,36 @@ def run_ours(args, rank, world, local_rank):
     h2d = xh.numel() * xh.element_size() + gh.numel() * 4 + bh.numel() * bh.element_size() + cuh.numel() * 4
     d2h = oh.numel() * oh.element_size() + hfh.numel() * 4
 
-    # ---- dominant kernel: the chunk kernel alone (same kernel, same work) ----
-    Cch = w.Cch
-    y = torch.empty((w.T, Cch), dtype=tdt, device=dev)
-    g.gdn_conv_silu(x, cw, None, cu, out=y)
-    q = y[:, :w.Hk * w.dk].view(w.T, w.Hk, w.dk)
-    k = y[:, w.Hk * w.dk:2 * w.Hk * w.dk].view(w.T, w.Hk, w.dk)
-    v = y[:, 2 * w.Hk * w.dk:].view(w.T, w.Hv, w.dv)
-    hf_k = torch.empty((w.N, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
-    o_k = torch.empty_like(o)
+    # ---- per-phase times of the same step (events between its kernels) ----
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    g.binding.debug_set_phase_events(evs)
+    phases = []
+    try:
+        for _ in range(max(5, min(args.steps, 30))):
+            step()
+            evs[-1].synchronize()
+            phases.append([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
+    finally:
+        g.binding.debug_set_phase_events(None)
+    ph = np.median(np.array(phases), axis=0)
+    conv_ms, pass1_ms, combine_ms, pass2_ms, final_ms = (float(x) for x in ph)
+    chunk_ms = pass1_ms + pass2_ms
+    timeouts = g.binding.device_timeouts(reset=True)
+    if timeouts:
+        raise RuntimeError(f"{timeouts} bounded device waits expired during the bench: outputs incomplete")
 
-    def chunk_only():
-        g.gdn_chunk_fwd(q, k, v, gg, bb, cu, h0=h0, l2norm=True, out=o_k)
-
-    def conv_only():
-        g.gdn_conv_silu(x, cw, None, cu, out=y)
-
-    for _ in range(3):
-        chunk_only()
-        conv_only()
-    n_k = max(5, min(args.steps, 50))
-    chunk_ms = time_loop(chunk_only, n_k, stream)
-    conv_ms = time_loop(conv_only, n_k, stream)
-    del hf_k
+    _, _, plan = g.gdn_shard_fwd(x, cw, None, gg, bb, cu, w.Hk, w.Hv, w.dk, w.dv, P, h0=h0, workspace=ws,
+                                 out=o, h_final=hf_d, want_plan=True)
+    _, recs = g.decode_plan(plan, w.N, P)
+    span_tokens, n_affine = shard_extras(recs)
 
     peaks, peak_src = load_peaks()
-    chunk_bytes, flops, conv_bytes = algorithmic(w)
+    chunk_bytes, flops, conv_bytes = algorithmic(w, span_tokens, n_affine)
     hbm = float(peaks["hbm_gbs"])
-    tfl = float(peaks["bf16_tflops"])
+    tfl = float(peaks["bf16_tflops_sustained" if chunk_ms > 50 else "bf16_tflops"])
     t_bytes = chunk_bytes / (hbm * 1e9)
     t_flops = flops / (tfl * 1e12)
     traffic = None
@@ -372,7 +396,7 @@ def run_ours(args, rank, world, local_rank):
         rec = json.load(open(tp))
         # counters are only valid for the kernel sources they were taken on
         if rec.get("kernel_sources_sha256") == kernel_sources_sha256():
-            traffic = rec.get("bytes_per_launch")
+            traffic = rec.get("bytes_per_step")
     if t_bytes >= t_flops:
         ach = chunk_bytes / (chunk_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
@@ -383,10 +407,12 @@ def run_ours(args, rank, world, local_rank):
                 "frac": ach / tfl, "traffic": traffic}
     roof.update({"kernel": ("chunk_tc_kernel" if (w.dtype == "bf16" and w.dk == 128 and w.dv == 128)
                             else "chunk_bf16_kernel" if w.dtype == "bf16" else "chunk_f32_kernel"),
-                 "kernel_ms": chunk_ms, "peak_source": peak_src + " (burst)",
+                 "kernel_ms": chunk_ms, "launches_per_step": 2 if P > 1 else 1,
+                 "peak_source": peak_src + (" (sustained)" if chunk_ms > 50 else " (burst)"),
                  "algorithmic_bytes": chunk_bytes, "algorithmic_flops": flops,
                  "tensor_frac": (flops / (chunk_ms * 1e-3) / 1e12) / tfl,
-                 "roofline_ms": max(t_bytes, t_flops) * 1e3})
+                 "roofline_ms": max(t_bytes, t_flops) * 1e3,
+                 "step_frac": max(t_bytes, t_flops) * 1e3 / ms})
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
@@ -397,9 +423,11 @@ def run_ours(args, rank, world, local_rank):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roof,
-            "kernels": {"chunk_ms": chunk_ms, "conv_ms": conv_ms,
+            "kernels": {"plan_conv_ms": conv_ms, "pass1_ms": pass1_ms, "combine_ms": combine_ms,
+                        "pass2_ms": pass2_ms, "final_ms": final_ms, "chunk_ms": chunk_ms,
                         "conv_GBps": conv_bytes / (conv_ms * 1e-3) / 1e9,
                         "conv_frac_hbm": conv_bytes / (conv_ms * 1e-3) / 1e9 / hbm},
+            "device_timeouts": timeouts,
             "clocks": clk.summary()}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(workload(args.config))
@@ -412,7 +440,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="packed_varlen")
+    ap.add_argument("--config", default="million")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -87,6 +87,24 @@ const char *gdn_last_error(void);
    device (a copy from device memory).  reset != 0 zeroes the counter. */
 gdn_status gdn_device_timeouts(int32_t *count, int reset);
 
+/* Testing hook (no counterpart on the source pages): settings of the
+   split-item hand-over of the tensor-core chunk kernel, used by the launches
+   that follow on any thread.  wait_ns bounds the wait of a second half for
+   its first half's final state (default 1e9 ns); publish == 0 makes first
+   halves skip publishing it, so that every second half's wait expires:
+   the kernel then stops early, counts a timeout (gdn_device_timeouts) and
+   writes GDN_ERR_TIMEOUT to the launch's status word (the plan's word for
+   gdn_shard_fwd, word 2 of the gdn_chunk_fwd workspace).  Restore with
+   gdn_debug_set_handover(1000000000, 1).  Not for production use. */
+gdn_status gdn_debug_set_handover(int64_t wait_ns, int publish);
+
+/* Profiling hook (no counterpart on the source pages): while n > 0, every
+   gdn_shard_fwd call on this host thread records events[i] (cudaEvent_t
+   handles, created by the caller) on its stream: [0] at entry, [1] after the
+   plan and the conv, [2] after chunk pass 1, [3] after the merge, [4] after
+   pass 2, [5] at exit (as far as n reaches).  n = 0 turns it off. */
+gdn_status gdn_debug_set_phase_events(void *const *events, int32_t n);
+
 /* ------------------------------------------------------------------------
  * Shard plan  ([FLA-CP] get_cp_cu_seqlens, steps 1-5)
  *
@@ -256,6 +274,36 @@ gdn_status gdn_shard_fwd(const void *x, const void *conv_w, const void *conv_b, 
                          void *stream);
 
 /* ------------------------------------------------------------------------
+ * The layer between its projections ([HP-CP] LinearAttentionP2PCPWrapper /
+ * LinearAttentionAllGatherCPWrapper forward, from the projection outputs to
+ * the input of the output projection):
+ *   beta = sigmoid(b),  g = -exp(A_log) * softplus(a + dt_bias)   (per v-head)
+ *   o    = the path of gdn_shard_fwd on n_shards virtual shards
+ *   y    = norm_w * o / sqrt(mean(o^2) + norm_eps) * silu(z)   per (token,
+ *          v-head) row of dv values (the wrappers' norm(core_attn_out, z))
+ *   x, conv_w, conv_b, h0, cu_seqlens, workspace, h_final, plan_out: as in
+ *           gdn_shard_fwd (same workspace size)
+ *   a, b    device [T, Hv] dtype (the raw gate projections)
+ *   A_log, dt_bias  device [Hv] fp32
+ *   z       device [T, Hv, dv] dtype with token row stride ldz (a multiple of
+ *           8, >= Hv*dv), 16-byte aligned; or NULL: no norm (y = o)
+ *   norm_w  device [dv] dtype, 16-byte aligned (with z)
+ *   y       device [T, Hv, dv] dtype
+ * The gates are computed where g and beta are read (inside the chunk
+ * kernels): g in fp32 (softplus(x) = x for x > 20), beta rounded to dtype.
+ * The norm is the tensor-core chunk kernel's output epilogue for bf16 with
+ * dk = dv = 128 (on the bf16-rounded o); other shapes run it as one more
+ * pass over y.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const void *conv_b, int32_t conv_k,
+                         const void *a, const void *b, const float *A_log, const float *dt_bias,
+                         const void *z, int64_t ldz, const void *norm_w, float norm_eps,
+                         const float *h0, const int32_t *cu_seqlens, int32_t num_seqs, int32_t T,
+                         int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         int32_t n_shards, gdn_dtype dtype, void *workspace, size_t workspace_bytes,
+                         void *y, float *h_final, int32_t *plan_out, void *stream);
+
+/* ------------------------------------------------------------------------
  * gdn_shard_fwd without a caller workspace.  The source pages have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory -- a plugin whose host application owns all device buffers
@@ -269,8 +317,10 @@ gdn_status gdn_shard_fwd(const void *x, const void *conv_w, const void *conv_b, 
  * rejected with GDN_ERR_WORKSPACE before anything is enqueued.  The entry
  * point never calls cudaMalloc/cudaFree or any allocating routine.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, once per device, with that device current); make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with
+ *     the device's current CUDA context; a call under a new context (after
+ *     cudaDeviceReset) looks it up again.  Make the first call on a device,
+ *     and the first after a reset, before any stream capture.
  *   - All calls share the one array and it keeps the previous call's
  *     contents; nothing in it needs to start at zero.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads) race on it:

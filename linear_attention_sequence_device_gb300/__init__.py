@@ -4,5 +4,5 @@ The computation lives in the CUDA library ``libgdncp.so`` (C ABI declared in
 ``include/gdn_cp.h``); ``binding`` is its thin Python front end.
 """
 from .binding import (GdnError, decode_plan, gdn_chunk_fwd, gdn_chunk_summary,  # noqa: F401
-                      gdn_conv_silu, gdn_cp_plan, gdn_shard_fwd, gdn_state_combine, load,
+                      gdn_conv_silu, gdn_cp_plan, gdn_layer_fwd, gdn_shard_fwd, gdn_state_combine, load,
                       plan_words, shard_fwd_workspace_size)

@@ -33,6 +33,8 @@ SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_error": (ctypes.c_char_p, []),
     "gdn_device_timeouts": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "gdn_debug_set_handover": (ctypes.c_int, [_i64, ctypes.c_int]),
+    "gdn_debug_set_phase_events": (ctypes.c_int, [_vp, _i32]),
     "gdn_cp_plan_words": (_i64, [_i32, _i32]),
     "gdn_cp_plan": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp]),
     "gdn_conv_silu": (ctypes.c_int, [_vp, _i64, ctypes.c_int, _i32, _i32, _vp, _vp, _i32, _vp,
@@ -49,6 +51,9 @@ SIGNATURES = {
                                            ctypes.c_int]),
     "gdn_shard_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      _i32, _i32, _i32, _f32, _u32, _i32, ctypes.c_int, _vp, _sz,
+                                     _vp, _vp, _vp, _vp]),
+    "gdn_layer_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _f32, _vp, _vp,
+                                     _i32, _i32, _i32, _i32, _i32, _i32, _f32, _u32, _i32, ctypes.c_int, _vp, _sz,
                                      _vp, _vp, _vp, _vp]),
     "gdn_shard_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                              _i32, _i32, _i32, _i32, _f32, _u32, _i32,
@@ -129,6 +134,22 @@ def device_timeouts(reset: bool = False) -> int:
     n = ctypes.c_int32(0)
     _check(load().gdn_device_timeouts(ctypes.byref(n), 1 if reset else 0))
     return n.value
+
+
+def debug_set_handover(wait_ns: int = 1_000_000_000, publish: bool = True):
+    """Testing hook: bound of the split-item hand-over wait and whether first
+    halves publish their final state (see gdn_cp.h); the defaults restore
+    normal operation."""
+    _check(load().gdn_debug_set_handover(int(wait_ns), 1 if publish else 0))
+
+
+def debug_set_phase_events(events=None):
+    """Profiling hook: torch.cuda.Event objects (already recorded once, so
+    that their handles exist) that gdn_shard_fwd records between its phases
+    on this thread; None turns it off."""
+    events = list(events or [])
+    arr = (ctypes.c_void_p * max(1, len(events)))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load().gdn_debug_set_phase_events(arr, len(events)))
 
 
 def plan_words(num_seqs: int, n_shards: int) -> int:
@@ -285,6 +306,47 @@ def gdn_shard_fwd(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shar
                                 n_shards, _dt(x), _p(workspace), workspace.numel(), _p(o), _p(hf),
                                 _p(plan), _stream()))
     return o, hf, plan
+
+
+def gdn_layer_fwd(x, conv_w, conv_b, a, b, A_log, dt_bias, z, norm_w, cu_seqlens, Hk, Hv, dk, dv,
+                  n_shards, h0=None, scale=None, eps=1e-6, l2norm=True, workspace=None, out=None,
+                  h_final=True, want_plan=False):
+    """The layer between its projections: gates from a and b, the path on
+    n_shards virtual shards, the gated RMS norm with z (None: no norm).
+    x [T, Cch]; a, b [T, Hv]; A_log, dt_bias [Hv] fp32; z [T, Hv, dv] (dense
+    heads, token stride free); norm_w [dv].  Returns (y, h_final, plan)."""
+    dt = x.dtype
+    for t, n in ((x, "x"), (conv_w, "conv_w"), (conv_b, "conv_b"), (a, "a"), (b, "b"), (z, "z"),
+                 (norm_w, "norm_w")):
+        _need(t, n, dt)
+    _need(A_log, "A_log", torch.float32)
+    _need(dt_bias, "dt_bias", torch.float32)
+    _need(h0, "h0", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T = x.shape[0]
+    N = cu_seqlens.numel() - 1
+    scale = dk ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(shard_fwd_workspace_size(T, N, n_shards, Hk, Hv, dk, dv, dt), dtype=torch.uint8,
+                                device=x.device)
+    y = torch.empty((T, Hv, dv), dtype=dt, device=x.device) if out is None else out
+    if isinstance(h_final, torch.Tensor):
+        hf = h_final
+    else:
+        hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=x.device) if h_final else None
+    plan = torch.empty(plan_words(N, n_shards), dtype=torch.int32, device=x.device) if want_plan else None
+    ldz = 0
+    if z is not None:
+        z3 = z.view(T, Hv, dv) if z.dim() == 2 else z
+        ldz = _row_stride(z3, "z")
+    _check(load().gdn_layer_fwd(_p(x.contiguous()), _p(conv_w.contiguous()), _p(conv_b), conv_w.shape[1],
+                                _p(a.contiguous()), _p(b.contiguous()), _p(A_log.contiguous()),
+                                _p(dt_bias.contiguous()), _p(z), ldz,
+                                _p(None if norm_w is None else norm_w.contiguous()), float(eps),
+                                _p(None if h0 is None else h0.contiguous()), _p(cu_seqlens), N, T, Hk, Hv, dk,
+                                dv, float(scale), GDN_QK_L2NORM if l2norm else 0, n_shards, _dt(x),
+                                _p(workspace), workspace.numel(), _p(y), _p(hf), _p(plan), _stream()))
+    return y, hf, plan
 
 
 def gdn_shard_fwd_noalloc(x, conv_w, conv_b, g, beta, cu_seqlens, Hk, Hv, dk, dv, n_shards,

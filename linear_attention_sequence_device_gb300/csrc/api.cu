@@ -10,6 +10,10 @@ namespace gdn {
 
 static thread_local char g_err[512] = "";
 
+// Profiling hook: events recorded between the phases of gdn_shard_fwd.
+static thread_local cudaEvent_t g_phase_events[8];
+static thread_local int g_phase_n = 0;
+
 gdn_status fail(gdn_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -108,6 +112,13 @@ const char* gdn_status_string(gdn_status s) {
 }
 
 const char* gdn_last_error(void) { return g_err; }
+
+gdn_status gdn_debug_set_phase_events(void* const* events, int32_t n) {
+    if (n < 0 || n > 8 || (n > 0 && !events)) return fail(GDN_ERR_INVALID_ARG, "n=%d events=%p", n, (const void*)events);
+    for (int i = 0; i < n; ++i) g_phase_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_phase_n = n;
+    return GDN_OK;
+}
 
 gdn_status gdn_device_timeouts(int32_t* count, int reset) {
     if (!count) return fail(GDN_ERR_INVALID_ARG, "count is NULL");
@@ -249,12 +260,29 @@ size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shard
            pass1_sched_bytes(num_seqs, n_shards, Hv, dk, dv, dtype);
 }
 
-gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k,
-                         const float* g, const void* beta, const float* h0,
-                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
-                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
-                         int32_t n_shards, gdn_dtype dtype, void* workspace, size_t workspace_bytes,
-                         void* o, float* h_final, int32_t* plan_out, void* stream) {
+}  // extern "C"
+
+namespace gdn {
+
+// The layer's extras around the path: gates from the raw projections and the
+// gated RMS norm of the output (null: gdn_shard_fwd's g / beta, plain o).
+struct LayerExtras {
+    const void* a;
+    const float* A_log;
+    const float* dt_bias;
+    const void* z;  // or null: no norm
+    int64_t ldz;
+    const void* norm_w;
+    float norm_eps;
+};
+
+static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k,
+                                 const float* g, const void* beta, const float* h0,
+                                 const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                                 int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                                 int32_t n_shards, gdn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                 void* o, float* h_final, int32_t* plan_out, void* stream,
+                                 const LayerExtras* ex) {
     gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
     if (st != GDN_OK) return st;
     if (n_shards < 1 || n_shards > 65536)
@@ -265,8 +293,20 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     if (conv_k < 1 || conv_k > 4) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "conv_k=%d not in 1..4", conv_k);
     if (n_shards > 1 && T / n_shards < conv_k - 1)
         return fail(GDN_ERR_SHARD_TOO_SHORT, "shard length %d < conv halo %d", T / n_shards, conv_k - 1);
-    if (!x || !conv_w || !g || !beta || !cu_seqlens || !o)
+    if (!x || !conv_w || (!g && !ex) || !beta || !cu_seqlens || !o)
         return fail(GDN_ERR_INVALID_ARG, "x/conv_w/g/beta/cu_seqlens/o is NULL");
+    if (ex) {
+        if (!ex->a || !ex->A_log || !ex->dt_bias)
+            return fail(GDN_ERR_INVALID_ARG, "a/A_log/dt_bias is NULL");
+        if (ex->z) {
+            if (!ex->norm_w || !al16(ex->z) || !al16(ex->norm_w))
+                return fail(GDN_ERR_INVALID_ARG, "z and norm_w must be non-NULL and 16-byte aligned");
+            if (ex->ldz < (int64_t)Hv * dv || ex->ldz % 8 != 0)
+                return fail(GDN_ERR_INVALID_ARG, "row stride of z (%lld) must be >= Hv*dv and a multiple of 8",
+                            (long long)ex->ldz);
+            if (!(ex->norm_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARG, "norm_eps must be >= 0");
+        }
+    }
     if (!al16(x) || !al16(o)) return fail(GDN_ERR_INVALID_ARG, "x and o must be 16-byte aligned");
     if (h_final && (reinterpret_cast<uintptr_t>(h_final) & 7u))
         return fail(GDN_ERR_INVALID_ARG, "h_final must be 8-byte aligned");
@@ -293,12 +333,17 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     ws += align256(carry * dk * sizeof(float));
     int32_t* sched = reinterpret_cast<int32_t*>(ws);
 
+    auto mark = [&](int i) {
+        if (i < g_phase_n) cudaEventRecord(g_phase_events[i], s);
+    };
+    mark(0);
     // 1. plan
     if ((st = launch_plan(cu_seqlens, num_seqs, P, plan, s)) != GDN_OK) return st;
     // 2. conv + SiLU, each shard reading its halo from the previous shard's rows
     if ((st = launch_conv(x, cch, dtype, T, (int)cch, conv_w, conv_b, conv_k, cu_seqlens, num_seqs,
                           nullptr, 0, y, cch, plan, P, s)) != GDN_OK)
         return st;
+    mark(1);
     // 3. pass 1: every segment with a known initial state, plus [N | M] summaries
     ChunkParams p{};
     const size_t es = esize(dtype);
@@ -310,6 +355,12 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
     p.sumN = carryN; p.sumM = carryM; p.S_in = S_in; p.plan = plan; p.n_shards = P;
+    p.status = plan;  // an expired device wait is reported in the plan's status word
+    const bool tc_norm = ex && ex->z && chunk_tc_eligible(dtype, dk, dv);
+    if (ex) {
+        p.a_raw = ex->a; p.A_log = ex->A_log; p.dt_bias = ex->dt_bias;
+        if (tc_norm) { p.z = ex->z; p.ldz = ex->ldz; p.norm_w = ex->norm_w; p.norm_eps = ex->norm_eps; }
+    }
     p.col_tile = chunk_col_tile(dtype, dk, dv);
     {
         if (chunk_tc_eligible(dtype, dk, dv)) p.sched = sched;  // filled by the order kernel
@@ -317,14 +368,23 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
         p.sched = nullptr;
     }
+    mark(2);
     if (P > 1) {
         // 4. prefix merge of the shard carries
         if ((st = launch_combine(carryM, carryN, nullptr, P, Hv, dk, dv, S_in, plan, s)) != GDN_OK)
             return st;
+        mark(3);
         // 5. pass 2: the first segment of every shard that continues a sequence
         dim3 grid(P, Hv, dv / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS2, grid, s)) != GDN_OK) return st;
+    } else {
+        mark(3);
     }
+    if (ex && ex->z && !tc_norm) {  // kernels without the norm epilogue: a separate pass over o
+        if ((st = launch_gated_norm(o, ex->z, ex->ldz, ex->norm_w, ex->norm_eps, T, Hv, dv, dtype, s)) != GDN_OK)
+            return st;
+    }
+    mark(4);
     if (h_final) {
         if ((st = launch_empty_seq_final(cu_seqlens, num_seqs, Hv, dk, dv, h0, h_final, plan, s)) != GDN_OK)
             return st;
@@ -334,7 +394,34 @@ gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, 
             cudaSuccess)
             return check_launch("plan copy");
     }
+    mark(5);
     return GDN_OK;
+}
+
+}  // namespace gdn
+
+extern "C" {
+
+gdn_status gdn_shard_fwd(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k,
+                         const float* g, const void* beta, const float* h0,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         int32_t n_shards, gdn_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* o, float* h_final, int32_t* plan_out, void* stream) {
+    return shard_fwd_core(x, conv_w, conv_b, conv_k, g, beta, h0, cu_seqlens, num_seqs, T, Hk, Hv, dk, dv, scale,
+                          flags, n_shards, dtype, workspace, workspace_bytes, o, h_final, plan_out, stream, nullptr);
+}
+
+gdn_status gdn_layer_fwd(const void* x, const void* conv_w, const void* conv_b, int32_t conv_k, const void* a,
+                         const void* b, const float* A_log, const float* dt_bias, const void* z, int64_t ldz,
+                         const void* norm_w, float norm_eps, const float* h0, const int32_t* cu_seqlens,
+                         int32_t num_seqs, int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale,
+                         uint32_t flags, int32_t n_shards, gdn_dtype dtype, void* workspace,
+                         size_t workspace_bytes, void* y, float* h_final, int32_t* plan_out, void* stream) {
+    const LayerExtras ex{a, A_log, dt_bias, z, ldz, norm_w, norm_eps};
+    return shard_fwd_core(x, conv_w, conv_b, conv_k, nullptr, b, h0, cu_seqlens, num_seqs, T, Hk, Hv, dk, dv,
+                          scale, flags, n_shards, dtype, workspace, workspace_bytes, y, h_final, plan_out, stream,
+                          &ex);
 }
 
 }  // extern "C"

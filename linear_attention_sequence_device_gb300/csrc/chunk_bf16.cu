@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_bf16_kernel(const ChunkParams p, 
     const bf16* __restrict__ q = static_cast<const bf16*>(p.q);
     const bf16* __restrict__ k = static_cast<const bf16*>(p.k);
     const bf16* __restrict__ v = static_cast<const bf16*>(p.v);
-    const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
     bf16* __restrict__ o = static_cast<bf16*>(p.o);
     const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
 
@@ -169,8 +168,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_bf16_kernel(const ChunkParams p, 
         cp_async_commit();
         if (tid < 64) {
             const int64_t t = tb + tid;
-            sm.g[tid] = tid < valid ? __ldg(p.g + t * p.Hv + hv) : 0.f;
-            sm.beta[tid] = tid < valid ? __bfloat162float(beta[t * p.Hv + hv]) : 0.f;
+            float gv = 0.f, bv = 0.f;
+            if (tid < valid) gate_beta<bf16>(p, t, hv, gv, bv);
+            sm.g[tid] = gv;
+            sm.beta[tid] = bv;
         }
         cp_async_wait_all();
         __syncthreads();

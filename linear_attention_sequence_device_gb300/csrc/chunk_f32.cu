@@ -37,7 +37,6 @@ __global__ void __launch_bounds__(NT) chunk_f32_kernel(const ChunkParams p, cons
     const float* __restrict__ q = static_cast<const float*>(p.q);
     const float* __restrict__ k = static_cast<const float*>(p.k);
     const float* __restrict__ v = static_cast<const float*>(p.v);
-    const float* __restrict__ beta = static_cast<const float*>(p.beta);
     float* __restrict__ o = static_cast<float*>(p.o);
     const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
 
@@ -71,8 +70,10 @@ __global__ void __launch_bounds__(NT) chunk_f32_kernel(const ChunkParams p, cons
         }
         if (tid < 64) {
             const int64_t t = tb + tid;
-            sm.g[tid] = tid < valid ? p.g[t * p.Hv + hv] : 0.f;
-            sm.beta[tid] = tid < valid ? beta[t * p.Hv + hv] : 0.f;
+            float gv = 0.f, bv = 0.f;
+            if (tid < valid) gate_beta<float>(p, t, hv, gv, bv);
+            sm.g[tid] = gv;
+            sm.beta[tid] = bv;
         }
         __syncthreads();
         if (l2) {  // q, k <- x * rsqrt(|x|^2 + 1e-6), one warp per row

@@ -3,42 +3,39 @@
 //
 // A CTA runs jobs: a job is a token range of one value head with the full
 // 128-column state, chunk after chunk (C = 64).  Every product has M = 128
-// (a head dimension).  A tensor-core instruction (K = 16) costs a fixed
-// ~50 cycles to issue from one thread and ~65 cycles of pipe time at N = 64
-// against ~150 at N = 256, so products that share their A operand are
-// concatenated along N (fewer instructions for the same work):
-//   [K;Q] K^T or [Q;K] K^T          -> [128 x 64]   the K K^T and Q K^T blocks
-//   W^T = K^T Tbg^T                 -> [128 x 64]   Tbg = T diag(beta e^G / |k|)
-//   U^T = V^T Tb^T                  -> [128 x 64]   Tb  = T diag(beta)
-//   [v_new^T | o^T]  = [U^T | 0] - S^T [W ; -Q~]^T      N = 128, negated A
-//   [o^T | S^T]     += v_new^T [A ; K~^T]^T              N = 192, onto e^{G_last} S^T
-// with Q~ = scale e^G Q / |q|, K~ = diag(e^{G_last - G} / |k|) K and
-// A = scale Q^ K^T o Gamma (lower, diagonal included); the state update
-// S <- e^{G_last} S + K~^T v_new is the last 128 columns of the second product.
-// The row order of the concatenated operands alternates with the chunk's slot
-// so that both slots' outputs sit next to the one state region in tensor memory:
-//   columns  0-63 [Q;K]K^T | 64-127 W^T | 128-191 v_new (slot 0) | 192-255 o (slot 0)
-//          | 256-383 S^T | 384-447 o (slot 1) | 448-511 v_new (slot 1)
-//   slot 0: Q/K tile rows [K -> W ; Q -> -Q~], second operand rows [A ; K~^T]
-//   slot 1: Q/K tile rows [Q -> -Q~ ; K -> W], second operand rows [K~^T ; A]
-// Operands sit in shared memory in the 128-byte-swizzled canonical layout.
+// (a head dimension); the state is kept transposed, S^T [value][key], in
+// tensor memory (thread = value row).  Per chunk, with the chunk's in-chunk
+// gate prefix G, Q~ = diag(scale e^G / |q|) Q, K~ = diag(e^{G_last - G} / |k|) K,
+// Tbg = T diag(beta e^G / |k|), Tb = T diag(beta), T = (I + L)^-1 and
+// A = scale Q^ K^T o Gamma (lower, diagonal included):
+//   [Q;K] K^T                   -> the Q K^T and K K^T blocks (A and L)
+//   W^T = K^T Tbg^T,  U^T = V^T Tb^T
+//   v_new^T = U^T - S^T W^T      the state-dependent chain, part 1
+//   o^T     = S^T Q~^T           (off the chain)
+//   S^T    <- e^{G_last} S^T + v_new^T K~    the chain, part 2
+//   o^T    += v_new^T A^T        (off the chain)
+// Only the two chain products and the tensor-memory <-> shared-memory moves
+// of v_new and S are serial from chunk to chunk; everything else works a
+// chunk ahead.  Operands sit in shared memory in the 128-byte-swizzled
+// canonical layouts: Q/K tiles and A K-major, K~ and W^T MN-major (K~ is a
+// row-scaled copy of the K rows; W^T is read out of tensor memory one key row
+// per thread), so no operand is ever transposed element by element.
 //
 // Two roles of two warpgroups each work on different chunks at once:
-//   producer (warps 0-7), chunk c+1: the L2 norms (sums of squares of the
-//     loaded Q/K rows) and the gate prefix folded into per-row factors, A and L
-//     read from the [Q;K] K^T columns, the UT inverse on warps 0-3 (tf32
-//     mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg), then
-//     thread 0 issues W and U (it issues V as soon as the previous chunk's U
-//     has read it);
+//   producer (warps 0-7), chunk c+1 ahead of the consumer: A and L read from
+//     the [Q;K] K^T columns (warps 1-7); then the UT inverse on warps 0-3
+//     (tf32 mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg)
+//     while warps 4-7 scale Q to Q~ in place, copy K~, and take the next
+//     chunk's L2 norms, gate prefix and per-row factors; then thread 0 issues
+//     W and U (and issues V as soon as the previous chunk's U has read it);
 //   consumer (warps 8-15), chunk c: issues [Q;K] K^T of chunk c+1 as soon as
-//     the producer has read chunk c's columns, builds -Q~ in place and K~^T,
-//     moves W to shared memory, runs the two products above and writes the
-//     output.  The fp32 state stays in the state columns of tensor memory
-//     (scaled by e^{G_last} in place before the second product accumulates
-//     onto it); its bf16 copy in shared memory is the first product's A.
-// Q/K tiles, A/K~ tiles, v_new/o columns and per-chunk values are double
-// buffered ("slots"); the consumer refills a slot with the Q/K of chunk c+2
-// as soon as it is done with chunk c.
+//     the producer has read chunk c's columns, runs the chain, reads W^T of
+//     chunk c+1 out of tensor memory while its state update runs, writes the
+//     previous chunk's output while its first product runs, and refills the
+//     freed Q/K slot with chunk c+2 (TMA, 128-byte swizzle = operand layout).
+// The fp32 state stays in tensor memory: after each update it is read once
+// for its bf16 copy (the next chunk's A operand) and written back scaled by
+// the next chunk's e^{G_last}, onto which the next update accumulates.
 //
 // Work: one job is a token range of one value head.  With a work queue the
 // grid is one persistent CTA per SM; its chunks form one stream over the jobs
@@ -47,8 +44,9 @@
 // initial state, its last stores the final state (a split item's first half
 // hands it to the second half through a release flag).  Without one, every
 // CTA runs the job of its block.  Every wait is bounded: on expiry the
-// kernel counts a timeout, both roles leave their loops, outstanding copies
-// and products are waited for (bounded), and the tensor memory is freed.
+// kernel counts a timeout and writes GDN_ERR_TIMEOUT to the launch's status
+// word, both roles leave their loops, outstanding copies and products are
+// waited for (bounded), and the tensor memory is freed.
 #include <cuda.h>
 #include <string.h>
 
@@ -59,6 +57,22 @@ namespace gdn {
 
 __device__ int g_gdn_timeouts;  // bounded waits that expired (read by gdn_device_timeouts)
 
+#ifdef GDN_PHASE_STAMPS
+// Phase timestamps (clock64) of CTA 0 for chunks [kStamp0, kStamp0 + kStampN)
+// of its stream, 32 slots per chunk; a profiling build only.
+constexpr int kStamp0 = 24, kStampN = 32;
+__device__ long long g_gdn_stamps[kStampN * 32];
+#define GDN_STAMP(gq, idx)                                                           \
+    do {                                                                             \
+        if (blockIdx.x == 0 && (gq) >= kStamp0 && (gq) < kStamp0 + kStampN)          \
+            g_gdn_stamps[((gq) - kStamp0) * 32 + (idx)] = clock64();                 \
+    } while (0)
+#else
+#define GDN_STAMP(gq, idx) \
+    do {                   \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int NT = 512;
@@ -67,19 +81,20 @@ constexpr int LDF = 68;
 constexpr uint32_t kSpin = 1u << 20;  // try_wait polls before a wait is declared stuck
 constexpr int BAR_P = 1, BAR_S = 2;   // named barriers of the two roles
 constexpr int BAR_PA = 3;             // producer warps 0-3 (the UT inverse)
-constexpr int BAR_Q = 4;              // producer warps 1-7 (while thread 0 issues W and U)
+constexpr int BAR_Q = 4;              // producer warps 1-7 (A/L readout)
+constexpr int BAR_R = 5;              // producer warps 4-7 (next chunk's factors)
 typedef __nv_bfloat16 bf16;
 
 struct TmaMaps {
     CUtensorMap q, k, v;  // [T rows x heads*128 columns] bf16 views, 64x64 boxes, 128-byte swizzle
 };
 
+// Per-slot values that only the producer reads (written a chunk ahead).
 struct SlotSmall {
-    float fac[64];  // e^{G_last - G_j} / |k_j|: token factor of K~
-    float qf[64];   // scale e^{G_i} / |q_i|: row factor of Q~
-    float eglast;   // e^{G_last}
-    int tb, valid;  // first token and valid rows of the chunk
-    int pad;
+    float qf[64];    // scale e^{G_i} / |q_i|: row factor of Q~
+    float fac[64];   // e^{G_last - G_j} / |k_j|: row factor of K~
+    float beta[64];  // beta_j
+    float fbg[64];   // beta_j e^{G_j} / |k_j|: column factor of Tbg
 };
 
 // One job of a CTA's chunk stream (shared memory).  span = {global index of
@@ -100,40 +115,44 @@ constexpr int kRing = 8;  // jobs in flight per CTA: at most about 5 are live at
 
 // What the roles need of one chunk of the stream, filled two chunks ahead
 // (entry gq & 7 holds chunk gq; it is overwritten when chunk gq + 8 is filled,
-// by which time both roles are past chunk gq).
+// by which time both roles are past chunk gq).  eglast is written by the
+// producer's gate prefix of the chunk, a chunk ahead of the consumer.
 struct ChunkInfo {
     int tb, valid;      // first token, valid rows
     int hv, hk;         // value head, key head
     int vz, write_o;    // value columns zero; o written
     int first, last;    // first / last chunk of its job
     int jr;             // ring entry of its job
-    int pad[3];
+    float eglast;       // e^{G_last}
+    int pad[2];
 };
 
 struct SmemWS {
-    bf16 QK[2][128 * 128];  // per slot: Q/K rows (order above); K rows become W, Q rows -Q~
-    bf16 B2[2][192 * 64];   // per slot: A (64 rows) and K~^T (128 rows), order above
+    bf16 QK[2][128 * 128];  // per slot: Q rows 0-63 (scaled to Q~ in place), K rows 64-127 (W^T once read)
+    bf16 KT[2][64 * 128];   // per slot: K~ [token][key], MN-major B of the state update
+    bf16 A[2][64 * 64];     // per slot: A [token][token], K-major B of the output update
     bf16 V[64 * 128];       // [token][value column]
     bf16 S[128 * 128];      // S^T [value column][key column] (bf16 copy of the state)
-    bf16 VN[128 * 64];      // v_new^T [value column][token]
+    bf16 VN[128 * 64];      // v_new^T [value column][token]; output staging as [token][value]
     bf16 Tb[64 * 64];       // T diag(beta)
     bf16 Tbg[64 * 64];      // T diag(beta e^G / |k|)
     __align__(16) float LT[64 * LDF];  // L; the inverse's blocks replace it block by block
     SlotSmall slot[2];
-    __align__(16) float beta[64];
     __align__(16) float G[64];
     __align__(16) float eG[64];
     __align__(16) float eGl[64];
     __align__(16) float rn[128];  // 1/|q_i| (0-63), 1/|k_j| (64-127); 1 without the L2-norm flag
-    // per-chunk factors; e^{G_i - G_j} = e^{G_i - G_r} e^{G_r - G_j} with G_r = G_31
-    __align__(16) float colf[64];  // e^{G_r - G_j} / |k_j|
-    __align__(16) float rowA[64];  // scale e^{G_i - G_r} / |q_i|
-    __align__(16) float rowL[64];  // beta_i e^{G_i - G_r} / |k_i|
-    __align__(16) float fbg[64];   // beta_j e^{G_j} / |k_j|
-    int factored;                  // the split exponentials stay well inside fp32 range
-    uint64_t mbar_p, mbar_s;       // tensor-core completion, producer / consumer
+    // split decay mask e^{G_i - G_j} = e^{G_i - G_r} e^{G_r - G_j}, with one
+    // reference token r_b = 16 b + 7 per 16-row block b of the rows i
+    __align__(16) float colf[4][64];  // e^{G_{r_b} - G_j} / |k_j|
+    __align__(16) float rowA[64];     // scale e^{G_i - G_r} / |q_i|
+    __align__(16) float rowL[64];     // beta_i e^{G_i - G_r} / |k_i|
+    float Gref[4];
+    int factored;                  // the split factors stay well inside fp32 range
+    uint64_t mbar_p, mbar_s, mbar_o;  // tensor-core completion: Gram; chain products; output products
+    uint64_t mbar_q;               // the first product (last reader of the slot's Q/K tile) done
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
-    uint64_t gfree;                // the producer has read this chunk's [rows] K^T columns
+    uint64_t gfree;                // the producer has read this chunk's [Q;K] K^T columns
     uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
     uint64_t fin_p, fin_s, fin_s2; // end-of-job drains of the issuing threads' products
     int qk_issued[2], qk_waited[2], v_issued, v_waited;
@@ -148,20 +167,26 @@ struct SmemWS {
     int lpt_left;  // without a work queue: the CTA's one job is still to be pushed
     int lpt_b[3];
     int acq_ok;    // the first jobs were pushed without a ring timeout
+    int abort;     // a role gave up: every bounded wait of the other role returns
     ChunkInfo ci[8];
+    float ored[4][64];  // gated norm: per value-lane quarter, each token's sum of o^2
 };
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
 constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
-constexpr uint32_t ID_N128_NEG = tc::idesc_bf16(128, 128, false, false, true);
-constexpr uint32_t ID_N192 = tc::idesc_bf16(128, 192, false, false, false);
+constexpr uint32_t ID_VNEW = tc::idesc_bf16(128, 64, false, true, true);     // B MN-major, A negated
+constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 
 // One warp: the chunk's gate prefix from per-token values held by lanes
 // (lane l holds g of tokens 2l and 2l+1; beta likewise), written to shared
-// memory with e^G, e^{G_last - G}, beta, and whether split exponentials
-// around G_31 stay within fp32 range.
+// memory with e^G, e^{G_last - G}, beta, the block references of the split
+// decay mask and whether the split factors stay within fp32 range: inside a
+// block b, |G_i - G_{r_b}| < 60, and G_{r_b} - G_j < 60 for every j up to the
+// block's end (a column factor that underflows stands for a decay product
+// that underflows as well).  e^{G_last} goes to the chunk's info entry.
 template <class Sm>
-__device__ __forceinline__ void gate_prefix_fast(Sm& sm, float g0, float g1, float b0, float b1) {
+__device__ __forceinline__ void gate_prefix_fast(Sm& sm, SlotSmall& sl, ChunkInfo& ci, float g0, float g1, float b0,
+                                                 float b1) {
     const int lane = threadIdx.x & 31;
     float s = g0 + g1;
 #pragma unroll
@@ -171,19 +196,47 @@ __device__ __forceinline__ void gate_prefix_fast(Sm& sm, float g0, float g1, flo
     }
     const float G1 = s, G0 = s - g1;
     const float Gl = __shfl_sync(0xffffffffu, s, 31);
-    const float Gr = __shfl_sync(0xffffffffu, s, 15);  // G_31 = inclusive sum through token 31
+    const float Gr = __shfl_sync(0xffffffffu, G1, (lane & ~7) + 3);  // G of token 16 b + 7
+    float mn = fminf(G0, G1);  // running minimum of G
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, mn, off);
+        if (lane >= off) mn = fminf(mn, t);
+    }
+    const float mend = __shfl_sync(0xffffffffu, mn, lane | 7);  // through the block's last token
+    float dev = fmaxf(fmaxf(fabsf(G0 - Gr), fabsf(G1 - Gr)), Gr - mend);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
     sm.G[2 * lane] = G0;
     sm.G[2 * lane + 1] = G1;
     sm.eG[2 * lane] = __expf(G0);
     sm.eG[2 * lane + 1] = __expf(G1);
     sm.eGl[2 * lane] = __expf(Gl - G0);
     sm.eGl[2 * lane + 1] = __expf(Gl - G1);
-    sm.beta[2 * lane] = b0;
-    sm.beta[2 * lane + 1] = b1;
-    float dev = fmaxf(fabsf(G0 - Gr), fabsf(G1 - Gr));
+    sl.beta[2 * lane] = b0;
+    sl.beta[2 * lane + 1] = b1;
+    if ((lane & 7) == 3) sm.Gref[lane >> 3] = Gr;
+    if (lane == 0) {
+        sm.factored = dev < 60.f;
+        ci.eglast = __expf(Gl);
+    }
+}
+
+// One warp: 32 values per lane in, lane l out with the sum over the warp's
+// lanes of their value l (a butterfly that halves the values each step).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
-    if (lane == 0) sm.factored = dev < 60.f;
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool up = (lane & k) != 0;
+#pragma unroll
+        for (int i = 0; i < k; ++i) {
+            const float send = up ? v[i] : v[i + k];
+            const float keep = up ? v[i + k] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+        }
+    }
+    return v[0];
 }
 
 // Flag hand-over between the two halves of a split item (global memory).
@@ -195,15 +248,17 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// Waits (at most about one second) for a released flag; false on expiry.
-__device__ __forceinline__ bool wait_flag(const int32_t* f) {
+// Waits (at most `limit_ns` of the global timer) for a released flag; false
+// on expiry.
+__device__ __forceinline__ bool wait_flag(const int32_t* f, long long limit_ns, const volatile int* abort) {
     uint64_t t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         if (ld_acquire(f)) return true;
+        if (*abort) return false;
         uint64_t t;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        if (t - t0 > 1000000000ull) return false;
+        if ((long long)(t - t0) > limit_ns) return false;
         __nanosleep(256);
     }
     return false;
@@ -249,7 +304,8 @@ __device__ __forceinline__ void store_tb16_neg(const float (&acc)[2][4], bf16* T
 // there from the start.
 template <class Sync>
 __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, const float* beta, const float* fbg,
-                                              int gtid, Sync sync) {
+                                              int gtid, Sync sync, int gq) {
+    (void)gq;
     const int gw = gtid >> 5;
     auto blk = [&](int a, int b) { return Ls + 16 * a * LDF + 16 * b; };
     if (gtid < 64) {
@@ -274,6 +330,7 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
         for (int i = 0; i < 16; ++i) Lb[i * LDF + dc] = x[i];
     }
     sync();
+    if (gtid == 0) GDN_STAMP(gq, 11);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (gw < 2) {
@@ -294,6 +351,7 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
         mma_block16_tf32<LDF>(acc2, blk(gw, 1), blk(1, 1));
     }
     sync();
+    if (gtid == 0) GDN_STAMP(gq, 12);
     if (gw >= 2) {
         mma_block16_tf32<LDF>(acc, blk(gw, 1), blk(1, 0));
         __syncwarp();
@@ -319,6 +377,7 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
         }
     }
     sync();
+    if (gtid == 0) GDN_STAMP(gq, 13);
     {
         const int a = 2 + (gw >> 1), b = gw & 1;
 #pragma unroll
@@ -346,7 +405,8 @@ __device__ __noinline__ bool acquire_jobs(const ChunkParams& p, int src, SmemWS&
     volatile int* vdone = &sm.jdone;
     while (!sm.src_end && sm.chunks < need) {
         if (sm.jn - *vdone >= kRing) {
-            for (uint32_t it = 0; it < kSpin && sm.jn - *vdone >= kRing; ++it) __nanosleep(64);
+            const volatile int* vab = &sm.abort;
+            for (uint32_t it = 0; it < kSpin && sm.jn - *vdone >= kRing && !*vab; ++it) __nanosleep(64);
             if (sm.jn - *vdone >= kRing) return false;
         }
         int bx, by, bz, part = 0, first_chunks = 0, flag = 0;
@@ -460,7 +520,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         if (!p.sched) lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
         if (tid == 0) {
             for (int i = 0; i < kRing; ++i) sm.ring[i].span = make_int2(-1, 0);
-            sm.jn = sm.jdone = sm.chunks = sm.src_end = 0;
+            sm.jn = sm.jdone = sm.chunks = sm.src_end = sm.abort = 0;
             sm.lpt_left = p.sched ? 0 : 1;
             sm.lpt_b[0] = bx;
             sm.lpt_b[1] = by;
@@ -484,6 +544,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     if (tid == 0) {
         tc::mbar_init(&sm.mbar_p, 1);
         tc::mbar_init(&sm.mbar_s, 1);
+        tc::mbar_init(&sm.mbar_o, 1);
+        tc::mbar_init(&sm.mbar_q, 1);
         tc::mbar_init(&sm.full[0], 2);  // the W/U products' commit and a producer thread
         tc::mbar_init(&sm.full[1], 2);
         tc::mbar_init(&sm.wfree, 1);
@@ -497,26 +559,40 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         sm.qk_issued[0] = sm.qk_issued[1] = sm.qk_waited[0] = sm.qk_waited[1] = 0;
         sm.v_issued = sm.v_waited = 0;
     }
+    // A above its diagonal and the upper blocks of Tb/Tbg stay zero; the
+    // readout below writes only blocks that hold kept entries
+    for (int e = tid; e < 2 * 64 * 64 / 8; e += NT) reinterpret_cast<uint4*>(sm.A)[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid; e < 64 * 64 / 8; e += NT) {
+        reinterpret_cast<uint4*>(sm.Tb)[e] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_async_smem();
     if (warp == 0) tc::tmem_alloc(&sm.tmem_slot, 512);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
-    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_S = tmem + 256;
+    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_S = tmem + 384;
     // per-slot columns are picked with selects (a runtime-indexed array would live in local memory)
-    const uint32_t T_VN0 = tmem + 128, T_O0 = tmem + 192, T_O1 = tmem + 384, T_VN1 = tmem + 448;
-    const uint32_t aQK0 = tc::smem_addr(sm.QK[0]), aQK1 = tc::smem_addr(sm.QK[1]);
-    const uint32_t aB20 = tc::smem_addr(sm.B2[0]), aB21 = tc::smem_addr(sm.B2[1]);
+    const uint32_t T_VN0 = tmem + 128, T_VN1 = tmem + 192, T_O0 = tmem + 256, T_O1 = tmem + 320;
+    const uint32_t aQK0 = tc::smem_addr(sm.QK[0]), aKT0 = tc::smem_addr(sm.KT[0]), aA0 = tc::smem_addr(sm.A[0]);
     const uint32_t aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S), aVN = tc::smem_addr(sm.VN);
     const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
     bool ok = sm.acq_ok != 0;
-    // base descriptors; a K step adds a constant to the start-address field
-    const uint64_t dQK0 = tc::desc(aQK0, 16, 1024), dQK1 = tc::desc(aQK1, 16, 1024);
-    // K rows as the MN-major A operand of W^T: slot 0 rows 0-63, slot 1 rows 64-127
-    const uint64_t dKmn0 = tc::desc(aQK0, 128 * 128, 1024), dKmn1 = tc::desc(aQK1 + 64 * 128, 128 * 128, 1024);
-    const uint64_t dB20 = tc::desc(aB20, 16, 1024), dB21 = tc::desc(aB21, 16, 1024);
+    // base descriptors of slot 0; a K step or the other slot adds a constant
+    // to the start-address field (slot 1 lies a fixed distance further on)
+    const uint64_t dQK0 = tc::desc(aQK0, 16, 1024);          // [Q;K] rows, Q~ rows
+    const uint64_t dK0 = tc::desc(aQK0 + 8192, 16, 1024);    // K rows
+    // K rows as the MN-major A operand of W^T (atoms 16 KB apart); W^T rows as
+    // the MN-major B operand of v_new (keys 0-63 in atom 0's K rows, 64-127 in atom 1's)
+    const uint64_t dKmn0 = tc::desc(aQK0 + 8192, 16384, 1024);
+    const uint64_t dKT0 = tc::desc(aKT0, 8192, 1024);
+    const uint64_t dA0 = tc::desc(aA0, 16, 1024);
     const uint64_t dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024), dVN = tc::desc(aVN, 16, 1024);
     const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
+    constexpr uint64_t kQKslot = sizeof(bf16) * 128 * 128 / 16, kKTslot = sizeof(bf16) * 64 * 128 / 16,
+                       kAslot = sizeof(bf16) * 64 * 64 / 16;
+    auto wtoff = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 2048) >> 4); };
 
     // The CTA's chunks form one stream over its jobs, indexed by gq; every
     // barrier phase and slot follows gq.  Chunk gq is in the stream once
@@ -525,11 +601,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     auto stream_len = [&]() -> int { return *reinterpret_cast<volatile int*>(&sm.chunks); };
 
     // Q/K of chunk gq into its slot: four 64x64 boxes (128-byte swizzle = the
-    // operand layout); one thread
+    // operand layout), Q into rows 0-63 and K into rows 64-127; one thread
     auto issue_qk = [&](int gq, int tbn, int hk) {
         const int ss = gq & 1;
-        bf16* qd = sm.QK[ss] + (ss ? 0 : 64 * 64);
-        bf16* kd = sm.QK[ss] + (ss ? 64 * 64 : 0);
+        bf16* qd = sm.QK[ss];
+        bf16* kd = sm.QK[ss] + 64 * 64;
         uint64_t* bar = &sm.ld_qk[ss];
         tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
         tc::tma_load_2d(qd, &maps.q, hk * 128, tbn, bar);
@@ -538,25 +614,36 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::tma_load_2d(kd + 128 * 64, &maps.k, hk * 128 + 64, tbn, bar);
         sm.qk_issued[ss] += 1;
     };
+    // [Q;K] K^T of chunk gq once its Q/K have landed (one thread); true when
+    // the load arrived
+    auto issue_gram = [&](int gq) -> bool {
+        const int ss = gq & 1;
+        if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort)) return false;
+        sm.qk_waited[ss] += 1;
+        tc::fence_after();
+        const uint64_t so = ss ? kQKslot : 0, dA = dQK0 + so, dB = dK0 + so;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
+        tc::commit(&sm.mbar_p);
+        return true;
+    };
 
     if (producer) {
         // ====================== producer warpgroups ======================
-        const bf16* __restrict__ beta = static_cast<const bf16*>(p.beta);
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
-        uint32_t ph = 0;  // phase of the [rows] K^T completions
+        uint32_t ph = 0;  // phase of the [Q;K] K^T completions
         int nvw = 0;      // thread 0: V loads waited for
-        // g and beta of chunk gq into warp 1's registers (lane l: tokens 2l, 2l+1)
+        // g and beta of chunk gq into warp 5's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
         auto load_gb = [&](int gq) {
-            if (warp == 1) {
+            if (warp == 5) {
                 const ChunkInfo& I = sm.ci[gq & 7];
                 const int tbn = I.tb, hv = I.hv, vn = I.valid;
                 const int r0 = 2 * lane, r1 = 2 * lane + 1;
                 const int64_t t0 = tbn + r0, t1 = tbn + r1;
-                g_next0 = r0 < vn ? __ldg(p.g + t0 * p.Hv + hv) : 0.f;
-                g_next1 = r1 < vn ? __ldg(p.g + t1 * p.Hv + hv) : 0.f;
-                b_next0 = r0 < vn ? __bfloat162float(beta[t0 * p.Hv + hv]) : 0.f;
-                b_next1 = r1 < vn ? __bfloat162float(beta[t1 * p.Hv + hv]) : 0.f;
+                g_next0 = g_next1 = b_next0 = b_next1 = 0.f;
+                if (r0 < vn) gate_beta<bf16>(p, t0, hv, g_next0, b_next0);
+                if (r1 < vn) gate_beta<bf16>(p, t1, hv, g_next1, b_next1);
             }
         };
         auto issue_v = [&](int gq) {  // one thread
@@ -569,24 +656,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 sm.v_issued += 1;
             }
         };
-        // Once chunk gq's Q/K have landed: [rows] K^T on the tensor cores (one
-        // thread).  True when the load arrived.
-        auto issue_gram = [&](int gq) -> bool {
-            const int ss = gq & 1;
-            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin)) return false;
-            sm.qk_waited[ss] += 1;
-            tc::fence_after();
-            const uint64_t dA = ss ? dQK1 : dQK0, dB = ss ? dQK1 + (uint64_t)((64 * 128) >> 4) : dQK0;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
-            tc::commit(&sm.mbar_p);
-            return true;
-        };
-        // the L2 norms of chunk gq's 128 rows (warps 4-7, one thread per row;
-        // rn[0-63] Q rows, rn[64-127] K rows)
+        // warps 4-7 (f = 0..127, one row each): the L2 norms of chunk gq's
+        // rows (rn[0-63] Q rows, rn[64-127] K rows)
         auto norms = [&](int gq) -> bool {
             const int ss = gq & 1;
-            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin)) return false;
+            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort)) return false;
             const int r = gt - 128;
             float acc0 = 0.f, acc1 = 0.f;
             if (l2) {
@@ -603,42 +677,102 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     }
                 }
             }
-            const bool qrow = ss ? (r < 64) : (r >= 64);
-            sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
+            sm.rn[r] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
             return true;
         };
-        // Chunk gq's per-row factors and slot values (its norms are in rn), on
-        // warps 1-7 (thread 0 is issuing the previous chunk's W and U): the gate
-        // prefix on warp 1, then the factors on threads 32-159.
-        auto prep = [&](int gq, bool extra) -> bool {
+        // warps 4-7: chunk gq's gate prefix (warp 5) and per-row factors (its
+        // norms are in rn); `in` is this thread's verdict so far
+        auto prep = [&](int gq, bool in) -> bool {
             const int ss = gq & 1;
-            if (warp == 1) gate_prefix_fast(sm, g_next0, g_next1, b_next0, b_next1);
-            if (!tc::bar_and(BAR_Q, GS - 32, extra)) return false;
-            if (gt >= 32 && gt < 160) {
-                const int f = gt - 32, i = f & 63;
-                const float r = sm.rn[f], Gi = sm.G[i], Gr = sm.G[31];
-                if (f < 64) {
-                    sm.rowA[i] = p.scale * r * __expf(Gi - Gr);
-                    sm.slot[ss].qf[i] = p.scale * sm.eG[i] * r;
-                } else {
-                    sm.colf[i] = r * __expf(Gr - Gi);
-                    sm.rowL[i] = sm.beta[i] * r * __expf(Gi - Gr);
-                    sm.fbg[i] = sm.beta[i] * sm.eG[i] * r;
-                    sm.slot[ss].fac[i] = sm.eGl[i] * r;
-                }
-                if (f == 0) {
-                    sm.slot[ss].eglast = sm.eG[63];
-                    sm.slot[ss].tb = sm.ci[gq & 7].tb;
-                    sm.slot[ss].valid = sm.ci[gq & 7].valid;
-                }
+            SlotSmall& sl = sm.slot[ss];
+            if (warp == 5) gate_prefix_fast(sm, sl, sm.ci[gq & 7], g_next0, g_next1, b_next0, b_next1);
+            if (!tc::bar_and(BAR_R, 128, in)) return false;
+            const int f = gt - 128;
+            if (f < 64) {
+                const int i = f;
+                const float r = sm.rn[i], Gi = sm.G[i];
+                sm.rowA[i] = p.scale * r * __expf(Gi - sm.Gref[i >> 4]);
+                sl.qf[i] = p.scale * sm.eG[i] * r;
+            } else {
+                const int j = f - 64;
+                const float rk = sm.rn[64 + j], Gj = sm.G[j], bj = sl.beta[j];
+                sm.rowL[j] = bj * rk * __expf(Gj - sm.Gref[j >> 4]);
+                sl.fbg[j] = bj * sm.eG[j] * rk;
+                sl.fac[j] = sm.eGl[j] * rk;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) sm.colf[b][j] = (j < 16 * (b + 1)) ? rk * __expf(sm.Gref[b] - Gj) : 0.f;
             }
             return true;
         };
-        // blocks above the diagonal of Tb and Tbg stay zero
-        for (int e = gt; e < 64 * 64 / 8; e += GS) {
-            reinterpret_cast<uint4*>(sm.Tb)[e] = make_uint4(0u, 0u, 0u, 0u);
-            reinterpret_cast<uint4*>(sm.Tbg)[e] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        // warps 4-7: Q~ = diag(qf) Q in place and K~ = diag(fac) K into the
+        // slot's K~ tile (same swizzled chunk positions), 16 chunks per thread
+        auto qk_prep = [&](int gq) {
+            const int ss = gq & 1;
+            const SlotSmall& sl = sm.slot[ss];
+            bf16* QKs = sm.QK[ss];
+            bf16* KTs = sm.KT[ss];
+            const int f = gt - 128;
+#pragma unroll 4
+            for (int k = 0; k < 16; ++k) {
+                const int e = f + 128 * (k & 7), r = e >> 4, ch = e & 15;
+                const bool isk = k >= 8;
+                const float fs = isk ? sl.fac[r] : sl.qf[r];
+                const uint4 raw = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, (isk ? 64 : 0) + r, ch)]);
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 t2 = __bfloat1622float2(h[i]);
+                    x[2 * i] = t2.x * fs;
+                    x[2 * i + 1] = t2.y * fs;
+                }
+                bf16* dst = isk ? &KTs[tc::sw128_chunk(64, r, ch)] : &QKs[tc::sw128_chunk(128, r, ch)];
+                *reinterpret_cast<uint4*>(dst) = pack8(x);
+            }
+        };
+        // A (Q rows, lanes 0-63) and L (K rows, lanes 64-127) from the Q K^T /
+        // K K^T blocks: this thread's lane, columns [32 hh, 32 hh + 32)
+        auto al_readout = [&](int s, int hh) {
+            const bool isq = row < 64;
+            const int i = row & 63;
+            float gv[32];
+            tc::ld32(T_GRAM + lb + 32 * hh, gv);
+            float a[32];
+            const int lim = isq ? i : i - 1;  // A keeps the diagonal, L does not
+            if (sm.factored) {
+                const float fi = isq ? sm.rowA[i] : sm.rowL[i];
+                const float4* cf = reinterpret_cast<const float4*>(sm.colf[i >> 4] + 32 * hh);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 f4 = cf[c4];
+                    const float fc[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c2 = 4 * c4 + e;
+                        a[c2] = (32 * hh + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
+                    }
+                }
+            } else {  // wide gate range: one exponential per element
+                const float Gi = sm.G[i];
+                const float fi = isq ? p.scale * sm.rn[i] : sm.slot[s].beta[i] * sm.rn[64 + i];
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const int j = 32 * hh + c2;
+                    a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
+                }
+            }
+            if (isq) {
+                bf16* As = sm.A[s];
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4*>(&As[tc::sw128_chunk(64, i, 4 * hh + c8)]) = pack8(&a[8 * c8]);
+            } else {
+                float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * hh);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
+            }
+        };
         bool pend = true;  // this thread's verdict on work whose barrier is still ahead
         if (stream_len() > 0 && ok) {
             if (gt == 32) {
@@ -646,10 +780,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (stream_len() > 1) issue_qk(1, sm.ci[1].tb, sm.ci[1].hk);
                 issue_v(0);
             }
-            load_gb(0);
-            if (warp != 0) {
-                bool in = true;
-                if (gt >= 128) in = norms(0);
+            if (gt >= 128) {
+                load_gb(0);
+                bool in = norms(0);
                 if (gt == 224 && in) in = issue_gram(0);
                 pend = prep(0, in);
             }
@@ -658,122 +791,95 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         for (int g = 0; g < len && ok; ++g) {
             const int s = g & 1;
             const bool vz = gt == 0 && sm.ci[g & 7].vz != 0;  // thread 0: no U product for this chunk
-            bf16* B2s = sm.B2[s];
-            // A (Q rows) and L (K rows) from the Q K^T / K K^T blocks: this
-            // thread's lane, columns [32 hh, 32 hh + 32)
-            auto al_readout = [&](int hh) {
-                const bool isq = s ? (row < 64) : (row >= 64);
-                const int i = row & 63;
-                float gv[32];
-                tc::ld32(T_GRAM + lb + 32 * hh, gv);
-                float a[32];
-                const int lim = isq ? i : i - 1;  // A keeps the diagonal, L does not
-                if (sm.factored) {
-                    const float fi = isq ? sm.rowA[i] : sm.rowL[i];
-                    const float4* cf = reinterpret_cast<const float4*>(sm.colf + 32 * hh);
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 f4 = cf[c4];
-                        const float fc[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c2 = 4 * c4 + e;
-                            a[c2] = (32 * hh + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
-                        }
-                    }
-                } else {  // wide gate range: one exponential per element
-                    const float Gi = sm.G[i];
-                    const float fi = isq ? p.scale * sm.rn[i] : sm.beta[i] * sm.rn[64 + i];
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) {
-                        const int j = 32 * hh + c2;
-                        a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
-                    }
-                }
-                if (isq) {
-                    const int arow = (s ? 128 : 0) + i;
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(&B2s[tc::sw128_chunk(192, arow, 4 * hh + c8)]) = pack8(&a[8 * c8]);
-                } else {
-                    float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * hh);
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
-                }
-            };
-            // warps 1-7: chunk g's [rows] K^T, then A and L (warp 4 also takes
-            // warp 0's lanes); thread 0 meanwhile finishes the previous chunk's
-            // W and U, which must have read Tb and Tbg before the inverse below
-            // rewrites them
+            // ---- A: chunk g's [Q;K] K^T, then A and L (warps 1-7: warp w takes
+            // lane quarter w & 3 and column half w >> 2; a half with no kept
+            // entry is skipped, and warp 4 takes warp 0's quarter); thread 0
+            // meanwhile waits for the previous chunk's W and U, which must have
+            // read Tb, Tbg and V before the inverse and the next V load rewrite them
             if (warp != 0) {
-                bool a = pend && tc::mbar_wait(&sm.mbar_p, ph, kSpin);
+                if (gt == 32) GDN_STAMP(g, 0);
+                bool a = pend && tc::mbar_wait(&sm.mbar_p, ph, kSpin, &sm.abort);
                 a = tc::bar_and(BAR_Q, GS - 32, a);
                 tc::fence_after();
+                if (gt == 32) GDN_STAMP(g, 1);
                 if (a) {
-                    if (g + 1 < len) load_gb(g + 1);
-                    al_readout(half);
-                    if (warp == 4) al_readout(0);
+                    const int qd = warp & 3, hh = warp == 4 ? 0 : (warp >> 2);
+                    if (!(hh == 1 && (qd & 1) == 0)) al_readout(s, hh);  // quarters 0, 2: rows 0-31 of A / L
                 }
                 tc::fence_before();
                 pend = tc::bar_and(BAR_Q, GS - 32, a);
+                if (gt == 32) GDN_STAMP(g, 2);
                 if (gt == 32 && pend) tc::mbar_arrive(&sm.gfree);
             } else if (gt == 0 && g >= 1) {
-                // the previous chunk's W and U are done: V is free for this chunk's
-                // load, issued now so that it has the A/L readout and the inverse
-                // to land (chunk 0: prologue)
-                pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((g - 1) >> 1) & 1, kSpin);
+                pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((g - 1) >> 1) & 1, kSpin, &sm.abort);
                 if (pend) issue_v(g);
             }
             ph ^= 1u;
+            tc::fence_async_smem();
             tc::fence_before();
             if (!(ok = tc::bar_and(BAR_P, GS, pend))) break;
             tc::fence_after();
-            // the UT inverse (warps 0-3, straight into Tb and Tbg); thread 160:
-            // the stream two chunks ahead
+            if (gt == 0) GDN_STAMP(g, 3);
+            // ---- B: the UT inverse (warps 0-3, straight into Tb and Tbg); warps
+            // 4-7: Q~ and K~ of this chunk, the next chunk's norms, gate prefix
+            // and factors, and (thread 128) the stream two chunks ahead
             bool nok = true;
             if (gt < 128) {
-                ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.beta, sm.fbg, gt, [] { tc::bar_sync(BAR_PA, 128); });
-            } else if (gt == 160) {
-                // the job of chunk g + 2, taken no earlier than the pipeline needs
-                // it (the consumer loads that chunk's Q/K during chunk g; out of
-                // line, once per job), and that chunk's info
-                if (!sm.src_end && sm.chunks < g + 3) nok = acquire_jobs(p, src, sm, g + 3);
-                if (g + 2 < sm.chunks) fill_chunk_info(sm, g + 2);
+                ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.slot[s].beta, sm.slot[s].fbg, gt,
+                              [] { tc::bar_sync(BAR_PA, 128); }, g);
+                if (gt == 0) GDN_STAMP(g, 4);
+            } else {
+                if (g + 1 < len) load_gb(g + 1);
+                qk_prep(g);
+                if (gt == 128) GDN_STAMP(g, 5);
+                bool in = true;
+                if (g + 1 < len) {
+                    in = norms(g + 1);
+                    if (gt == 128) GDN_STAMP(g, 6);
+                    in = prep(g + 1, in);
+                    if (gt == 128) GDN_STAMP(g, 7);
+                }
+                nok = in;
+                if (gt == 128) {
+                    // the job of chunk g + 2, taken no earlier than the pipeline needs
+                    // it (the consumer loads that chunk's Q/K during chunk g; out of
+                    // line, once per job), and that chunk's info
+                    if (!sm.src_end && sm.chunks < g + 3) nok = nok && acquire_jobs(p, src, sm, g + 3);
+                    if (g + 2 < sm.chunks) fill_chunk_info(sm, g + 2);
+                }
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
             len = stream_len();
-            // thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed and the
-            // consumer has read the previous W; warps 1-7: the next chunk's norms
-            // (warps 4-7), gate prefix and factors
+            if (gt == 0) GDN_STAMP(g, 8);
+            // ---- C: thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed
+            // and the consumer has read the previous W
             if (gt == 0) {
                 bool w = true;
                 if (!vz) {
-                    w = tc::mbar_wait(&sm.ld_v, nvw & 1, kSpin);
+                    w = tc::mbar_wait(&sm.ld_v, nvw & 1, kSpin, &sm.abort);
                     nvw += 1;
                 }
-                if (w && g >= 1) w = tc::mbar_wait(&sm.wfree, (g - 1) & 1, kSpin);
+                if (w && g >= 1) w = tc::mbar_wait(&sm.wfree, (g - 1) & 1, kSpin, &sm.abort);
+                GDN_STAMP(g, 9);
                 if (w) {
                     if (!vz) sm.v_waited += 1;
                     tc::fence_after();
                     const uint32_t T_U = s ? T_VN1 : T_VN0;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        tc::mma(T_W, (s ? dKmn1 : dKmn0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        tc::mma(T_W, dKmn0 + (s ? kQKslot : 0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                         if (!vz) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                     }
                     tc::commit(&sm.full[s]);
                     tc::mbar_arrive(&sm.full[s]);
                 }
+                GDN_STAMP(g, 10);
                 pend = w;
-            } else if (warp != 0 && g + 1 < len) {
-                bool in = true;
-                if (gt >= 128) in = norms(g + 1);
-                pend = prep(g + 1, in);
             }
         }
         if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
+        if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
         if (gt == 0 || gt == 224) {  // every product these threads issued has completed
             uint64_t* fb = gt ? &sm.fin_s2 : &sm.fin_p;
             tc::commit(fb);
@@ -782,9 +888,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     } else {
         // ====================== consumer warpgroups ======================
         bf16* __restrict__ o = static_cast<bf16*>(p.o);
-        uint32_t ph = 0;
-        auto wait_mma = [&]() -> bool {
-            const bool done = tc::mbar_wait(&sm.mbar_s, ph, kSpin);
+        uint32_t ph = 0;  // phase of the chain products' completions
+        auto wait_s = [&]() -> bool {
+            const bool done = tc::mbar_wait(&sm.mbar_s, ph, kSpin, &sm.abort);
             ph ^= 1u;
             const bool all = tc::bar_and(BAR_S, GS, done);
             tc::fence_after();
@@ -793,9 +899,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         // The fp32 state lives in the state columns of tensor memory: thread
         // (row, half) holds S^T row `row` (value column), key columns
         // [64 half, 64 half + 64), in 32-column pieces q2.
-        // A job's initial state into the state columns and its bf16 copy (the A
-        // operand of the first product) into shared memory.
-        auto load_state = [&](const JobRec& J) {
+        // A job's initial state: its bf16 copy (the A operand of the first
+        // product) into shared memory, and the state scaled by e^{G_last} of
+        // the job's first chunk (the first update accumulates onto it) into
+        // the state columns.
+        auto load_state = [&](const JobRec& J, float eg) {
             const float* ini = J.init;
             const int64_t ild = J.init_ld;
             const bool idi = J.identity_init != 0;
@@ -811,11 +919,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     else if (ini) s0 = ini[(int64_t)d * ild + row];
                     v[c2] = s0;
                 }
-                tc::st32(T_S + lb + 64 * half + 32 * q2, v);
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8)
                     *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 4 * q2 + c8)]) =
                         pack8(&v[8 * c8]);
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2) v[c2] *= eg;
+                tc::st32(T_S + lb + 64 * half + 32 * q2, v);
             }
             tc::wait_st();
         };
@@ -832,24 +942,82 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
             }
         };
-        // o columns start at zero (and v_new columns too when no U product writes them)
-        float zero[32];
+        // W^T of the chunk in slot ss from tensor memory into the slot's K
+        // rows (free once K~ is copied and the W/U products have run), as the
+        // MN-major [key][token] operand: this thread's key row, tokens
+        // [32 half, 32 half + 32), four 16-byte chunks
+        auto w_readout = [&](int ss) {
+            float wv[32];
+            tc::ld32(T_W + lb + 32 * half, wv);
+            unsigned char* base = reinterpret_cast<unsigned char*>(sm.QK[ss]) + (row >> 6) * 16384 + 8192 + (row & 63) * 128;
 #pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2) zero[c2] = 0.f;
-        tc::st32(T_O0 + lb + 32 * half, zero);
-        tc::st32(T_O1 + lb + 32 * half, zero);
-        if (stream_len() > 0 && sm.ci[0].vz) tc::st32(T_VN0 + lb + 32 * half, zero);
-        tc::wait_st();
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const int ch = 4 * half + c8;
+                *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = pack8(&wv[8 * c8]);
+            }
+        };
+        // The pending output of chunk og (slot og & 1), tensor memory -> global
+        // memory: thread (row, half) holds value column `row` of tokens
+        // [32 half, 32 half + 32); a warp's 32 lanes store 64 contiguous bytes
+        // of a token row at a time (no shared-memory staging).  With the gated
+        // norm (the wrappers' norm(o, z) on rows of head_v_dim) each token's
+        // sum of squares of its bf16 outputs is reduced over the 128 value
+        // lanes (warp butterfly, then the four lane quarters through shared
+        // memory) and the stores write norm_w * o / sqrt(mean(o^2) + eps) * silu(z).
+        const bool gnorm = p.z != nullptr;
+        auto write_output = [&](int og, int otb, int ovalid, int ohv) -> bool {
+            bool w = tc::mbar_wait(&sm.mbar_o, og & 1, kSpin, &sm.abort);
+            if (!tc::bar_and(BAR_S, GS, w)) return false;
+            tc::fence_after();
+            float ov[32];
+            tc::ld32(((og & 1) ? T_O1 : T_O0) + lb + 32 * half, ov);
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) ov[c2] = __bfloat162float(__float2bfloat16_rn(ov[c2]));
+            bf16* orow = o + ((int64_t)(otb + 32 * half) * p.Hv + ohv) * 128 + row;
+            const int64_t ost = (int64_t)p.Hv * 128;
+            const int nv = min(32, ovalid - 32 * half);  // valid tokens of this half
+            if (!gnorm) {
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2)
+                    if (c2 < nv) orow[c2 * ost] = __float2bfloat16_rn(ov[c2]);
+                return true;
+            }
+            float sq[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) sq[c2] = ov[c2] * ov[c2];
+            sm.ored[warp & 3][32 * half + lane] = reduce_scatter32(sq);
+            tc::bar_sync(BAR_S, GS);
+            const int tk = 32 * half + lane;  // this lane's token for the row factor
+            const float rl = rsqrtf((sm.ored[0][tk] + sm.ored[1][tk] + sm.ored[2][tk] + sm.ored[3][tk]) * (1.f / 128.f) +
+                                    p.norm_eps);
+            const float wv = __bfloat162float(static_cast<const bf16*>(p.norm_w)[row]);
+            const bf16* zrow = static_cast<const bf16*>(p.z) + (int64_t)(otb + 32 * half) * p.ldz + ohv * 128 + row;
+#pragma unroll
+            for (int c16 = 0; c16 < 2; ++c16) {
+                float zv[16];
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2)
+                    zv[c2] = (16 * c16 + c2 < nv) ? __bfloat162float(zrow[(int64_t)(16 * c16 + c2) * p.ldz]) : 0.f;
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) {
+                    const int cc = 16 * c16 + c2;
+                    const float r = __shfl_sync(0xffffffffu, rl, cc);
+                    const float y = wv * (ov[cc] * r) * __fdividef(zv[c2], 1.f + __expf(-zv[c2]));
+                    if (cc < nv) orow[cc * ost] = __float2bfloat16_rn(y);
+                }
+            }
+            return true;
+        };
         if (stream_len() == 0 && ok) {  // a job without tokens: its final state is its initial state
-            load_state(sm.ring[0]);
+            load_state(sm.ring[0], 1.f);
             store_state(sm.ring[0]);
         }
-        tc::fence_async_smem();
         tc::fence_before();
         tc::bar_sync(BAR_S, GS);
-        int o_tb = 0, o_valid = 0, o_slot = 0, o_hv = 0;
+        int o_tb = 0, o_valid = 0, o_hv = 0, o_g = 0;
         bool o_pending = false;
-        int g = 0;        // chunk of the stream
+        bool w_ready = false;  // W^T of chunk g is already in shared memory
+        int g = 0;             // chunk of the stream
         int len = stream_len();  // chunks in the stream when last read (at least 2 ahead, or all)
         while (ok && g < len) {
             // a job: its initial state (a second half waits for the first's final
@@ -859,146 +1027,65 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             const bool write_o = J.write_o != 0;
             {
                 bool fl = true;
-                if (J.part == 2) fl = wait_flag(p.sched + 2 + J.flag);
+                if (J.part == 2) fl = wait_flag(p.sched + kSchedHeader + J.flag, p.handover_ns, &sm.abort);
                 if (!(ok = tc::bar_and(BAR_S, GS, fl))) break;
-                load_state(J);
             }
             for (int c = 0; c < nchj && ok; ++c, ++g) {
                 const int s = g & 1;
-                // [rows] K^T of chunk g + 1 as soon as its Q/K are in and the producer
-                // has read chunk g's columns (the producer's first wait of chunk g + 1)
+                bool qok = true;  // thread 0: the refill's wait for the first product
+                if (gt == 0) GDN_STAMP(g, 16);
+                // [Q;K] K^T of chunk g + 1 as soon as its Q/K are in and the producer
+                // has read chunk g's columns
                 bool gok = true;
                 if (gt == 0 && g + 1 < len) {
-                    gok = tc::mbar_wait(&sm.gfree, g & 1, kSpin) && tc::mbar_wait(&sm.ld_qk[s ^ 1], ((g + 1) >> 1) & 1, kSpin);
-                    if (gok) {
-                        sm.qk_waited[s ^ 1] += 1;
-                        tc::fence_after();
-                        const uint64_t dA = s ? dQK0 : dQK1, dB = s ? dQK0 : dQK1 + (uint64_t)((64 * 128) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
-                        tc::commit(&sm.mbar_p);
-                    }
+                    gok = tc::mbar_wait(&sm.gfree, g & 1, kSpin, &sm.abort) && issue_gram(g + 1);
+                    GDN_STAMP(g, 17);
                 }
-                if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (g >> 1) & 1, kSpin)))) break;
+                // chunk g's operands: W/U products done, Q~ / K~ / A / factors written
+                if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (g >> 1) & 1, kSpin, &sm.abort)))) break;
                 tc::fence_after();
-                // the producer has topped up the stream for chunk g + 2: what this
-                // chunk needs of the next two, read ahead of use
+                if (gt == 0) GDN_STAMP(g, 18);
                 len = stream_len();
-                const bool vz_next = g + 1 < len && sm.ci[(g + 1) & 7].vz;
-                int qk_tb = 0, qk_hk = 0;
-                if (gt == 0 && g + 2 < len) {
-                    qk_tb = sm.ci[(g + 2) & 7].tb;
-                    qk_hk = sm.ci[(g + 2) & 7].hk;
-                }
-                const float eglast = sm.slot[s].eglast;
-                const int tb = sm.slot[s].tb, valid = sm.slot[s].valid;
-                bf16* QKs = sm.QK[s];
-                bf16* B2s = sm.B2[s];
-                const int qrow0 = s ? 0 : 64, krow0 = 64 - qrow0;  // Q and K rows of the slot's tile
-                // -Q~ in place and K~^T (the K rows are overwritten by W next)
-                if (write_o) {  // -Q~ = -(scale e^G / |q|) Q, in place
-                    for (int e = gt; e < 64 * 16; e += GS) {
-                        const int r = e >> 4, c8 = e & 15;
-                        uint4* ptr = reinterpret_cast<uint4*>(&QKs[tc::sw128_chunk(128, qrow0 + r, c8)]);
-                        uint4 raw = *ptr;
-                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                        const float f = -sm.slot[s].qf[r];
-                        float x[8];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 t2 = __bfloat1622float2(h[i]);
-                            x[2 * i] = t2.x * f;
-                            x[2 * i + 1] = t2.y * f;
-                        }
-                        *ptr = pack8(x);
-                    }
-                }
-                // K~^T [key column][token] = K[token][key column] e^{G_last - G_token} / |k_token|
-                const float* fac = sm.slot[s].fac;
-                const int ktrow0 = s ? 0 : 64;
-                for (int t = gt; t < 512; t += GS) {
-                    // a warp: 2 column chunks x 16 token pairs, the two half-warps on
-                    // different token halves (distinct banks for loads and stores)
-                    const int w4 = t >> 5, ln = t & 31, hw = ln >> 4;
-                    const int j0 = 2 * (16 * ((w4 >> 3) ^ hw) + (ln & 15)), ch = 2 * (w4 & 7) + hw;
-                    const uint4 k0 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0, ch)]);
-                    const uint4 k1 = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, krow0 + j0 + 1, ch)]);
-                    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&k0);
-                    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&k1);
-                    const float f0 = fac[j0], f1 = fac[j0 + 1];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
-                        const int d = 8 * ch + 2 * i;
-                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d, j0)]) =
-                            __floats2bfloat162_rn(a0.x * f0, a1.x * f1);
-                        *reinterpret_cast<__nv_bfloat162*>(&B2s[tc::sw128(192, ktrow0 + d + 1, j0)]) =
-                            __floats2bfloat162_rn(a0.y * f0, a1.y * f1);
-                    }
-                }
-                tc::bar_sync(BAR_S, GS);
-                {  // W [token][key column] into the K rows of the slot's Q/K tile
-                    float wv[32];
-                    tc::ld32(T_W + lb + 32 * half, wv);
-                    const int d = row, wrow0 = s ? 64 : 0;
-                    bf16* wb = QKs + (d >> 6) * 128 * 64 + (wrow0 + 32 * half) * 64 + (d & 7);
-                    const int dch = (d & 63) >> 3;
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
-                }
+                const ChunkInfo& I = sm.ci[g & 7];
+                const int tb = I.tb, valid = I.valid;
+                const bool vz = I.vz != 0;
+                if (c == 0) load_state(J, I.eglast);
+                const bool w_now = !w_ready;  // W^T not read during the previous chunk
+                if (w_now) w_readout(s);
+                w_ready = false;
                 tc::fence_async_smem();
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
                 if (gt == 0) {
-                    tc::mbar_arrive(&sm.wfree);
+                    GDN_STAMP(g, 19);
+                    if (w_now) tc::mbar_arrive(&sm.wfree);  // the W columns are free for the next W product
                     tc::fence_after();
-                    // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T  (row order of the slot)
-                    const uint32_t D1 = s ? T_O1 : T_VN0;
-                    const uint64_t dB = s ? dQK1 : dQK0;
+                    // v_new^T = U^T - S^T W^T (no U product: the first step overwrites)
+                    const uint32_t DV = s ? T_VN1 : T_VN0;
+                    const uint64_t dW = dKmn0 + (s ? kQKslot : 0);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma(D1, dS + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N128_NEG, 1u);
+                        tc::mma(DV, dS + tc::koff(128, kk), dW + wtoff(kk), ID_VNEW, (kk > 0 || !vz) ? 1u : 0u);
                     tc::commit(&sm.mbar_s);
-                }
-                // while it runs: the previous chunk's output (through the v_new tile,
-                // free until this chunk's v_new, as [token][value column] rows), its
-                // o columns back to zero, the next chunk's v_new columns to zero when
-                // no U product writes them, and e^{G_last} S^T into the state columns
-                if (o_pending) {
-                    float ov[32];
-                    tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
-                    bf16* ot = sm.VN + (32 * half) * 128 + row;
+                    if (write_o) {  // o^T = S^T Q~^T
+                        const uint32_t DO = s ? T_O1 : T_O0;
+                        const uint64_t dQ = dQK0 + (s ? kQKslot : 0);
 #pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
-                }
-                if (g >= 1) tc::st32((s ? T_O0 : T_O1) + lb + 32 * half, zero);
-                if (vz_next)
-                    tc::st32((s ? T_VN0 : T_VN1) + lb + 32 * half, zero);
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {  // S^T <- e^{G_last} S^T in place
-                    float es[32];
-                    tc::ld32(T_S + lb + 64 * half + 32 * q2, es);
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) es[c2] *= eglast;
-                    tc::st32(T_S + lb + 64 * half + 32 * q2, es);
-                }
-                tc::wait_st();
-                if (o_pending) {  // 16-byte stores of the staged rows
-                    tc::bar_sync(BAR_S, GS);
-                    for (int e = gt; e < 64 * 16; e += GS) {
-                        const int t = e >> 4, ch = e & 15;
-                        if (t < o_valid)
-                            *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + o_hv) * 128 + 8 * ch) =
-                                *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma(DO, dS + tc::koff(128, kk), dQ + tc::koff(128, kk), ID_N64, kk > 0);
                     }
+                    tc::commit(&sm.mbar_q);
+                    GDN_STAMP(g, 20);
                 }
-                tc::fence_before();
-                if (!(ok = wait_mma())) break;
-                // the first product was the last reader of the slot's Q/K tile: refill
-                // it with the Q/K of chunk g + 2 (the second product reads only A and K~^T)
-                if (gt == 0 && g + 2 < len) issue_qk(g + 2, qk_tb, qk_hk);
-                {  // v_new^T [value column][token] as the A operand of the second product
+                // while it runs: the previous chunk's output
+                if (o_pending) {
+                    if (!(ok = write_output(o_g, o_tb, o_valid, o_hv))) break;
+                    o_pending = false;
+                }
+                if (gt == 0) GDN_STAMP(g, 21);
+                if (!(ok = wait_s())) break;
+                if (gt == 0) GDN_STAMP(g, 22);
+                {  // v_new^T [value column][token] as the A operand of the updates
                     float vv[32];
                     tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
 #pragma unroll
@@ -1009,65 +1096,94 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
                 if (gt == 0) {
+                    GDN_STAMP(g, 23);
                     tc::fence_after();
-                    // [o^T | S^T] += v_new^T [A ; K~^T]^T  (row order of the slot)
-                    const uint32_t D2 = s ? T_S : T_O0;
-                    const uint64_t dB = s ? dB21 : dB20;
+                    // S^T <- e^{G_last} S^T + v_new^T K~ (the scaled state is in place)
+                    const uint64_t dKT = dKT0 + (s ? kKTslot : 0);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) tc::mma(D2, dVN + tc::koff(128, kk), dB + tc::koff(192, kk), ID_N192, 1u);
+                    for (int kk = 0; kk < 4; ++kk) tc::mma(T_S, dVN + tc::koff(128, kk), dKT + tc::mnoff(kk), ID_N128_BMN, 1u);
                     tc::commit(&sm.mbar_s);
+                    if (write_o) {  // o^T += v_new^T A^T
+                        const uint32_t DO = s ? T_O1 : T_O0;
+                        const uint64_t dAs = dA0 + (s ? kAslot : 0);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) tc::mma(DO, dVN + tc::koff(128, kk), dAs + tc::koff(64, kk), ID_N64, 1u);
+                    }
+                    tc::commit(&sm.mbar_o);
+                    GDN_STAMP(g, 24);
+                    // the first product was the last reader of the slot's Q/K tile:
+                    // refill it with the Q/K of chunk g + 2
+                    if (g + 2 < len) {
+                        qok = tc::mbar_wait(&sm.mbar_q, g & 1, kSpin, &sm.abort);
+                        if (qok) issue_qk(g + 2, sm.ci[(g + 2) & 7].tb, sm.ci[(g + 2) & 7].hk);
+                    }
                 }
-                if (!(ok = wait_mma())) break;
+                // while it runs: W^T of chunk g + 1, if its products are done
+                if (g + 1 < len) {
+                    bool rdy = true;
+                    if (gt == 0) rdy = tc::mbar_test(&sm.full[s ^ 1], ((g + 1) >> 1) & 1);
+                    if (tc::bar_and(BAR_S, GS, rdy)) {
+                        tc::fence_after();
+                        w_readout(s ^ 1);
+                        w_ready = true;
+                    }
+                }
+                if (gt == 0) GDN_STAMP(g, 25);
+                tc::fence_before();
+                if (!(ok = wait_s() && tc::bar_and(BAR_S, GS, qok))) break;
+                if (gt == 0 && w_ready) tc::mbar_arrive(&sm.wfree);  // every thread has read chunk g + 1's W
+                if (gt == 0) GDN_STAMP(g, 26);
+                if (c + 1 < nchj) {
+                    // the new state: its bf16 copy, and the state scaled by the next
+                    // chunk's e^{G_last} back into tensor memory
+                    const float egn = sm.ci[(g + 1) & 7].eglast;
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {  // S <- e^{G_last} S + K~^T v_new: its bf16 copy
-                    float sv[32];
-                    tc::ld32(T_S + lb + 64 * half + 32 * q2, sv);
+                    for (int q4 = 0; q4 < 4; ++q4) {  // 16-column pieces (bounded register use)
+                        float sv[16];
+                        tc::ld16(T_S + lb + 64 * half + 16 * q4, sv);
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 4 * q2 + c8)]) =
-                            pack8(&sv[8 * c8]);
+                        for (int c8 = 0; c8 < 2; ++c8)
+                            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 2 * q4 + c8)]) =
+                                pack8(&sv[8 * c8]);
+#pragma unroll
+                        for (int c2 = 0; c2 < 16; ++c2) sv[c2] *= egn;
+                        tc::st16(T_S + lb + 64 * half + 16 * q4, sv);
+                    }
+                    tc::wait_st();
+                } else {
+                    store_state(J);
                 }
                 o_tb = tb;
                 o_valid = valid;
-                o_slot = s;
                 o_hv = hvj;
+                o_g = g;
                 o_pending = write_o;
                 tc::fence_async_smem();
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
+                if (gt == 0) GDN_STAMP(g, 27);
             }
             if (!ok) break;
-            store_state(J);
             if (J.part == 1) {  // hand the final state to the second half
-                tc::bar_sync(BAR_S, GS);
-                if (gt == 0) {
+                if (gt == 0 && !p.no_publish) {
                     __threadfence();
-                    st_release(p.sched + 2 + J.flag, 1);
+                    st_release(p.sched + kSchedHeader + J.flag, 1);
                 }
             }
             tc::bar_sync(BAR_S, GS);
             if (gt == 0) *reinterpret_cast<volatile int*>(&sm.jdone) += 1;  // the job's ring entry is free
         }
-        if (ok && o_pending) {  // the last chunk's output, the same way
-            float ov[32];
-            tc::ld32((o_slot ? T_O1 : T_O0) + lb + 32 * half, ov);
-            bf16* ot = sm.VN + (32 * half) * 128 + row;
-#pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) ot[c2 * 128] = __float2bfloat16_rn(ov[c2]);
-            tc::bar_sync(BAR_S, GS);
-            for (int e = gt; e < 64 * 16; e += GS) {
-                const int t = e >> 4, ch = e & 15;
-                if (t < o_valid)
-                    *reinterpret_cast<uint4*>(o + ((int64_t)(o_tb + t) * p.Hv + o_hv) * 128 + 8 * ch) =
-                        *reinterpret_cast<const uint4*>(sm.VN + t * 128 + 8 * ch);
-            }
-        }
+        if (ok && o_pending) ok = write_output(o_g, o_tb, o_valid, o_hv);  // the last chunk's output
+        if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
         if (tid == GS) {  // every product this thread issued has completed
             tc::commit(&sm.fin_s);
             tc::mbar_wait(&sm.fin_s, 0, kSpin);
         }
     }
-    if (!ok && gt == 0) atomicAdd(&g_gdn_timeouts, 1);
+    if (!ok && gt == 0) {
+        atomicAdd(&g_gdn_timeouts, 1);
+        if (p.status) atomicCAS(p.status, 0, (int)GDN_ERR_TIMEOUT);
+    }
     tc::fence_before();
     __syncthreads();
     if (tid == 0) {  // copies still in flight after an early exit land before the memory is released
@@ -1118,7 +1234,13 @@ static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t
     return GDN_OK;
 }
 
+// Split-item hand-over settings (a testing hook, gdn_debug_set_handover).
+static long long g_handover_ns = 1000000000ll;
+static int g_handover_publish = 1;
+
 gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
+    p.handover_ns = g_handover_ns;
+    p.no_publish = g_handover_publish ? 0 : 1;
     const size_t smem = sizeof(SmemWS) + 1024;
     gdn_status st = set_smem_attr((const void*)chunk_tc_kernel, smem);
     if (st != GDN_OK) return st;
@@ -1130,6 +1252,7 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
     }
     if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the order kernel's scratch
+    if (!p.status && p.sched) p.status = p.sched + 2;  // the work queue's status word
     if (p.sched) {  // work queue: the order of the entries, then one persistent CTA per SM
         static int sms[64];
         int dev = 0;
@@ -1151,3 +1274,18 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
 }
 
 }  // namespace gdn
+
+extern "C" gdn_status gdn_debug_set_handover(int64_t wait_ns, int publish) {
+    if (wait_ns < 0) return gdn::fail(GDN_ERR_INVALID_ARG, "wait_ns=%lld < 0", (long long)wait_ns);
+    gdn::g_handover_ns = wait_ns;
+    gdn::g_handover_publish = publish ? 1 : 0;
+    return GDN_OK;
+}
+
+#ifdef GDN_PHASE_STAMPS
+extern "C" int gdn_debug_phase_stamps(long long* out, int n) {
+    if (n > gdn::kStampN * 32) n = gdn::kStampN * 32;
+    if (cudaMemcpyFromSymbol(out, gdn::g_gdn_stamps, sizeof(long long) * n) != cudaSuccess) return -1;
+    return n;
+}
+#endif

@@ -79,7 +79,52 @@ __global__ void empty_seq_final_kernel(const int32_t* __restrict__ cu, int Hv, i
         h_final[n * sz + e] = h0 ? h0[n * sz + e] : 0.f;
 }
 
+// Gated RMS norm in place, one warp per (token, value head) row of dv
+// values (the wrappers' norm(core_attn_out, z) on rows of head_v_dim):
+// o <- w * o / sqrt(mean(o^2) + eps) * silu(z); the tensor-core chunk kernel
+// applies the same as its output epilogue instead.
+template <typename E>
+__global__ void gated_norm_kernel(E* __restrict__ o, const E* __restrict__ z, int64_t ldz, const E* __restrict__ w,
+                                  float eps, int64_t rows, int Hv, int dv) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const int64_t t = r / Hv;
+    const int h = (int)(r - t * Hv);
+    E* orow = o + r * dv;
+    const E* zrow = z + t * ldz + (int64_t)h * dv;
+    float ss = 0.f;
+    for (int d = lane; d < dv; d += 32) {
+        const float x = Elem<E>::to_f(orow[d]);
+        ss = fmaf(x, x, ss);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = rsqrtf(ss / (float)dv + eps);
+    for (int d = lane; d < dv; d += 32) {
+        const float zz = Elem<E>::to_f(zrow[d]);
+        const float y = Elem<E>::to_f(w[d]) * (Elem<E>::to_f(orow[d]) * inv) * (zz / (1.f + expf(-zz)));
+        orow[d] = Elem<E>::from_f(y);
+    }
+}
+
 }  // namespace
+
+gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w, float eps, int64_t T, int Hv,
+                             int dv, gdn_dtype dt, cudaStream_t s) {
+    const int64_t rows = T * Hv;
+    if (rows == 0) return GDN_OK;
+    const int wpb = 8;
+    const unsigned blocks = (unsigned)((rows + wpb - 1) / wpb);
+    if (dt == GDN_BF16)
+        gated_norm_kernel<__nv_bfloat16><<<blocks, 32 * wpb, 0, s>>>(
+            static_cast<__nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(z), ldz,
+            static_cast<const __nv_bfloat16*>(w), eps, rows, Hv, dv);
+    else
+        gated_norm_kernel<float><<<blocks, 32 * wpb, 0, s>>>(static_cast<float*>(o), static_cast<const float*>(z),
+                                                             ldz, static_cast<const float*>(w), eps, rows, Hv, dv);
+    return check_launch("gated_norm_kernel");
+}
 
 gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
                           int dv, float* S_in, const int32_t* plan, cudaStream_t s) {

@@ -93,7 +93,45 @@ struct ChunkParams {
     int32_t* sched;
     int sched_items, sched_m, sched_ny;
     int num_sms;
+    // device status word (plan or work-queue header) that receives
+    // GDN_ERR_TIMEOUT when a bounded wait expires, or null
+    int32_t* status;
+    // limit of the split-item hand-over wait (ns of the global timer); a
+    // test hook may also stop first halves from publishing their state
+    long long handover_ns;
+    int no_publish;
+    // gates from the raw projections (a_raw != null): g = -exp(A_log[h])
+    // softplus(a + dt_bias[h]) and beta = sigmoid(b), with b read through
+    // `beta`; otherwise g and beta are read as given
+    const void* a_raw;
+    const float* A_log;
+    const float* dt_bias;
+    // gated RMS norm of the output (z != null, tensor-core kernel only):
+    // o <- norm_w * o / sqrt(mean(o^2) + norm_eps) * silu(z), z row stride ldz
+    const void* z;
+    int64_t ldz;
+    const void* norm_w;
+    float norm_eps;
 };
+
+// g and beta of token t, value head hv (E = the input dtype).  With raw
+// projections, the wrappers' formulas ([HP-CP] P2P / all-gather forward):
+// g = -exp(A_log) softplus(a + dt_bias) in fp32 (softplus(x) = x beyond 20,
+// as torch's threshold), beta = sigmoid(b) rounded to the input dtype.
+template <typename E>
+__device__ __forceinline__ void gate_beta(const ChunkParams& p, int64_t t, int hv, float& g, float& b) {
+    const int64_t i = t * p.Hv + hv;
+    const E* bp = static_cast<const E*>(p.beta);
+    if (p.a_raw) {
+        const float x = Elem<E>::load(static_cast<const E*>(p.a_raw) + i) + __ldg(p.dt_bias + hv);
+        const float sp = x > 20.f ? x : log1pf(__expf(x));
+        g = -__expf(__ldg(p.A_log + hv)) * sp;
+        b = Elem<E>::to_f(Elem<E>::from_f(1.f / (1.f + __expf(-Elem<E>::load(bp + i)))));
+    } else {
+        g = __ldg(p.g + i);
+        b = Elem<E>::load(bp + i);
+    }
+}
 
 // Resolve a block index (bx = job item, by = value head, bz = state tile)
 // -> job.  Returns false when this CTA has nothing to do.
@@ -276,10 +314,13 @@ __device__ __forceinline__ void lpt_block(const ChunkParams& p, int src, int* le
     bz = rem / gridDim.y;
 }
 
-// Offset (in words, even: the entries are read as int2) of the sorted entries
-// in the schedule words.
+// Schedule words of a ticket-scheduled launch: [0] ticket counter, [1] entry
+// count, [2] status word (0, or GDN_ERR_TIMEOUT once a bounded wait expired),
+// [3] unused, then one hand-over flag per (item, head, tile) from
+// kSchedHeader, then the sorted entries at an even offset (read as int2).
+constexpr int kSchedHeader = 4;
 __host__ __device__ __forceinline__ int64_t chunk_sched_order_off(int S, int m) {
-    const int64_t o = 2 + (int64_t)S * m;
+    const int64_t o = kSchedHeader + (int64_t)S * m;
     return o + (o & 1);
 }
 // schedule.cu: words of a launch's schedule (S items, m head/tile pairs) and
@@ -306,6 +347,9 @@ gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, c
 // combine.cu: plan == null -> every shard affine
 gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
                           int dv, float* S_in, const int32_t* plan, cudaStream_t s);
+// gated RMS norm of o in place (combine.cu), for the kernels without the epilogue
+gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w, float eps, int64_t T, int Hv,
+                             int dv, gdn_dtype dt, cudaStream_t s);
 // empty sequences in the shard path: h_final = h0 or 0
 gdn_status launch_empty_seq_final(const int32_t* cu, int num_seqs, int Hv, int dk, int dv,
                                   const float* h0, float* h_final, const int32_t* plan,

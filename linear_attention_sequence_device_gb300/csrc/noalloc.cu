@@ -20,10 +20,32 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCR
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};  // the context the cached address belongs to
+
+typedef int (*CtxGetCurrentFn)(void**);
+
+// The driver's cuCtxGetCurrent (through the runtime's entry-point query, so
+// that the library needs no link against the driver library).
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+        tried = true;
+    }
+    return fn;
+}
 
 // Device address of g_noalloc_scratch on the current device.  In host code
-// the symbol is only a host-side stand-in, so the address is looked up once
-// per device with that device current, and cached.
+// the symbol is only a host-side stand-in, so the address is looked up with
+// the device current and cached per device, together with the CUDA context
+// it belongs to: a new primary context on the device (after cudaDeviceReset)
+// reloads the module, and the address is looked up again.
 gdn_status scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -31,12 +53,20 @@ gdn_status scratch_address(void** out) {
     if (dev < 0 || dev >= kMaxDevices)
         return fail(GDN_ERR_INVALID_ARG, "device %d beyond the %d supported", dev, kMaxDevices);
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    void* ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (get) get(&ctx);
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        if (!get || !ctx) {  // the runtime has made a context current by now
+            ctx = nullptr;
+            if (get) get(&ctx);
+        }
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return GDN_OK;

@@ -14,9 +14,11 @@
 // Layout of the schedule words (int32, device):
 //   [0]                    ticket counter, zeroed here
 //   [1]                    number of entries n
-//   [2, 2 + S*m)           hand-over flags, one per (item, head, tile), zeroed here
+//   [2]                    status word, zeroed here (a chunk kernel whose bounded
+//                          wait expires writes GDN_ERR_TIMEOUT into it)
+//   [4, 4 + S*m)           hand-over flags, one per (item, head, tile), zeroed here
 //   [o + 2r, o + 2r + 1]   entry of rank r < n: item | part << 16, chunks of the
-//                          first half (o = 2 + S*m rounded up to even)
+//                          first half (o = 4 + S*m rounded up to even)
 // part: 0 whole item, 1 first half, 2 second half.
 #include "gdn_internal.cuh"
 
@@ -38,7 +40,7 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const ChunkParams 
         s_sum = 0ull;
         s_n = 0;
     }
-    for (int64_t i = tid; i < (int64_t)S * m; i += kOrderThreads) w[2 + i] = 0;
+    for (int64_t i = tid; i < (int64_t)S * m; i += kOrderThreads) w[kSchedHeader + i] = 0;
     __syncthreads();
     const int nvt = p.dv / p.col_tile;
     for (int x = tid; x < S; x += kOrderThreads) {
@@ -105,6 +107,8 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const ChunkParams 
     if (tid == 0) {
         w[0] = 0;
         w[1] = s_n;
+        w[2] = 0;
+        w[3] = 0;
     }
 }
 

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.parity import assert_close, chunk_inputs, dev, f64, rel_l2, to_dev
+from tests.parity import assert_close, chunk_inputs, dev, f64, path_inputs, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -205,6 +205,45 @@ def test_chunk_fwd_split_sequences_match_unsplit():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+def test_expired_handover_wait_reports_timeout():
+    """A second half whose first half never publishes its final state (the
+    gdn_debug_set_handover hook) waits out a 2 ms limit instead of hanging:
+    the kernel stops early, writes GDN_ERR_TIMEOUT (7) into the launch's
+    status word (word 2 of the gdn_chunk_fwd workspace; the plan's word for
+    gdn_shard_fwd) and counts a timeout.  The next launches on the same
+    context run normally and match the oracle."""
+    import linear_attention_sequence_device_gb300 as g
+    b = g.binding
+    w = make_chunk_workload(("bf16", 2, 4, 128, 128, (1280, 800, 150), 0.05, 0.5))
+    host, d = chunk_inputs(w)
+    ws = torch.zeros(b.chunk_fwd_workspace_size(w.N, w.Hv, 128, 128, torch.bfloat16), dtype=torch.uint8,
+                     device=dev())
+    wp = W.Workload("handover", 2240, 2, 4, 128, 128, "bf16", 1, 13, (1280, 800, 160))
+    _, dp = path_inputs(wp)
+    b.device_timeouts(reset=True)
+    try:
+        b.debug_set_handover(2_000_000, publish=False)
+        g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"], workspace=ws)
+        _, _, plan = g.gdn_shard_fwd(dp["x"], dp["conv_w"], None, dp["g"], dp["beta"], dp["cu"], wp.Hk, wp.Hv,
+                                     wp.dk, wp.dv, 1, want_plan=True)
+        torch.cuda.synchronize()
+    finally:
+        b.debug_set_handover()
+    assert int(ws.view(torch.int32)[2]) == 7
+    assert int(plan[0]) == 7
+    assert b.device_timeouts(reset=True) >= 2
+    o, hf = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"], workspace=ws)
+    _, _, plan = g.gdn_shard_fwd(dp["x"], dp["conv_w"], None, dp["g"], dp["beta"], dp["cu"], wp.Hk, wp.Hv,
+                                 wp.dk, wp.dv, 1, want_plan=True)
+    torch.cuda.synchronize()
+    assert int(ws.view(torch.int32)[2]) == 0 and int(plan[0]) == 0
+    assert b.device_timeouts() == 0
+    o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                                       host["h0"], w.cu_seqlens(), w.scale)
+    assert_close(f64(o), o_ref, w.dtype, "o")
+    assert_close(f64(hf), hf_ref, w.dtype, "h_final")
+
+
 def test_chunk_fwd_schedule_many_sequences():
     """300 sequences (bf16, d = 128), most short, a few between half and 0.7 of
     the longest: the launch's schedule words, read back, hold every item once
@@ -228,7 +267,8 @@ def test_chunk_fwd_schedule_many_sequences():
     n = int(words[1])
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert words[0] == n * m + min(sms, 2 * S * m)   # one ticket past the end per CTA
-    off = 2 + S * m + ((2 + S * m) & 1)
+    assert words[2] == 0                              # status word: no wait expired
+    off = 4 + S * m + ((4 + S * m) & 1)
     ent = words[off:off + 2 * n].reshape(n, 2)
     items, parts, first = ent[:, 0] & 0xFFFF, ent[:, 0] >> 16, ent[:, 1]
     chunks = [(L + 63) // 64 for L in lengths]

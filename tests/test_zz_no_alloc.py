@@ -49,6 +49,21 @@ def test_noalloc_matches_workspace_path_two_calls(g):
         assert rel_l2(f64(hf), f64(hf_ref)) <= TOL_REL_L2[w.dtype], w.name
 
 
+def test_noalloc_split_item_after_a_sharded_call(g):
+    """One shard whose sequence lengths make the tensor-core kernel split an
+    item into two halves chained through flags in the scratch array, right
+    after a multi-shard call has left its own contents there: the flags are
+    rewritten by the call, so the result matches gdn_shard_fwd with a fresh
+    workspace, and no bounded device wait expires."""
+    g.device_timeouts(reset=True)
+    _both(g, _case(23, 4))
+    w = W.Workload("noalloc_split", 2240, 2, 4, 128, 128, "bf16", 1, 24, (1280, 800, 160), h0_std=0.02)
+    o, hf, o_ref, hf_ref = _both(g, w)
+    assert rel_l2(f64(o), f64(o_ref)) <= TOL_REL_L2[w.dtype]
+    assert rel_l2(f64(hf), f64(hf_ref)) <= TOL_REL_L2[w.dtype]
+    assert g.device_timeouts() == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(g):
     w = W.long_seq(T=8192)
     _, d = path_inputs(w)

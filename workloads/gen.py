@@ -26,6 +26,9 @@ _lib = None
 
 # tensor ids: one independent stream per input tensor
 TID_X, TID_CONV_W, TID_CONV_B, TID_Q, TID_K, TID_V, TID_BETA, TID_G, TID_H0, TID_LEN = range(1, 11)
+# the layer's raw inputs around the path: gate projections a and b, A_log,
+# dt_bias, the norm gate z and the norm weight
+TID_A, TID_B, TID_ALOG, TID_DTB, TID_Z, TID_NORMW = range(11, 17)
 KIND_NORMAL, KIND_SIGMOID, KIND_NEG_SOFTPLUS, KIND_UNIFORM = 0, 1, 2, 3
 DT_F32, DT_BF16, DT_F64 = 0, 1, 2
 
@@ -197,6 +200,33 @@ class Workload:
         return fill(self.seed, TID_H0, self.Hv * self.dk * self.dv, (0, self.N),
                     (0, self.Hv * self.dk * self.dv), b=self.h0_std,
                     dtype=DT_F32).reshape(self.N, self.Hv, self.dk, self.dv)
+
+    # ---- the layer's raw inputs (gates from projections, gated norm) -----
+    # a, b ~ N(0, 1) per (token, v-head) (so beta = sigmoid(b) has the
+    # recipe's distribution); A_log = log U[1, 16] and dt_bias ~ N(0, 1) per
+    # v-head; z ~ N(0, 1) [T, Hv, dv]; norm weight ~ 1 + N(0, 0.1^2) [dv]
+    def a_proj(self, rows=None):
+        rows = rows or (0, self.T)
+        return fill(self.seed, TID_A, self.Hv, rows, (0, self.Hv), dtype=self.dt)
+
+    def b_proj(self, rows=None):
+        rows = rows or (0, self.T)
+        return fill(self.seed, TID_B, self.Hv, rows, (0, self.Hv), dtype=self.dt)
+
+    def A_log(self):
+        u = fill(self.seed, TID_ALOG, self.Hv, (0, 1), (0, self.Hv), kind=KIND_UNIFORM, a=1.0,
+                 b=15.0)[0]
+        return np.log(u).astype(np.float32)
+
+    def dt_bias(self):
+        return fill(self.seed, TID_DTB, self.Hv, (0, 1), (0, self.Hv), dtype=DT_F32)[0]
+
+    def z(self, rows=None):
+        rows = rows or (0, self.T)
+        return fill(self.seed, TID_Z, self.Hv * self.dv, rows, (0, self.Hv * self.dv), dtype=self.dt)
+
+    def norm_w(self):
+        return fill(self.seed, TID_NORMW, self.dv, (0, 1), (0, self.dv), a=1.0, b=0.1, dtype=self.dt)[0]
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
