@@ -217,6 +217,32 @@ size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int32_t Hv, int32_t dk, in
                                     gdn_dtype dtype);
 
 /* ------------------------------------------------------------------------
+ * Head-major layout ([HP-CP] LinearAttentionUlyssesCPWrapper: after its
+ * seq-to-heads all-to-all every rank holds whole sequences of a subset of the
+ * heads; on one device that exchange is a re-layout of whole d-element rows)
+ *   gdn_to_head_major   x device [T, H, d] dtype with token stride ldx
+ *                       (elements, ldx >= H*d, 16-byte rows) -> y device
+ *                       [H, T, d] dense
+ *   gdn_to_token_major  the inverse: y [H, T, d] -> x [T, H, d] (stride ldx)
+ *   gdn_chunk_fwd_heads gdn_chunk_fwd on dense head-major q, k [Hk, T, dk],
+ *                       v [Hv, T, dv] -> o [Hv, T, dv]; g, beta [T, Hv], h0,
+ *                       h_final, cu_seqlens, scale, flags and the optional
+ *                       workspace as in gdn_chunk_fwd (same size); q, k, v, o
+ *                       16-byte aligned.  Same arithmetic as the token-major
+ *                       call, so the results are bit-identical.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_to_head_major(const void *x, int64_t ldx, gdn_dtype dtype, int32_t T, int32_t H,
+                             int32_t d, void *y, void *stream);
+gdn_status gdn_to_token_major(const void *y, gdn_dtype dtype, int32_t T, int32_t H, int32_t d,
+                              void *x, int64_t ldx, void *stream);
+gdn_status gdn_chunk_fwd_heads(const void *q, const void *k, const void *v, gdn_dtype dtype,
+                               const float *g, const void *beta, const float *h0,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                               int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                               void *o, float *h_final, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* ------------------------------------------------------------------------
  * State summary of each sequence ([HP-CP]
  * _compute_gdn_state_summary_from_prepared): the affine map of the state
  * across the sequence,  S_end = M S_start + N, with
@@ -235,9 +261,11 @@ gdn_status gdn_chunk_summary(const void *k, const void *v, int64_t ldk, int64_t 
  * Prefix merge of shard summaries ([HP-CP]
  * _merge_gdn_prefix_state_summaries_torch), for every value head h:
  *   S_in[0] = S0 (or 0);   S_in[r] = M[r-1] S_in[r-1] + N[r-1],  r = 1..P-1
- *   M device [P, Hv, dk, dk], N device [P, Hv, dk, dv], S0 device [Hv, dk, dv]
- *   or NULL, S_in device [P, Hv, dk, dv]; all fp32.  M[P-1], N[P-1] unused.
- * Sequential over r in fp32, parallel over heads and value columns.
+ *   M device [P, Hv, dk, dk] (16-byte aligned), N device [P, Hv, dk, dv],
+ *   S0 device [Hv, dk, dv] or NULL, S_in device [P, Hv, dk, dv]; all fp32.
+ *   M[P-1], N[P-1] unused.
+ * Sequential over r in fp32, parallel over heads and 32-column tiles of the
+ * state; each M is staged in shared memory while the previous one is applied.
  * ---------------------------------------------------------------------- */
 gdn_status gdn_state_combine(const float *M, const float *N, const float *S0, int32_t P,
                              int32_t Hv, int32_t dk, int32_t dv, float *S_in, void *stream);

@@ -42,6 +42,10 @@ SIGNATURES = {
     "gdn_chunk_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp,
                                      _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _u32,
                                      _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "gdn_chunk_fwd_heads": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                           _i32, _i32, _i32, _f32, _u32, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "gdn_to_head_major": (ctypes.c_int, [_vp, _i64, ctypes.c_int, _i32, _i32, _i32, _vp, _vp]),
+    "gdn_to_token_major": (ctypes.c_int, [_vp, ctypes.c_int, _i32, _i32, _i32, _vp, _i64, _vp]),
     "gdn_chunk_fwd_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, ctypes.c_int]),
     "gdn_chunk_summary": (ctypes.c_int, [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
                                          _i32, _i32, _i32, _i32, _i32, _i32, _u32, _vp, _vp,
@@ -229,6 +233,56 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, h0=None, scale=None, l2norm=Fals
                              _p(cu_seqlens), N, T, Hk, Hv, dk, dv, float(scale),
                              GDN_QK_L2NORM if l2norm else 0, _p(o), _p(hf), _p(ws),
                              0 if ws is None else ws.numel(), _stream()))
+    return o, hf
+
+
+def to_head_major(x, out=None):
+    """[T, H, d] (token-strided view with dense heads) -> dense [H, T, d]."""
+    _need(x, "x")
+    T, H, d = x.shape
+    ld = _row_stride(x, "x")
+    y = torch.empty((H, T, d), dtype=x.dtype, device=x.device) if out is None else out
+    _check(load().gdn_to_head_major(_p(x), ld, _dt(x), T, H, d, _p(y), _stream()))
+    return y
+
+
+def to_token_major(y, out=None):
+    """Dense [H, T, d] -> [T, H, d] (out may be a token-strided view)."""
+    _need(y, "y")
+    H, T, d = y.shape
+    x = torch.empty((T, H, d), dtype=y.dtype, device=y.device) if out is None else out
+    _check(load().gdn_to_token_major(_p(y.contiguous()), _dt(y), T, H, d, _p(x), _row_stride(x, "out"),
+                                     _stream()))
+    return x
+
+
+def gdn_chunk_fwd_heads(q, k, v, g, beta, cu_seqlens, h0=None, scale=None, l2norm=False, out=None,
+                        workspace=None):
+    """Head-major chunked forward: q, k [Hk, T, dk], v [Hv, T, dv] dense;
+    g, beta [T, Hv].  Returns (o [Hv, T, dv], h_final [N, Hv, dk, dv])."""
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
+        _need(t, n, dt)
+    _need(g, "g", torch.float32)
+    _need(h0, "h0", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    Hk, T, dk = q.shape
+    Hv, dv = v.shape[0], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    scale = dk ** -0.5 if scale is None else scale
+    o = torch.empty((Hv, T, dv), dtype=dt, device=q.device) if out is None else out
+    hf = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
+    lib = load()
+    if workspace is None:
+        ws = torch.empty(max(lib.gdn_chunk_fwd_workspace_size(N, Hv, dk, dv, _dt(q)), 16), dtype=torch.uint8,
+                         device=q.device)
+    else:
+        ws = workspace if workspace is not False else None
+    _check(lib.gdn_chunk_fwd_heads(_p(q.contiguous()), _p(k.contiguous()), _p(v.contiguous()), _dt(q),
+                                   _p(g.contiguous()), _p(beta.contiguous()),
+                                   _p(None if h0 is None else h0.contiguous()), _p(cu_seqlens), N, T, Hk, Hv, dk,
+                                   dv, float(scale), GDN_QK_L2NORM if l2norm else 0, _p(o), _p(hf), _p(ws),
+                                   0 if ws is None else ws.numel(), _stream()))
     return o, hf
 
 

@@ -197,10 +197,71 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
+    set_token_major(p);
     if (workspace && T > 0 && chunk_tc_eligible(dtype, dk, dv))
         p.sched = static_cast<int32_t*>(workspace);  // work queue, filled by the order kernel before the chunk kernel
     dim3 grid(num_seqs, Hv, dv / p.col_tile);
     return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_fwd_heads(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* g,
+                               const void* beta, const float* h0, const int32_t* cu_seqlens, int32_t num_seqs,
+                               int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale,
+                               uint32_t flags, void* o, float* h_final, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    const size_t need = gdn_chunk_fwd_workspace_size(num_seqs, Hv, dk, dv, dtype);
+    if (workspace && workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace_bytes, need);
+    if (workspace && !al16(workspace)) return fail(GDN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (T > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return fail(GDN_ERR_INVALID_ARG, "q/k/v/g/beta/o is NULL");
+        if (!al16(q) || !al16(k) || !al16(v) || !al16(o))
+            return fail(GDN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    }
+    if (h_final && (reinterpret_cast<uintptr_t>(h_final) & 7u))
+        return fail(GDN_ERR_INVALID_ARG, "h_final must be 8-byte aligned");
+    ChunkParams p{};
+    p.q = q; p.k = k; p.v = v; p.ldq = dk; p.ldk = dk; p.ldv = dv;
+    p.g = g; p.beta = beta; p.h0 = h0; p.cu = cu_seqlens;
+    p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = scale; p.flags = flags; p.o = o; p.h_final = h_final;
+    p.col_tile = chunk_col_tile(dtype, dk, dv);
+    // dense head-major [H, T, d]: a head is T rows further on
+    p.hsq = p.hsk = (int64_t)T * dk;
+    p.hsv = (int64_t)T * dv;
+    p.ldo = dv;
+    p.hso = (int64_t)T * dv;
+    p.head_major = 1;
+    if (workspace && T > 0 && chunk_tc_eligible(dtype, dk, dv)) p.sched = static_cast<int32_t*>(workspace);
+    dim3 grid(num_seqs, Hv, dv / p.col_tile);
+    return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
+}
+
+gdn_status gdn_to_head_major(const void* x, int64_t ldx, gdn_dtype dtype, int32_t T, int32_t H, int32_t d,
+                             void* y, void* stream) {
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return fail(GDN_ERR_DTYPE, "unknown dtype %d", (int)dtype);
+    if (T < 0 || H < 1 || d < 1) return fail(GDN_ERR_INVALID_ARG, "T=%d H=%d d=%d", T, H, d);
+    if ((d * (dtype == GDN_BF16 ? 2 : 4)) % 16 != 0) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "d=%d rows not 16-byte", d);
+    if (T == 0) return GDN_OK;
+    if (!x || !y || !al16(x) || !al16(y)) return fail(GDN_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+    if (ldx < (int64_t)H * d || (ldx * (dtype == GDN_BF16 ? 2 : 4)) % 16 != 0)
+        return fail(GDN_ERR_INVALID_ARG, "token stride %lld of x", (long long)ldx);
+    return launch_relayout(x, y, T, H, d, ldx, dtype, true, (cudaStream_t)stream);
+}
+
+gdn_status gdn_to_token_major(const void* y, gdn_dtype dtype, int32_t T, int32_t H, int32_t d, void* x,
+                              int64_t ldx, void* stream) {
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return fail(GDN_ERR_DTYPE, "unknown dtype %d", (int)dtype);
+    if (T < 0 || H < 1 || d < 1) return fail(GDN_ERR_INVALID_ARG, "T=%d H=%d d=%d", T, H, d);
+    if ((d * (dtype == GDN_BF16 ? 2 : 4)) % 16 != 0) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "d=%d rows not 16-byte", d);
+    if (T == 0) return GDN_OK;
+    if (!x || !y || !al16(x) || !al16(y)) return fail(GDN_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+    if (ldx < (int64_t)H * d || (ldx * (dtype == GDN_BF16 ? 2 : 4)) % 16 != 0)
+        return fail(GDN_ERR_INVALID_ARG, "token stride %lld of x", (long long)ldx);
+    return launch_relayout(y, x, T, H, d, ldx, dtype, false, (cudaStream_t)stream);
 }
 
 size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
@@ -229,6 +290,7 @@ gdn_status gdn_chunk_summary(const void* k, const void* v, int64_t ldk, int64_t 
     p.num_seqs = num_seqs; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
     p.scale = 1.f; p.flags = flags; p.sumN = N; p.sumM = M;
     p.col_tile = chunk_col_tile(dtype, dk, dv);
+    set_token_major(p);
     dim3 grid(num_seqs, Hv, (dv + dk) / p.col_tile);
     return launch_chunk(p, dtype, JOBS_SUMMARY, grid, (cudaStream_t)stream);
 }
@@ -236,6 +298,7 @@ gdn_status gdn_chunk_summary(const void* k, const void* v, int64_t ldk, int64_t 
 gdn_status gdn_state_combine(const float* M, const float* N, const float* S0, int32_t P, int32_t Hv,
                              int32_t dk, int32_t dv, float* S_in, void* stream) {
     if (!M || !N || !S_in) return fail(GDN_ERR_INVALID_ARG, "M/N/S_in is NULL");
+    if (!al16(M)) return fail(GDN_ERR_INVALID_ARG, "M must be 16-byte aligned");
     if (P < 1 || Hv < 1 || Hv > 65535) return fail(GDN_ERR_INVALID_ARG, "P=%d Hv=%d", P, Hv);
     if (!dim_ok(dk) || !dim_ok(dv))
         return fail(GDN_ERR_UNSUPPORTED_SHAPE, "dk=%d dv=%d must be in {32,64,128}", dk, dv);
@@ -362,6 +425,7 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
         if (tc_norm) { p.z = ex->z; p.ldz = ex->ldz; p.norm_w = ex->norm_w; p.norm_eps = ex->norm_eps; }
     }
     p.col_tile = chunk_col_tile(dtype, dk, dv);
+    set_token_major(p);
     {
         if (chunk_tc_eligible(dtype, dk, dv)) p.sched = sched;  // filled by the order kernel
         dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
@@ -375,8 +439,11 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
             return st;
         mark(3);
         // 5. pass 2: the first segment of every shard that continues a sequence
+        // (the work queue's words are free again once pass 1 has run)
+        if (chunk_tc_eligible(dtype, dk, dv)) p.sched = sched;
         dim3 grid(P, Hv, dv / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS2, grid, s)) != GDN_OK) return st;
+        p.sched = nullptr;
     } else {
         mark(3);
     }

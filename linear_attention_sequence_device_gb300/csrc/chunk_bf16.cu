@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_bf16_kernel(const ChunkParams p, 
             const int r = e / QCH, c8 = e % QCH;
             const int64_t t = tb + (r < valid ? r : 0);
             const int nb = r < valid ? 16 : 0;
-            cp_async16(&sm.Q[swz<DK>(r, c8)], q + t * p.ldq + (int64_t)hk * DK + c8 * 8, nb);
-            cp_async16(&sm.K[swz<DK>(r, c8)], k + t * p.ldk + (int64_t)hk * DK + c8 * 8, nb);
+            cp_async16(&sm.Q[swz<DK>(r, c8)], q + t * p.ldq + (int64_t)hk * p.hsq + c8 * 8, nb);
+            cp_async16(&sm.K[swz<DK>(r, c8)], k + t * p.ldk + (int64_t)hk * p.hsk + c8 * 8, nb);
         }
         if (!job.value_zero) {
             constexpr int VCH = DVT / 8;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_bf16_kernel(const ChunkParams p, 
                 const int r = e / VCH, c8 = e % VCH;
                 const int64_t t = tb + (r < valid ? r : 0);
                 cp_async16(&sm.VO[swz<DVT>(r, c8)],
-                           v + t * p.ldv + (int64_t)hv * p.dv + job.col0 + c8 * 8, r < valid ? 16 : 0);
+                           v + t * p.ldv + (int64_t)hv * p.hsv + job.col0 + c8 * 8, r < valid ? 16 : 0);
             }
         }
         cp_async_commit();
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_bf16_kernel(const ChunkParams p, 
             for (int e = tid; e < 64 * VCH; e += NT) {
                 const int r = e / VCH, c8 = e % VCH;
                 if (r < valid) {
-                    *reinterpret_cast<uint4*>(o + ((int64_t)(tb + r) * p.Hv + hv) * p.dv + job.col0 + c8 * 8) =
+                    *reinterpret_cast<uint4*>(o + (int64_t)(tb + r) * p.ldo + (int64_t)hv * p.hso + job.col0 + c8 * 8) =
                         *reinterpret_cast<const uint4*>(&sm.VO[swz<DVT>(r, c8)]);
                 }
             }

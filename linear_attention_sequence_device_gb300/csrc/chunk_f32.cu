@@ -59,14 +59,14 @@ __global__ void __launch_bounds__(NT) chunk_f32_kernel(const ChunkParams p, cons
             const int r = e / DK, d = e % DK;
             const bool ok = r < valid;
             const int64_t t = tb + r;
-            sm.Q[r][d] = ok ? q[t * p.ldq + (int64_t)hk * DK + d] : 0.f;
-            sm.K[r][d] = ok ? k[t * p.ldk + (int64_t)hk * DK + d] : 0.f;
+            sm.Q[r][d] = ok ? q[t * p.ldq + (int64_t)hk * p.hsq + d] : 0.f;
+            sm.K[r][d] = ok ? k[t * p.ldk + (int64_t)hk * p.hsk + d] : 0.f;
         }
         for (int e = tid; e < 64 * CT; e += NT) {
             const int r = e / CT, c = e % CT;
             const int64_t t = tb + r;
             sm.V[r][c] = (r < valid && !job.value_zero)
-                             ? v[t * p.ldv + (int64_t)hv * p.dv + job.col0 + c] : 0.f;
+                             ? v[t * p.ldv + (int64_t)hv * p.hsv + job.col0 + c] : 0.f;
         }
         if (tid < 64) {
             const int64_t t = tb + tid;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(NT) chunk_f32_kernel(const ChunkParams p, cons
                 for (int d = 0; d < DK; ++d) qs = fmaf(sm.Q[i][d], sm.S[d][c], qs);
                 float acc = p.scale * sm.eG[i] * qs;
                 for (int j = 0; j <= i; ++j) acc = fmaf(sm.A[i * LDL + j], sm.V[j][c], acc);
-                o[((int64_t)(tb + i) * p.Hv + hv) * p.dv + job.col0 + c] = acc;
+                o[(int64_t)(tb + i) * p.ldo + (int64_t)hv * p.hso + job.col0 + c] = acc;
             }
         }
         __syncthreads();

@@ -124,18 +124,18 @@ struct ChunkInfo {
     int first, last;    // first / last chunk of its job
     int jr;             // ring entry of its job
     float eglast;       // e^{G_last}
-    int pad[2];
+    int eg_ready;       // == the chunk's stream index once its gate prefix and factors are written
+    int aread;          // == the chunk's stream index once its [rows] K^T columns have been read
 };
 
 struct SmemWS {
-    bf16 QK[2][128 * 128];  // per slot: Q rows 0-63 (scaled to Q~ in place), K rows 64-127 (W^T once read)
+    bf16 QK[2][128 * 128];  // per slot: slot 0 [K;Q], slot 1 [Q;K]; Q becomes -Q~ in place, K becomes W once read
     bf16 KT[2][64 * 128];   // per slot: K~ [token][key], MN-major B of the state update
     bf16 A[2][64 * 64];     // per slot: A [token][token], K-major B of the output update
     bf16 V[64 * 128];       // [token][value column]
-    bf16 S[128 * 128];      // S^T [value column][key column] (bf16 copy of the state)
-    bf16 VN[128 * 64];      // v_new^T [value column][token]; output staging as [token][value]
     bf16 Tb[64 * 64];       // T diag(beta)
     bf16 Tbg[64 * 64];      // T diag(beta e^G / |k|)
+    bf16 OST[64 * 128];     // output staging: [token][value column]
     __align__(16) float LT[64 * LDF];  // L; the inverse's blocks replace it block by block
     SlotSmall slot[2];
     __align__(16) float G[64];
@@ -150,11 +150,9 @@ struct SmemWS {
     float Gref[4];
     int factored;                  // the split factors stay well inside fp32 range
     uint64_t mbar_p, mbar_s, mbar_o;  // tensor-core completion: Gram; chain products; output products
-    uint64_t mbar_q;               // the first product (last reader of the slot's Q/K tile) done
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
-    uint64_t gfree;                // the producer has read this chunk's [Q;K] K^T columns
     uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
-    uint64_t fin_p, fin_s, fin_s2; // end-of-job drains of the issuing threads' products
+    uint64_t fin_p, fin_s, fin_s2, fin_g;  // end-of-kernel drains of the issuing threads' products
     int qk_issued[2], qk_waited[2], v_issued, v_waited;
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
@@ -174,7 +172,7 @@ struct SmemWS {
 
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
 constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
-constexpr uint32_t ID_VNEW = tc::idesc_bf16(128, 64, false, true, true);     // B MN-major, A negated
+constexpr uint32_t ID_N128_NEG = tc::idesc_bf16(128, 128, false, false, false) | (1u << 14);  // B negated
 constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 
 // One warp: the chunk's gate prefix from per-token values held by lanes
@@ -294,20 +292,39 @@ __device__ __forceinline__ void store_tb16_neg(const float (&acc)[2][4], bf16* T
 // Tb = T diag(beta) and Tbg = T diag(fbg) (bf16, 128-byte-swizzled K-major
 // 64x64) for T = (I + L)^-1, the strictly lower L in Ls (fp32, row stride
 // LDF), on 128 threads (gtid 0-127; `sync` is their barrier).  16x16 blocks:
-// the diagonal blocks D_a = (I + L_aa)^-1 by forward substitution, one column
-// per thread; then warps 0 and 1 form T10 = -D1 (L10 D0) and T32 = -D3 (L32 D2)
-// while warps 2 and 3 start X = C A0^-1 for the lower-left 32x32 block C
-// (X_a0 = L_a0 D0 + L_a1 T10, X_a1 = L_a1 D1); finally the lower-left blocks
-// T_2b = -D2 X_2b and T_3b = -(T32 X_2b + D3 X_3b).  Block products are tf32
-// mma.sync; each result replaces the L block that only its own warp still
-// reads.  Blocks above the diagonal are never written: Tb and Tbg hold zeros
-// there from the start.
+// the diagonal blocks D_a = (I + L_aa)^-1 by forward substitution (one column
+// per thread); then warps 0 and
+// 1 form T10 = -D1 (L10 D0) and T32 = -D3 (L32 D2) while warps 2 and 3 start
+// X = C A0^-1 for the lower-left 32x32 block C (X_a0 = L_a0 D0 + L_a1 T10,
+// X_a1 = L_a1 D1) and write the bf16 copies of D0-D3; finally the lower-left
+// blocks T_2b = -D2 X_2b and T_3b = -(T32 X_2b + D3 X_3b).  Block products are
+// tf32 mma.sync; each result replaces the L block that only its own warp
+// still reads.  Blocks above the diagonal are never written: Tb and Tbg hold
+// zeros there from the start.
 template <class Sync>
 __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, const float* beta, const float* fbg,
                                               int gtid, Sync sync, int gq) {
     (void)gq;
     const int gw = gtid >> 5;
     auto blk = [&](int a, int b) { return Ls + 16 * a * LDF + 16 * b; };
+    // bf16 copies of a final 16x16 block of T, 8 columns per step: t < 128 the
+    // diagonal blocks D0-D3, 128-159 T10, 160-191 T32
+    auto tb_copy = [&](int t) {
+        const int bk = t >> 5, r = (t >> 1) & 15, h = t & 1;
+        const int bi = bk < 4 ? bk : (bk == 4 ? 1 : 3), bj = bk < 4 ? bk : (bk == 4 ? 0 : 2);
+        const int J = 16 * bj + 8 * h;
+        const float* src = Ls + (16 * bi + r) * LDF + J;
+        const float4 v0 = *reinterpret_cast<const float4*>(src), v1 = *reinterpret_cast<const float4*>(src + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(beta + J), b1 = *reinterpret_cast<const float4*>(beta + J + 4);
+        const float4 f0 = *reinterpret_cast<const float4*>(fbg + J), f1 = *reinterpret_cast<const float4*>(fbg + J + 4);
+        const float tb[8] = {v0.x * b0.x, v0.y * b0.y, v0.z * b0.z, v0.w * b0.w,
+                             v1.x * b1.x, v1.y * b1.y, v1.z * b1.z, v1.w * b1.w};
+        const float tg[8] = {v0.x * f0.x, v0.y * f0.y, v0.z * f0.z, v0.w * f0.w,
+                             v1.x * f1.x, v1.y * f1.y, v1.z * f1.z, v1.w * f1.w};
+        const int e = tc::sw128_chunk(64, 16 * bi + r, J >> 3);
+        *reinterpret_cast<uint4*>(Tb + e) = pack8(tb);
+        *reinterpret_cast<uint4*>(Tbg + e) = pack8(tg);
+    };
     if (gtid < 64) {
         const int da = gtid >> 4, dc = gtid & 15;
         float* Lb = blk(da, da);
@@ -349,6 +366,8 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
     } else {
         mma_block16_tf32<LDF>(acc, blk(gw, 0), blk(0, 0));
         mma_block16_tf32<LDF>(acc2, blk(gw, 1), blk(1, 1));
+        tb_copy(gtid - 64);
+        tb_copy(gtid);
     }
     sync();
     if (gtid == 0) GDN_STAMP(gq, 12);
@@ -358,23 +377,7 @@ __device__ __forceinline__ void ut_inverse_tb(float* Ls, bf16* Tb, bf16* Tbg, co
         store_block16<LDF>(acc, blk(gw, 0));
         store_block16<LDF>(acc2, blk(gw, 1));
     } else {
-        // D0-D3, T10 and T32 are final: their bf16 copies, 8 columns per step
-        for (int t = gtid; t < 192; t += 64) {
-            const int bk = t >> 5, r = (t >> 1) & 15, h = t & 1;
-            const int bi = bk < 4 ? bk : (bk == 4 ? 1 : 3), bj = bk < 4 ? bk : (bk == 4 ? 0 : 2);
-            const int J = 16 * bj + 8 * h;
-            const float* src = Ls + (16 * bi + r) * LDF + J;
-            const float4 v0 = *reinterpret_cast<const float4*>(src), v1 = *reinterpret_cast<const float4*>(src + 4);
-            const float4 b0 = *reinterpret_cast<const float4*>(beta + J), b1 = *reinterpret_cast<const float4*>(beta + J + 4);
-            const float4 f0 = *reinterpret_cast<const float4*>(fbg + J), f1 = *reinterpret_cast<const float4*>(fbg + J + 4);
-            const float tb[8] = {v0.x * b0.x, v0.y * b0.y, v0.z * b0.z, v0.w * b0.w,
-                                 v1.x * b1.x, v1.y * b1.y, v1.z * b1.z, v1.w * b1.w};
-            const float tg[8] = {v0.x * f0.x, v0.y * f0.y, v0.z * f0.z, v0.w * f0.w,
-                                 v1.x * f1.x, v1.y * f1.y, v1.z * f1.z, v1.w * f1.w};
-            const int e = tc::sw128_chunk(64, 16 * bi + r, J >> 3);
-            *reinterpret_cast<uint4*>(Tb + e) = pack8(tb);
-            *reinterpret_cast<uint4*>(Tbg + e) = pack8(tg);
-        }
+        tb_copy(128 + gtid);  // T10 and T32 are final
     }
     sync();
     if (gtid == 0) GDN_STAMP(gq, 13);
@@ -510,6 +513,214 @@ __device__ __forceinline__ void empty_sequences_final(const ChunkParams& p, int 
     }
 }
 
+
+// ---- helpers of the kernel (each is called from more than one place) ----
+
+// Q/K of chunk gq into its slot: four 64x64 boxes (128-byte swizzle = the
+// operand layout); slot 0 holds [K;Q], slot 1 [Q;K]; one thread
+__device__ __forceinline__ void issue_qk_fn(SmemWS& sm, const TmaMaps& maps, const ChunkParams& p, int gq, int tbn,
+                                         int hk) {
+    const int ss = gq & 1;
+    bf16* qd = sm.QK[ss] + (ss ? 0 : 64 * 64);
+    bf16* kd = sm.QK[ss] + (ss ? 64 * 64 : 0);
+    uint64_t* bar = &sm.ld_qk[ss];
+    // token-major views [T x Hk*128]: (hk*128 + c, t); head-major [Hk*T x 128]: (c, hk*T + t)
+    const int x0 = p.head_major ? 0 : hk * 128, y0 = p.head_major ? hk * p.T + tbn : tbn;
+    tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
+    tc::tma_load_2d(qd, &maps.q, x0, y0, bar);
+    tc::tma_load_2d(qd + 128 * 64, &maps.q, x0 + 64, y0, bar);
+    tc::tma_load_2d(kd, &maps.k, x0, y0, bar);
+    tc::tma_load_2d(kd + 128 * 64, &maps.k, x0 + 64, y0, bar);
+    sm.qk_issued[ss] += 1;
+}
+
+// V of chunk gq (unless its value columns are zero); one thread
+__device__ __forceinline__ void issue_v_fn(SmemWS& sm, const TmaMaps& maps, const ChunkParams& p, int gq) {
+    const ChunkInfo& I = sm.ci[gq & 7];
+    if (!I.vz) {
+        const int tbn = I.tb, hv = I.hv;
+        const int x0 = p.head_major ? 0 : hv * 128, y0 = p.head_major ? hv * p.T + tbn : tbn;
+        tc::mbar_expect_tx(&sm.ld_v, 2 * 64 * 64 * 2);
+        tc::tma_load_2d(sm.V, &maps.v, x0, y0, &sm.ld_v);
+        tc::tma_load_2d(sm.V + 64 * 64, &maps.v, x0 + 64, y0, &sm.ld_v);
+        sm.v_issued += 1;
+    }
+}
+
+// [rows] K^T of chunk gq once its Q/K have landed (one thread; dA = the
+// slot's 128 rows, dB = its K rows); true when the load arrived
+__device__ __forceinline__ bool issue_gram_fn(SmemWS& sm, uint32_t t_gram, uint64_t dA, uint64_t dB, int gq) {
+    const int ss = gq & 1;
+    if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort)) return false;
+    sm.qk_waited[ss] += 1;
+    tc::fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) tc::mma(t_gram, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
+    tc::commit(&sm.mbar_p);
+    return true;
+}
+
+// warps 4-7 (one row each, r = gt - 128): the L2 norms of chunk gq's rows
+// (rn[0-63] Q rows, rn[64-127] K rows); one thread waits for the load
+__device__ __forceinline__ bool norms_fn(SmemWS& sm, int gq, int gt, bool l2) {
+    const int ss = gq & 1;
+    bool in = true;
+    if (gt == 128) in = tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort);
+    if (!tc::bar_and(BAR_R, 128, in)) return false;
+    if (gt == 128) GDN_STAMP(gq - 1, 14);
+    const int r = gt - 128;
+    float acc0 = 0.f, acc1 = 0.f;
+    if (l2) {
+        const bf16* QKn = sm.QK[ss];
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, ch)]);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h2[i]);
+                acc0 = fmaf(f.x, f.x, acc0);
+                acc1 = fmaf(f.y, f.y, acc1);
+            }
+        }
+    }
+    const bool qrow = ss ? (r < 64) : (r >= 64);
+    sm.rn[(qrow ? 0 : 64) + (r & 63)] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
+    return true;
+}
+
+// warps 4-7: chunk gq's gate prefix (warp 5, from its g / beta registers)
+// and per-row factors (its norms are in rn); `in` is this thread's verdict
+// so far.  Publishes e^{G_last} in the chunk's info entry for the consumer.
+__device__ __forceinline__ bool prep_fn(SmemWS& sm, float scale, int gq, bool in, int gt, float g0, float g1, float b0,
+                                     float b1) {
+    const int ss = gq & 1, warp = gt >> 5, lane = gt & 31;
+    SlotSmall& sl = sm.slot[ss];
+    (void)lane;
+    if (warp == 5) gate_prefix_fast(sm, sl, sm.ci[gq & 7], g0, g1, b0, b1);
+    if (!tc::bar_and(BAR_R, 128, in)) return false;
+    if (gt == 128) GDN_STAMP(gq - 1, 15);
+    const int f = gt - 128;
+    if (f < 64) {
+        const int i = f;
+        const float r = sm.rn[i], Gi = sm.G[i];
+        sm.rowA[i] = scale * r * __expf(Gi - sm.Gref[i >> 4]);
+        sl.qf[i] = scale * sm.eG[i] * r;
+    } else {
+        const int j = f - 64;
+        const float rk = sm.rn[64 + j], Gj = sm.G[j], bj = sl.beta[j];
+        sm.rowL[j] = bj * rk * __expf(Gj - sm.Gref[j >> 4]);
+        sl.fbg[j] = bj * sm.eG[j] * rk;
+        sl.fac[j] = sm.eGl[j] * rk;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) sm.colf[b][j] = (j < 16 * (b + 1)) ? rk * __expf(sm.Gref[b] - Gj) : 0.f;
+    }
+    tc::bar_sync(BAR_R, 128);  // every factor written: publish them with e^{G_last}
+    if (gt == 128) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&sm.ci[gq & 7].eg_ready) = gq;
+    }
+    return true;
+}
+
+// A job's initial state: its bf16 copy into the bf16 state columns (the A
+// operand of the first product), and the state scaled by e^{G_last} of the
+// job's first chunk (its update accumulates onto it) into the state columns.
+// Thread (row, half): S^T row `row`, keys [64 half, 64 half + 64).
+__device__ __forceinline__ void load_state_fn(const JobRec& J, float eg, uint32_t t_s, uint32_t t_sb, int row, int half) {
+    const float* ini = J.init;
+    const int64_t ild = J.init_ld;
+    const bool idi = J.identity_init != 0;
+    const int col0 = J.col0;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+        float v[16];
+        uint32_t w[8];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+            const int d = 64 * half + 16 * q4 + c2;
+            float s0 = 0.f;
+            if (idi) s0 = (d == col0 + row) ? 1.f : 0.f;
+            else if (ini) s0 = ini[(int64_t)d * ild + row];
+            v[c2] = s0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        tc::stw8(t_sb + 32 * half + 8 * q4, w);
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) v[c2] *= eg;
+        tc::st16(t_s + 64 * half + 16 * q4, v);
+    }
+}
+
+// the job's final state from the state columns (t_s includes the lane base)
+__device__ __forceinline__ void store_state_fn(const JobRec& J, uint32_t t_s, int row, int half) {
+    float* fin = J.fin;
+    const int64_t fld = J.fin_ld;
+    if (fin) {
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float v[16];
+            tc::ld16(t_s + 64 * half + 16 * q4, v);
+#pragma unroll
+            for (int c2 = 0; c2 < 16; ++c2) fin[(int64_t)(64 * half + 16 * q4 + c2) * fld + row] = v[c2];
+        }
+    }
+}
+
+// W of the chunk in slot ss from tensor memory (W^T: lane = key) into the
+// slot's K rows, free once K~ is copied and the W/U products have run: W
+// [token][key] K-major, the first product's B rows (t_w includes the lane base)
+__device__ __forceinline__ void w_readout_fn(SmemWS& sm, int ss, uint32_t t_w, int row, int half) {
+    const int d = row, wrow0 = ss ? 64 : 0;
+    const int dch = (d & 63) >> 3;
+#pragma unroll
+    for (int h16 = 0; h16 < 2; ++h16) {
+        float wv[16];
+        tc::ld16(t_w + 32 * half + 16 * h16, wv);
+        bf16* wb = sm.QK[ss] + (d >> 6) * 128 * 64 + (wrow0 + 32 * half + 16 * h16) * 64 + (d & 7);
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) wb[64 * c2 + ((dch ^ (c2 & 7)) << 3)] = __float2bfloat16_rn(wv[c2]);
+    }
+}
+
+// The consumer's 256 threads (c = gt): -Q~ = -diag(qf) Q in place and
+// K~ = diag(fac) K into the slot's K~ tile (same swizzled chunk positions),
+// 8 chunks each, loads first so that they overlap.  Needs the chunk's
+// factors (published with eg_ready) and its [rows] K^T read (aread).
+__device__ __forceinline__ void qk_prep_fn(SmemWS& sm, int gq, int c) {
+    const int ss = gq & 1;
+    const SlotSmall& sl = sm.slot[ss];
+    bf16* QKs = sm.QK[ss];
+    bf16* KTs = sm.KT[ss];
+    const int qrow0 = ss ? 0 : 64, krow0 = 64 - qrow0;
+    uint4 raw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // k < 4: Q rows, else K rows; chunk e = c + 256 (k & 3)
+        const int e = c + 256 * (k & 3), r = e >> 4, ch = e & 15;
+        raw[k] = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, (k >= 4 ? krow0 : qrow0) + r, ch)]);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int e = c + 256 * (k & 3), r = e >> 4, ch = e & 15;
+        const bool isk = k >= 4;
+        const float fs = isk ? sl.fac[r] : -sl.qf[r];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t2 = __bfloat1622float2(h[i]);
+            x[2 * i] = t2.x * fs;
+            x[2 * i + 1] = t2.y * fs;
+        }
+        bf16* dst = isk ? &KTs[tc::sw128_chunk(64, r, ch)] : &QKs[tc::sw128_chunk(128, qrow0 + r, ch)];
+        *reinterpret_cast<uint4*>(dst) = pack8(x);
+    }
+}
+
+// GNORM: the gated RMS norm output epilogue (the layer entry point); a
+// separate instantiation, so that the plain forward keeps its registers.
+template <bool GNORM>
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src,
                                                         const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -520,6 +731,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         if (!p.sched) lpt_block<NT>(p, src, sm.lpt_len, &sm.lpt_pick, bx, by, bz);
         if (tid == 0) {
             for (int i = 0; i < kRing; ++i) sm.ring[i].span = make_int2(-1, 0);
+            for (int i = 0; i < 8; ++i) sm.ci[i].eg_ready = sm.ci[i].aread = -1;
             sm.jn = sm.jdone = sm.chunks = sm.src_end = sm.abort = 0;
             sm.lpt_left = p.sched ? 0 : 1;
             sm.lpt_b[0] = bx;
@@ -545,17 +757,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::mbar_init(&sm.mbar_p, 1);
         tc::mbar_init(&sm.mbar_s, 1);
         tc::mbar_init(&sm.mbar_o, 1);
-        tc::mbar_init(&sm.mbar_q, 1);
         tc::mbar_init(&sm.full[0], 2);  // the W/U products' commit and a producer thread
         tc::mbar_init(&sm.full[1], 2);
         tc::mbar_init(&sm.wfree, 1);
-        tc::mbar_init(&sm.gfree, 1);
         tc::mbar_init(&sm.ld_qk[0], 1);
         tc::mbar_init(&sm.ld_qk[1], 1);
         tc::mbar_init(&sm.ld_v, 1);
         tc::mbar_init(&sm.fin_p, 1);
         tc::mbar_init(&sm.fin_s, 1);
         tc::mbar_init(&sm.fin_s2, 1);
+        tc::mbar_init(&sm.fin_g, 1);
         sm.qk_issued[0] = sm.qk_issued[1] = sm.qk_waited[0] = sm.qk_waited[1] = 0;
         sm.v_issued = sm.v_waited = 0;
     }
@@ -572,27 +783,24 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem_slot;
-    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_S = tmem + 384;
-    // per-slot columns are picked with selects (a runtime-indexed array would live in local memory)
-    const uint32_t T_VN0 = tmem + 128, T_VN1 = tmem + 192, T_O0 = tmem + 256, T_O1 = tmem + 320;
+    // tensor-memory columns: [Q;K] K^T | W^T | v_new (slot 0) | o | v_new (slot 1) | S^T bf16 | S^T fp32;
+    // the first product of slot 0 writes [v_new | o] = cols 128-255, of slot 1 [o | v_new] = 192-319
+    const uint32_t T_GRAM = tmem, T_W = tmem + 64, T_VN0 = tmem + 128, T_O = tmem + 192, T_VN1 = tmem + 256,
+                   T_SB = tmem + 320, T_S = tmem + 384;
     const uint32_t aQK0 = tc::smem_addr(sm.QK[0]), aKT0 = tc::smem_addr(sm.KT[0]), aA0 = tc::smem_addr(sm.A[0]);
-    const uint32_t aV = tc::smem_addr(sm.V), aS = tc::smem_addr(sm.S), aVN = tc::smem_addr(sm.VN);
-    const uint32_t aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
+    const uint32_t aV = tc::smem_addr(sm.V), aTb = tc::smem_addr(sm.Tb), aTbg = tc::smem_addr(sm.Tbg);
     bool ok = sm.acq_ok != 0;
     // base descriptors of slot 0; a K step or the other slot adds a constant
     // to the start-address field (slot 1 lies a fixed distance further on)
-    const uint64_t dQK0 = tc::desc(aQK0, 16, 1024);          // [Q;K] rows, Q~ rows
-    const uint64_t dK0 = tc::desc(aQK0 + 8192, 16, 1024);    // K rows
-    // K rows as the MN-major A operand of W^T (atoms 16 KB apart); W^T rows as
-    // the MN-major B operand of v_new (keys 0-63 in atom 0's K rows, 64-127 in atom 1's)
-    const uint64_t dKmn0 = tc::desc(aQK0 + 8192, 16384, 1024);
-    const uint64_t dKT0 = tc::desc(aKT0, 8192, 1024);
-    const uint64_t dA0 = tc::desc(aA0, 16, 1024);
-    const uint64_t dVmn = tc::desc(aV, 64 * 128, 1024), dS = tc::desc(aS, 16, 1024), dVN = tc::desc(aVN, 16, 1024);
-    const uint64_t dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
     constexpr uint64_t kQKslot = sizeof(bf16) * 128 * 128 / 16, kKTslot = sizeof(bf16) * 64 * 128 / 16,
-                       kAslot = sizeof(bf16) * 64 * 64 / 16;
-    auto wtoff = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 2048) >> 4); };
+                       kAslot = sizeof(bf16) * 64 * 64 / 16, kHalfRows = 64 * 128 / 16;
+    const uint64_t dQK0 = tc::desc(aQK0, 16, 1024);              // the slot's 128 rows, K-major
+    const uint64_t dKmn0 = tc::desc(aQK0, 128 * 128, 1024);      // K rows (slot 0: 0-63) as the MN-major A of W^T
+    const uint64_t dKT0 = tc::desc(aKT0, 64 * 128, 1024);        // K~ [token][key], MN-major B
+    const uint64_t dA0 = tc::desc(aA0, 16, 1024);
+    const uint64_t dVmn = tc::desc(aV, 64 * 128, 1024), dTb = tc::desc(aTb, 16, 1024), dTbg = tc::desc(aTbg, 16, 1024);
+    // K rows of slot ss: rows 0-63 in slot 0, 64-127 in slot 1 (Q rows the other half)
+    auto krows = [&](int ss) -> uint64_t { return ss ? kQKslot + kHalfRows : 0; };
 
     // The CTA's chunks form one stream over its jobs, indexed by gq; every
     // barrier phase and slot follows gq.  Chunk gq is in the stream once
@@ -600,38 +808,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
     // chunks ahead of the chunk it works on.
     auto stream_len = [&]() -> int { return *reinterpret_cast<volatile int*>(&sm.chunks); };
 
-    // Q/K of chunk gq into its slot: four 64x64 boxes (128-byte swizzle = the
-    // operand layout), Q into rows 0-63 and K into rows 64-127; one thread
-    auto issue_qk = [&](int gq, int tbn, int hk) {
-        const int ss = gq & 1;
-        bf16* qd = sm.QK[ss];
-        bf16* kd = sm.QK[ss] + 64 * 64;
-        uint64_t* bar = &sm.ld_qk[ss];
-        tc::mbar_expect_tx(bar, 4 * 64 * 64 * 2);
-        tc::tma_load_2d(qd, &maps.q, hk * 128, tbn, bar);
-        tc::tma_load_2d(qd + 128 * 64, &maps.q, hk * 128 + 64, tbn, bar);
-        tc::tma_load_2d(kd, &maps.k, hk * 128, tbn, bar);
-        tc::tma_load_2d(kd + 128 * 64, &maps.k, hk * 128 + 64, tbn, bar);
-        sm.qk_issued[ss] += 1;
-    };
-    // [Q;K] K^T of chunk gq once its Q/K have landed (one thread); true when
-    // the load arrived
+    auto issue_qk = [&](int gq, int tbn, int hk) { issue_qk_fn(sm, maps, p, gq, tbn, hk); };
     auto issue_gram = [&](int gq) -> bool {
         const int ss = gq & 1;
-        if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort)) return false;
-        sm.qk_waited[ss] += 1;
-        tc::fence_after();
-        const uint64_t so = ss ? kQKslot : 0, dA = dQK0 + so, dB = dK0 + so;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) tc::mma(T_GRAM, dA + tc::koff(128, kk), dB + tc::koff(128, kk), ID_N64, kk > 0);
-        tc::commit(&sm.mbar_p);
-        return true;
+        return issue_gram_fn(sm, T_GRAM, dQK0 + (ss ? kQKslot : 0), dQK0 + krows(ss), gq);
     };
 
     if (producer) {
         // ====================== producer warpgroups ======================
         const bool l2 = (p.flags & GDN_QK_L2NORM) != 0;
-        uint32_t ph = 0;  // phase of the [Q;K] K^T completions
+        uint32_t ph = 0;  // phase of the [rows] K^T completions
         int nvw = 0;      // thread 0: V loads waited for
         // g and beta of chunk gq into warp 5's registers (lane l: tokens 2l, 2l+1)
         float g_next0 = 0.f, g_next1 = 0.f, b_next0 = 0.f, b_next1 = 0.f;
@@ -646,94 +832,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (r1 < vn) gate_beta<bf16>(p, t1, hv, g_next1, b_next1);
             }
         };
-        auto issue_v = [&](int gq) {  // one thread
-            const ChunkInfo& I = sm.ci[gq & 7];
-            if (!I.vz) {
-                const int tbn = I.tb, hv = I.hv;
-                tc::mbar_expect_tx(&sm.ld_v, 2 * 64 * 64 * 2);
-                tc::tma_load_2d(sm.V, &maps.v, hv * 128, tbn, &sm.ld_v);
-                tc::tma_load_2d(sm.V + 64 * 64, &maps.v, hv * 128 + 64, tbn, &sm.ld_v);
-                sm.v_issued += 1;
-            }
-        };
-        // warps 4-7 (f = 0..127, one row each): the L2 norms of chunk gq's
-        // rows (rn[0-63] Q rows, rn[64-127] K rows)
-        auto norms = [&](int gq) -> bool {
-            const int ss = gq & 1;
-            if (!tc::mbar_wait(&sm.ld_qk[ss], (gq >> 1) & 1, kSpin, &sm.abort)) return false;
-            const int r = gt - 128;
-            float acc0 = 0.f, acc1 = 0.f;
-            if (l2) {
-                const bf16* QKn = sm.QK[ss];
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, ch)]);
-                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __bfloat1622float2(h2[i]);
-                        acc0 = fmaf(f.x, f.x, acc0);
-                        acc1 = fmaf(f.y, f.y, acc1);
-                    }
-                }
-            }
-            sm.rn[r] = l2 ? rsqrtf(acc0 + acc1 + 1e-6f) : 1.f;
-            return true;
-        };
-        // warps 4-7: chunk gq's gate prefix (warp 5) and per-row factors (its
-        // norms are in rn); `in` is this thread's verdict so far
+        auto issue_v = [&](int gq) { issue_v_fn(sm, maps, p, gq); };
+        auto norms = [&](int gq) -> bool { return norms_fn(sm, gq, gt, l2); };
         auto prep = [&](int gq, bool in) -> bool {
-            const int ss = gq & 1;
-            SlotSmall& sl = sm.slot[ss];
-            if (warp == 5) gate_prefix_fast(sm, sl, sm.ci[gq & 7], g_next0, g_next1, b_next0, b_next1);
-            if (!tc::bar_and(BAR_R, 128, in)) return false;
-            const int f = gt - 128;
-            if (f < 64) {
-                const int i = f;
-                const float r = sm.rn[i], Gi = sm.G[i];
-                sm.rowA[i] = p.scale * r * __expf(Gi - sm.Gref[i >> 4]);
-                sl.qf[i] = p.scale * sm.eG[i] * r;
-            } else {
-                const int j = f - 64;
-                const float rk = sm.rn[64 + j], Gj = sm.G[j], bj = sl.beta[j];
-                sm.rowL[j] = bj * rk * __expf(Gj - sm.Gref[j >> 4]);
-                sl.fbg[j] = bj * sm.eG[j] * rk;
-                sl.fac[j] = sm.eGl[j] * rk;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) sm.colf[b][j] = (j < 16 * (b + 1)) ? rk * __expf(sm.Gref[b] - Gj) : 0.f;
-            }
-            return true;
+            return prep_fn(sm, p.scale, gq, in, gt, g_next0, g_next1, b_next0, b_next1);
         };
-        // warps 4-7: Q~ = diag(qf) Q in place and K~ = diag(fac) K into the
-        // slot's K~ tile (same swizzled chunk positions), 16 chunks per thread
-        auto qk_prep = [&](int gq) {
-            const int ss = gq & 1;
-            const SlotSmall& sl = sm.slot[ss];
-            bf16* QKs = sm.QK[ss];
-            bf16* KTs = sm.KT[ss];
-            const int f = gt - 128;
-#pragma unroll 4
-            for (int k = 0; k < 16; ++k) {
-                const int e = f + 128 * (k & 7), r = e >> 4, ch = e & 15;
-                const bool isk = k >= 8;
-                const float fs = isk ? sl.fac[r] : sl.qf[r];
-                const uint4 raw = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, (isk ? 64 : 0) + r, ch)]);
-                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 t2 = __bfloat1622float2(h[i]);
-                    x[2 * i] = t2.x * fs;
-                    x[2 * i + 1] = t2.y * fs;
-                }
-                bf16* dst = isk ? &KTs[tc::sw128_chunk(64, r, ch)] : &QKs[tc::sw128_chunk(128, r, ch)];
-                *reinterpret_cast<uint4*>(dst) = pack8(x);
-            }
-        };
-        // A (Q rows, lanes 0-63) and L (K rows, lanes 64-127) from the Q K^T /
-        // K K^T blocks: this thread's lane, columns [32 hh, 32 hh + 32)
+        // A (Q rows) and L (K rows) from the [rows] K^T columns: this thread's
+        // lane, columns [32 hh, 32 hh + 32)
         auto al_readout = [&](int s, int hh) {
-            const bool isq = row < 64;
+            const bool isq = s ? (row < 64) : (row >= 64);
             const int i = row & 63;
             float gv[32];
             tc::ld32(T_GRAM + lb + 32 * hh, gv);
@@ -791,14 +898,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         for (int g = 0; g < len && ok; ++g) {
             const int s = g & 1;
             const bool vz = gt == 0 && sm.ci[g & 7].vz != 0;  // thread 0: no U product for this chunk
-            // ---- A: chunk g's [Q;K] K^T, then A and L (warps 1-7: warp w takes
+            // ---- A: chunk g's [rows] K^T, then A and L (warps 1-7: warp w takes
             // lane quarter w & 3 and column half w >> 2; a half with no kept
             // entry is skipped, and warp 4 takes warp 0's quarter); thread 0
             // meanwhile waits for the previous chunk's W and U, which must have
             // read Tb, Tbg and V before the inverse and the next V load rewrite them
             if (warp != 0) {
                 if (gt == 32) GDN_STAMP(g, 0);
-                bool a = pend && tc::mbar_wait(&sm.mbar_p, ph, kSpin, &sm.abort);
+                bool a = pend;
+                if (gt == 32) a = a && tc::mbar_wait(&sm.mbar_p, ph, kSpin, &sm.abort);
                 a = tc::bar_and(BAR_Q, GS - 32, a);
                 tc::fence_after();
                 if (gt == 32) GDN_STAMP(g, 1);
@@ -808,8 +916,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
                 tc::fence_before();
                 pend = tc::bar_and(BAR_Q, GS - 32, a);
-                if (gt == 32) GDN_STAMP(g, 2);
-                if (gt == 32 && pend) tc::mbar_arrive(&sm.gfree);
+                if (gt == 32) {
+                    GDN_STAMP(g, 2);
+                    *reinterpret_cast<volatile int*>(&sm.ci[g & 7].aread) = g;  // the Q rows may be scaled now
+                }
             } else if (gt == 0 && g >= 1) {
                 pend = pend && tc::mbar_wait(&sm.full[s ^ 1], ((g - 1) >> 1) & 1, kSpin, &sm.abort);
                 if (pend) issue_v(g);
@@ -821,8 +931,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::fence_after();
             if (gt == 0) GDN_STAMP(g, 3);
             // ---- B: the UT inverse (warps 0-3, straight into Tb and Tbg); warps
-            // 4-7: Q~ and K~ of this chunk, the next chunk's norms, gate prefix
-            // and factors, and (thread 128) the stream two chunks ahead
+            // 4-7: the next chunk's g / beta, and (thread 128) the stream two
+            // chunks ahead
             bool nok = true;
             if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.slot[s].beta, sm.slot[s].fbg, gt,
@@ -830,21 +940,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (gt == 0) GDN_STAMP(g, 4);
             } else {
                 if (g + 1 < len) load_gb(g + 1);
-                qk_prep(g);
-                if (gt == 128) GDN_STAMP(g, 5);
-                bool in = true;
-                if (g + 1 < len) {
-                    in = norms(g + 1);
-                    if (gt == 128) GDN_STAMP(g, 6);
-                    in = prep(g + 1, in);
-                    if (gt == 128) GDN_STAMP(g, 7);
-                }
-                nok = in;
                 if (gt == 128) {
+                    GDN_STAMP(g, 5);
                     // the job of chunk g + 2, taken no earlier than the pipeline needs
                     // it (the consumer loads that chunk's Q/K during chunk g; out of
                     // line, once per job), and that chunk's info
-                    if (!sm.src_end && sm.chunks < g + 3) nok = nok && acquire_jobs(p, src, sm, g + 3);
+                    if (!sm.src_end && sm.chunks < g + 3) nok = acquire_jobs(p, src, sm, g + 3);
                     if (g + 2 < sm.chunks) fill_chunk_info(sm, g + 2);
                 }
             }
@@ -853,7 +954,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             len = stream_len();
             if (gt == 0) GDN_STAMP(g, 8);
             // ---- C: thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed
-            // and the consumer has read the previous W
+            // and the consumer has read the previous W; warps 4-7 meanwhile: the
+            // next chunk's norms (once its Q/K land), gate prefix and factors
             if (gt == 0) {
                 bool w = true;
                 if (!vz) {
@@ -868,7 +970,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     const uint32_t T_U = s ? T_VN1 : T_VN0;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        tc::mma(T_W, dKmn0 + (s ? kQKslot : 0) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        tc::mma(T_W, dKmn0 + krows(s) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                         if (!vz) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
                     }
                     tc::commit(&sm.full[s]);
@@ -876,12 +978,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 }
                 GDN_STAMP(g, 10);
                 pend = w;
+            } else if (gt == 32 && g + 1 < len) {
+                // the next chunk's [rows] K^T once its Q/K have landed (this
+                // role has read this chunk's columns)
+                pend = issue_gram(g + 1);
+            } else if (gt >= 128 && g + 1 < len) {
+                bool in = norms(g + 1);
+                if (gt == 128) GDN_STAMP(g, 6);
+                pend = prep(g + 1, in);
+                if (gt == 128) GDN_STAMP(g, 7);
             }
         }
         if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
         if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
-        if (gt == 0 || gt == 224) {  // every product these threads issued has completed
-            uint64_t* fb = gt ? &sm.fin_s2 : &sm.fin_p;
+        if (gt == 0 || gt == 32 || gt == 224) {  // every product these threads issued has completed
+            uint64_t* fb = gt == 0 ? &sm.fin_p : (gt == 32 ? &sm.fin_g : &sm.fin_s2);
             tc::commit(fb);
             tc::mbar_wait(fb, 0, kSpin);
         }
@@ -890,7 +1001,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         bf16* __restrict__ o = static_cast<bf16*>(p.o);
         uint32_t ph = 0;  // phase of the chain products' completions
         auto wait_s = [&]() -> bool {
-            const bool done = tc::mbar_wait(&sm.mbar_s, ph, kSpin, &sm.abort);
+            bool done = true;
+            if (gt == 0) done = tc::mbar_wait(&sm.mbar_s, ph, kSpin, &sm.abort);
             ph ^= 1u;
             const bool all = tc::bar_and(BAR_S, GS, done);
             tc::fence_after();
@@ -898,125 +1010,71 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         };
         // The fp32 state lives in the state columns of tensor memory: thread
         // (row, half) holds S^T row `row` (value column), key columns
-        // [64 half, 64 half + 64), in 32-column pieces q2.
-        // A job's initial state: its bf16 copy (the A operand of the first
-        // product) into shared memory, and the state scaled by e^{G_last} of
-        // the job's first chunk (the first update accumulates onto it) into
-        // the state columns.
-        auto load_state = [&](const JobRec& J, float eg) {
-            const float* ini = J.init;
-            const int64_t ild = J.init_ld;
-            const bool idi = J.identity_init != 0;
-            const int col0 = J.col0;
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float v[32];
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) {
-                    const int d = 64 * half + 32 * q2 + c2;
-                    float s0 = 0.f;
-                    if (idi) s0 = (d == col0 + row) ? 1.f : 0.f;
-                    else if (ini) s0 = ini[(int64_t)d * ild + row];
-                    v[c2] = s0;
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 4 * q2 + c8)]) =
-                        pack8(&v[8 * c8]);
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) v[c2] *= eg;
-                tc::st32(T_S + lb + 64 * half + 32 * q2, v);
-            }
-            tc::wait_st();
-        };
-        auto store_state = [&](const JobRec& J) {  // the job's final state from the state columns
-            float* fin = J.fin;
-            const int64_t fld = J.fin_ld;
-            if (fin) {
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    float v[32];
-                    tc::ld32(T_S + lb + 64 * half + 32 * q2, v);
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) fin[(int64_t)(64 * half + 32 * q2 + c2) * fld + row] = v[c2];
-                }
-            }
-        };
-        // W^T of the chunk in slot ss from tensor memory into the slot's K
-        // rows (free once K~ is copied and the W/U products have run), as the
-        // MN-major [key][token] operand: this thread's key row, tokens
-        // [32 half, 32 half + 32), four 16-byte chunks
-        auto w_readout = [&](int ss) {
-            float wv[32];
-            tc::ld32(T_W + lb + 32 * half, wv);
-            unsigned char* base = reinterpret_cast<unsigned char*>(sm.QK[ss]) + (row >> 6) * 16384 + 8192 + (row & 63) * 128;
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                const int ch = 4 * half + c8;
-                *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = pack8(&wv[8 * c8]);
-            }
-        };
-        // The pending output of chunk og (slot og & 1), tensor memory -> global
-        // memory: thread (row, half) holds value column `row` of tokens
-        // [32 half, 32 half + 32); a warp's 32 lanes store 64 contiguous bytes
-        // of a token row at a time (no shared-memory staging).  With the gated
-        // norm (the wrappers' norm(o, z) on rows of head_v_dim) each token's
-        // sum of squares of its bf16 outputs is reduced over the 128 value
-        // lanes (warp butterfly, then the four lane quarters through shared
-        // memory) and the stores write norm_w * o / sqrt(mean(o^2) + eps) * silu(z).
-        const bool gnorm = p.z != nullptr;
-        auto write_output = [&](int og, int otb, int ovalid, int ohv) -> bool {
-            bool w = tc::mbar_wait(&sm.mbar_o, og & 1, kSpin, &sm.abort);
-            if (!tc::bar_and(BAR_S, GS, w)) return false;
-            tc::fence_after();
+        // [64 half, 64 half + 64).  Its bf16 copy, the A operand of the first
+        // product, sits in the bf16 state columns (two keys per column).
+        auto load_state = [&](const JobRec& J, float eg) { load_state_fn(J, eg, T_S + lb, T_SB + lb, row, half); };
+        auto store_state = [&](const JobRec& J) { store_state_fn(J, T_S + lb, row, half); };
+        auto w_readout = [&](int ss) { w_readout_fn(sm, ss, T_W + lb, row, half); };
+        // The output of a chunk, tensor memory -> global memory: thread (row,
+        // half) holds value column `row` of tokens [32 half, 32 half + 32); a
+        // warp's 32 lanes store 64 contiguous bytes of a token row at a time.
+        // With the gated norm (the wrappers' norm(o, z) on rows of head_v_dim)
+        // each token's sum of squares of its bf16 outputs is reduced over the
+        // 128 value lanes (warp butterfly, then the four lane quarters through
+        // shared memory) and the stores write norm_w * o / sqrt(mean(o^2) + eps) * silu(z).
+        constexpr bool gnorm = GNORM;
+        auto write_output = [&](int otb, int ovalid, int ohv) {
             float ov[32];
-            tc::ld32(((og & 1) ? T_O1 : T_O0) + lb + 32 * half, ov);
+            tc::ld32(T_O + lb + 32 * half, ov);
+            bf16* ot = sm.OST + (32 * half) * 128 + row;
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) ov[c2] = __bfloat162float(__float2bfloat16_rn(ov[c2]));
-            bf16* orow = o + ((int64_t)(otb + 32 * half) * p.Hv + ohv) * 128 + row;
-            const int64_t ost = (int64_t)p.Hv * 128;
-            const int nv = min(32, ovalid - 32 * half);  // valid tokens of this half
-            if (!gnorm) {
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2)
-                    if (c2 < nv) orow[c2 * ost] = __float2bfloat16_rn(ov[c2]);
-                return true;
+            for (int c2 = 0; c2 < 32; ++c2) {
+                const bf16 ob = __float2bfloat16_rn(ov[c2]);
+                ot[c2 * 128] = ob;
+                const float of = __bfloat162float(ob);
+                ov[c2] = of * of;
             }
-            float sq[32];
-#pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) sq[c2] = ov[c2] * ov[c2];
-            sm.ored[warp & 3][32 * half + lane] = reduce_scatter32(sq);
+            if constexpr (gnorm) sm.ored[warp & 3][32 * half + lane] = reduce_scatter32(ov);
             tc::bar_sync(BAR_S, GS);
-            const int tk = 32 * half + lane;  // this lane's token for the row factor
-            const float rl = rsqrtf((sm.ored[0][tk] + sm.ored[1][tk] + sm.ored[2][tk] + sm.ored[3][tk]) * (1.f / 128.f) +
-                                    p.norm_eps);
-            const float wv = __bfloat162float(static_cast<const bf16*>(p.norm_w)[row]);
-            const bf16* zrow = static_cast<const bf16*>(p.z) + (int64_t)(otb + 32 * half) * p.ldz + ohv * 128 + row;
+            for (int e = gt; e < 64 * 16; e += GS) {
+                const int t = e >> 4, ch = e & 15;
+                if (t < ovalid) {
+                    uint4 val = *reinterpret_cast<const uint4*>(sm.OST + t * 128 + 8 * ch);
+                    if constexpr (gnorm) {
+                        const float ss = sm.ored[0][t] + sm.ored[1][t] + sm.ored[2][t] + sm.ored[3][t];
+                        const float r = rsqrtf(ss * (1.f / 128.f) + p.norm_eps);
+                        const uint4 zr = __ldg(reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.z) +
+                                                                              (int64_t)(otb + t) * p.ldz + ohv * 128 + 8 * ch));
+                        const uint4 wr = __ldg(reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.norm_w) + 8 * ch));
+                        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+                        const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(&zr);
+                        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wr);
+                        float y[8];
 #pragma unroll
-            for (int c16 = 0; c16 < 2; ++c16) {
-                float zv[16];
-#pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2)
-                    zv[c2] = (16 * c16 + c2 < nv) ? __bfloat162float(zrow[(int64_t)(16 * c16 + c2) * p.ldz]) : 0.f;
-#pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2) {
-                    const int cc = 16 * c16 + c2;
-                    const float r = __shfl_sync(0xffffffffu, rl, cc);
-                    const float y = wv * (ov[cc] * r) * __fdividef(zv[c2], 1.f + __expf(-zv[c2]));
-                    if (cc < nv) orow[cc * ost] = __float2bfloat16_rn(y);
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 of = __bfloat1622float2(o2[i]), zf = __bfloat1622float2(z2[i]),
+                                         wf = __bfloat1622float2(w2[i]);
+                            y[2 * i] = wf.x * (of.x * r) * __fdividef(zf.x, 1.f + __expf(-zf.x));
+                            y[2 * i + 1] = wf.y * (of.y * r) * __fdividef(zf.y, 1.f + __expf(-zf.y));
+                        }
+                        val = pack8(y);
+                    }
+                    *reinterpret_cast<uint4*>(o + (int64_t)(otb + t) * p.ldo + (int64_t)ohv * p.hso + 8 * ch) = val;
                 }
             }
-            return true;
         };
+        tc::st32_zero(T_O + lb + 32 * half);  // the first product accumulates its o half onto zero
         if (stream_len() == 0 && ok) {  // a job without tokens: its final state is its initial state
             load_state(sm.ring[0], 1.f);
+            tc::wait_st();
             store_state(sm.ring[0]);
         }
+        tc::wait_st();
         tc::fence_before();
         tc::bar_sync(BAR_S, GS);
+        bool w_ready = false;  // W of chunk g is already in shared memory
+        bool o_pending = false;  // a chunk's output is still in the o columns
         int o_tb = 0, o_valid = 0, o_hv = 0, o_g = 0;
-        bool o_pending = false;
-        bool w_ready = false;  // W^T of chunk g is already in shared memory
         int g = 0;             // chunk of the stream
         int len = stream_len();  // chunks in the stream when last read (at least 2 ahead, or all)
         while (ok && g < len) {
@@ -1027,32 +1085,59 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             const bool write_o = J.write_o != 0;
             {
                 bool fl = true;
-                if (J.part == 2) fl = wait_flag(p.sched + kSchedHeader + J.flag, p.handover_ns, &sm.abort);
+                if (J.part == 2 && gt == 0) fl = wait_flag(p.sched + kSchedHeader + J.flag, p.handover_ns, &sm.abort);
                 if (!(ok = tc::bar_and(BAR_S, GS, fl))) break;
             }
             for (int c = 0; c < nchj && ok; ++c, ++g) {
                 const int s = g & 1;
-                bool qok = true;  // thread 0: the refill's wait for the first product
                 if (gt == 0) GDN_STAMP(g, 16);
-                // [Q;K] K^T of chunk g + 1 as soon as its Q/K are in and the producer
-                // has read chunk g's columns
-                bool gok = true;
-                if (gt == 0 && g + 1 < len) {
-                    gok = tc::mbar_wait(&sm.gfree, g & 1, kSpin, &sm.abort) && issue_gram(g + 1);
-                    GDN_STAMP(g, 17);
+                // the previous chunk's output (its products are done once the output
+                // barrier completes), then its columns back to zero: the first
+                // product accumulates its o half onto them.  This overlaps the wait
+                // for this chunk's operands.
+                if (o_pending) {
+                    bool wo = true;
+                    if (gt == 0) wo = tc::mbar_wait(&sm.mbar_o, o_g & 1, kSpin, &sm.abort);
+                    if (!(ok = tc::bar_and(BAR_S, GS, wo))) break;
+                    tc::fence_after();
+                    write_output(o_tb, o_valid, o_hv);
+                    o_pending = false;
                 }
-                // chunk g's operands: W/U products done, Q~ / K~ / A / factors written
-                if (!(ok = tc::bar_and(BAR_S, GS, gok && tc::mbar_wait(&sm.full[s], (g >> 1) & 1, kSpin, &sm.abort)))) break;
+                if (g > 0) tc::st32_zero(T_O + lb + 32 * half);
+                // -Q~ and K~ of this chunk, once the producer has published its
+                // factors and read its [rows] K^T columns (while the UT inverse
+                // runs), unless done during the previous chunk
+                if (!w_ready) {
+                    bool rd = true;
+                    if (gt == 0) {
+                        const volatile int* e1 = &sm.ci[g & 7].eg_ready;
+                        const volatile int* e2 = &sm.ci[g & 7].aread;
+                        for (uint32_t it = 0; it < kSpin && (*e1 != g || *e2 != g); ++it) {
+                            __nanosleep(32);  // yield the issue slots while waiting
+                            if ((it & 63) == 63 && *reinterpret_cast<volatile int*>(&sm.abort)) break;
+                        }
+                        rd = *e1 == g && *e2 == g;
+                    }
+                    if (!(ok = tc::bar_and(BAR_S, GS, rd))) break;
+                    qk_prep_fn(sm, g, gt);
+                }
+                if (gt == 0) GDN_STAMP(g, 17);
+                // chunk g's operands: W/U products done, -Q~ / K~ / A / factors written
+                bool gok = true;
+                if (gt == 0) gok = tc::mbar_wait(&sm.full[s], (g >> 1) & 1, kSpin, &sm.abort);
+                if (!(ok = tc::bar_and(BAR_S, GS, gok))) break;
                 tc::fence_after();
                 if (gt == 0) GDN_STAMP(g, 18);
                 len = stream_len();
                 const ChunkInfo& I = sm.ci[g & 7];
                 const int tb = I.tb, valid = I.valid;
-                const bool vz = I.vz != 0;
+                const uint32_t T_VNs = s ? T_VN1 : T_VN0;
                 if (c == 0) load_state(J, I.eglast);
-                const bool w_now = !w_ready;  // W^T not read during the previous chunk
+                if (I.vz) tc::st32_zero(T_VNs + lb + 32 * half);  // no U product: v_new = -W S alone
+                const bool w_now = !w_ready;  // W not read during the previous chunk
                 if (w_now) w_readout(s);
                 w_ready = false;
+                tc::wait_st();
                 tc::fence_async_smem();
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
@@ -1060,105 +1145,107 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     GDN_STAMP(g, 19);
                     if (w_now) tc::mbar_arrive(&sm.wfree);  // the W columns are free for the next W product
                     tc::fence_after();
-                    // v_new^T = U^T - S^T W^T (no U product: the first step overwrites)
-                    const uint32_t DV = s ? T_VN1 : T_VN0;
-                    const uint64_t dW = dKmn0 + (s ? kQKslot : 0);
+                    // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T (slot 0; slot 1 the
+                    // other row order), S^T bf16 from tensor memory
+                    const uint32_t D1 = s ? T_O : T_VN0;
+                    const uint64_t dB = dQK0 + (s ? kQKslot : 0);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma(DV, dS + tc::koff(128, kk), dW + wtoff(kk), ID_VNEW, (kk > 0 || !vz) ? 1u : 0u);
+                        tc::mma_ta(D1, T_SB + 8 * kk, dB + tc::koff(128, kk), ID_N128_NEG, 1u);
                     tc::commit(&sm.mbar_s);
-                    if (write_o) {  // o^T = S^T Q~^T
-                        const uint32_t DO = s ? T_O1 : T_O0;
-                        const uint64_t dQ = dQK0 + (s ? kQKslot : 0);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            tc::mma(DO, dS + tc::koff(128, kk), dQ + tc::koff(128, kk), ID_N64, kk > 0);
-                    }
-                    tc::commit(&sm.mbar_q);
                     GDN_STAMP(g, 20);
                 }
-                // while it runs: the previous chunk's output
-                if (o_pending) {
-                    if (!(ok = write_output(o_g, o_tb, o_valid, o_hv))) break;
-                    o_pending = false;
-                }
-                if (gt == 0) GDN_STAMP(g, 21);
                 if (!(ok = wait_s())) break;
                 if (gt == 0) GDN_STAMP(g, 22);
-                {  // v_new^T [value column][token] as the A operand of the updates
+                // the first product was the last reader of the slot's Q/K tile:
+                // refill it with the Q/K of chunk g + 2
+                if (gt == 0 && g + 2 < len) issue_qk(g + 2, sm.ci[(g + 2) & 7].tb, sm.ci[(g + 2) & 7].hk);
+                {  // v_new^T as bf16 pairs in place (this thread's own columns), the
+                   // A operand of the updates
                     float vv[32];
-                    tc::ld32((s ? T_VN1 : T_VN0) + lb + 32 * half, vv);
+                    tc::ld32(T_VNs + lb + 32 * half, vv);
+                    uint32_t w[16];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(&sm.VN[tc::sw128_chunk(128, row, 4 * half + c8)]) = pack8(&vv[8 * c8]);
+                    for (int j = 0; j < 16; ++j) w[j] = tc::pack_bf16x2(vv[2 * j], vv[2 * j + 1]);
+                    tc::stw16(T_VNs + lb + 32 * half, w);
+                    tc::wait_st();
                 }
-                tc::fence_async_smem();
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
                 if (gt == 0) {
                     GDN_STAMP(g, 23);
                     tc::fence_after();
-                    // S^T <- e^{G_last} S^T + v_new^T K~ (the scaled state is in place)
+                    // S^T <- e^{G_last} S^T + v_new^T K~ (the scaled state is in place);
+                    // K step kk of v_new: tokens [16 kk, 16 kk + 16) = columns of half kk / 2
                     const uint64_t dKT = dKT0 + (s ? kKTslot : 0);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) tc::mma(T_S, dVN + tc::koff(128, kk), dKT + tc::mnoff(kk), ID_N128_BMN, 1u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ta(T_S, T_VNs + 32 * (kk >> 1) + 8 * (kk & 1), dKT + tc::mnoff(kk), ID_N128_BMN, 1u);
                     tc::commit(&sm.mbar_s);
                     if (write_o) {  // o^T += v_new^T A^T
-                        const uint32_t DO = s ? T_O1 : T_O0;
                         const uint64_t dAs = dA0 + (s ? kAslot : 0);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) tc::mma(DO, dVN + tc::koff(128, kk), dAs + tc::koff(64, kk), ID_N64, 1u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_ta(T_O, T_VNs + 32 * (kk >> 1) + 8 * (kk & 1), dAs + tc::koff(64, kk), ID_N64, 1u);
                     }
                     tc::commit(&sm.mbar_o);
                     GDN_STAMP(g, 24);
-                    // the first product was the last reader of the slot's Q/K tile:
-                    // refill it with the Q/K of chunk g + 2
-                    if (g + 2 < len) {
-                        qok = tc::mbar_wait(&sm.mbar_q, g & 1, kSpin, &sm.abort);
-                        if (qok) issue_qk(g + 2, sm.ci[(g + 2) & 7].tb, sm.ci[(g + 2) & 7].hk);
-                    }
                 }
-                // while it runs: W^T of chunk g + 1, if its products are done
+                // while it runs: -Q~ / K~ and W of chunk g + 1, if its products are
+                // done (then its factors are published and its columns read; the
+                // K~ copy must precede the W readout, which overwrites the K rows)
                 if (g + 1 < len) {
                     bool rdy = true;
                     if (gt == 0) rdy = tc::mbar_test(&sm.full[s ^ 1], ((g + 1) >> 1) & 1);
                     if (tc::bar_and(BAR_S, GS, rdy)) {
                         tc::fence_after();
+                        qk_prep_fn(sm, g + 1, gt);
+                        tc::bar_sync(BAR_S, GS);
                         w_readout(s ^ 1);
                         w_ready = true;
                     }
                 }
+                // e^{G_last} of the next chunk of this job (its gate prefix runs on
+                // the producer, published in the chunk's info entry)
+                bool eok = true;
+                if (c + 1 < nchj && gt == 0) {
+                    const volatile int* rdy = &sm.ci[(g + 1) & 7].eg_ready;
+                    for (uint32_t it = 0; it < kSpin && *rdy != g + 1; ++it) {
+                        __nanosleep(32);
+                        if ((it & 63) == 63 && *reinterpret_cast<volatile int*>(&sm.abort)) break;
+                    }
+                    eok = *rdy == g + 1;
+                }
                 if (gt == 0) GDN_STAMP(g, 25);
                 tc::fence_before();
-                if (!(ok = wait_s() && tc::bar_and(BAR_S, GS, qok))) break;
+                if (!(ok = wait_s() && tc::bar_and(BAR_S, GS, eok))) break;
                 if (gt == 0 && w_ready) tc::mbar_arrive(&sm.wfree);  // every thread has read chunk g + 1's W
                 if (gt == 0) GDN_STAMP(g, 26);
                 if (c + 1 < nchj) {
                     // the new state: its bf16 copy, and the state scaled by the next
-                    // chunk's e^{G_last} back into tensor memory
-                    const float egn = sm.ci[(g + 1) & 7].eglast;
+                    // chunk's e^{G_last}, back into tensor memory (16-column pieces)
+                    const float egn = *reinterpret_cast<volatile float*>(&sm.ci[(g + 1) & 7].eglast);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {  // 16-column pieces (bounded register use)
+                    for (int q4 = 0; q4 < 4; ++q4) {
                         float sv[16];
+                        uint32_t w[8];
                         tc::ld16(T_S + lb + 64 * half + 16 * q4, sv);
 #pragma unroll
-                        for (int c8 = 0; c8 < 2; ++c8)
-                            *reinterpret_cast<uint4*>(&sm.S[tc::sw128_chunk(128, row, 8 * half + 2 * q4 + c8)]) =
-                                pack8(&sv[8 * c8]);
+                        for (int j = 0; j < 8; ++j) w[j] = tc::pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
+                        tc::stw8(T_SB + lb + 32 * half + 8 * q4, w);
 #pragma unroll
                         for (int c2 = 0; c2 < 16; ++c2) sv[c2] *= egn;
                         tc::st16(T_S + lb + 64 * half + 16 * q4, sv);
                     }
-                    tc::wait_st();
                 } else {
                     store_state(J);
                 }
+                o_pending = write_o;
                 o_tb = tb;
                 o_valid = valid;
                 o_hv = hvj;
                 o_g = g;
-                o_pending = write_o;
-                tc::fence_async_smem();
+                tc::wait_st();
                 tc::fence_before();
                 tc::bar_sync(BAR_S, GS);
                 if (gt == 0) GDN_STAMP(g, 27);
@@ -1173,7 +1260,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             tc::bar_sync(BAR_S, GS);
             if (gt == 0) *reinterpret_cast<volatile int*>(&sm.jdone) += 1;  // the job's ring entry is free
         }
-        if (ok && o_pending) ok = write_output(o_g, o_tb, o_valid, o_hv);  // the last chunk's output
+        if (ok && o_pending) {  // the last chunk's output
+            bool wo = true;
+            if (gt == 0) wo = tc::mbar_wait(&sm.mbar_o, o_g & 1, kSpin, &sm.abort);
+            if ((ok = tc::bar_and(BAR_S, GS, wo))) {
+                tc::fence_after();
+                write_output(o_tb, o_valid, o_hv);
+            }
+        }
         if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
         if (tid == GS) {  // every product this thread issued has completed
             tc::commit(&sm.fin_s);
@@ -1242,14 +1336,18 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
     p.handover_ns = g_handover_ns;
     p.no_publish = g_handover_publish ? 0 : 1;
     const size_t smem = sizeof(SmemWS) + 1024;
-    gdn_status st = set_smem_attr((const void*)chunk_tc_kernel, smem);
+    gdn_status st = set_smem_attr(p.z ? (const void*)chunk_tc_kernel<true> : (const void*)chunk_tc_kernel<false>, smem);
     if (st != GDN_OK) return st;
     TmaMaps maps;
     memset(&maps, 0, sizeof(maps));
-    if (p.T > 0) {
+    if (p.T > 0 && !p.head_major) {
         if ((st = make_map(&maps.q, p.q, p.ldq, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.k, p.k, p.ldk, (int64_t)p.Hk * 128, p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.v, p.v, p.ldv, (int64_t)p.Hv * 128, p.T)) != GDN_OK) return st;
+    } else if (p.T > 0) {  // dense head-major [H, T, 128]: [H*T rows x 128 columns]
+        if ((st = make_map(&maps.q, p.q, 128, 128, (int64_t)p.Hk * p.T)) != GDN_OK) return st;
+        if ((st = make_map(&maps.k, p.k, 128, 128, (int64_t)p.Hk * p.T)) != GDN_OK) return st;
+        if ((st = make_map(&maps.v, p.v, 128, 128, (int64_t)p.Hv * p.T)) != GDN_OK) return st;
     }
     if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the order kernel's scratch
     if (!p.status && p.sched) p.status = p.sched + 2;  // the work queue's status word
@@ -1269,7 +1367,8 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         const long long jobs = 2ll * p.sched_items * p.sched_m;
         grid = dim3((unsigned)(jobs < p.num_sms ? jobs : (p.num_sms > 0 ? p.num_sms : 1)), 1, 1);
     }
-    chunk_tc_kernel<<<grid, NT, smem, s>>>(p, src, maps);
+    if (p.z) chunk_tc_kernel<true><<<grid, NT, smem, s>>>(p, src, maps);
+    else chunk_tc_kernel<false><<<grid, NT, smem, s>>>(p, src, maps);
     return check_launch("chunk_tc_kernel");
 }
 

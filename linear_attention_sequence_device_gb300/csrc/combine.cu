@@ -7,65 +7,85 @@
 // a single sequence spans from an earlier shard into a later one, constant
 // (N only, M = 0) when the carried sequence starts inside the shard, and
 // none when the next shard starts a new sequence.
+#include "chunk_common.cuh"
 #include "gdn_internal.cuh"
 
 namespace gdn {
+gdn_status set_smem_attr(const void* func, size_t bytes);
 namespace {
 
 constexpr int NT = 256;
-constexpr int CT = 32;
+constexpr int CT = 32;  // state columns per CTA: one per lane
 
+// grid (Hv, dv / 32), 8 warps.  Lane = state column c0 + lane, warp w = rows
+// [DK/8 w, DK/8 (w + 1)).  Each shard's M (DK x DK fp32) is staged in shared
+// memory with cp.async, the next one in flight while the current is applied
+// (the loads are the only global traffic on the sequential path); reads of M
+// are broadcasts (one row element for the whole warp), reads of S are one
+// column per lane.
 template <int DK>
 __global__ void __launch_bounds__(NT) combine_kernel(const float* __restrict__ M,
                                                      const float* __restrict__ N,
                                                      const float* __restrict__ S0, int P, int Hv,
                                                      int dv, float* __restrict__ S_in,
                                                      const int32_t* __restrict__ plan) {
-    constexpr int dk = DK;
-    __shared__ float S[DK][CT + 1];
+    extern __shared__ __align__(16) float csm[];
+    float* Ms = csm;                // [2][DK * DK]
+    float* S = csm + 2 * DK * DK;   // [DK][CT]
     if (plan && plan[0] != 0) return;
+    constexpr int RPW = DK / 8;     // rows per warp
     const int h = blockIdx.x, c0 = blockIdx.y * CT;
-    const int tid = threadIdx.x;
-    constexpr int tpr = NT / DK;      // threads per state row
-    constexpr int cpt = CT / tpr;     // columns per thread
-    const int row = tid / tpr, cs = (tid % tpr) * cpt;
-    const int64_t hs = (int64_t)dk * dv;
-    for (int e = tid; e < dk * CT; e += NT) {
-        const int i = e / CT, c = e % CT;
-        S[i][c] = S0 ? S0[h * hs + (int64_t)i * dv + c0 + c] : 0.f;
-    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t hs = (int64_t)DK * dv;
+    // 2 = affine (M, N), 1 = constant (N only, M = 0), 0 = none
+    auto kind = [&](int r) -> int {
+        if (!plan) return 2;
+        const int32_t* rec = plan + GDN_PLAN_REC(r);
+        if (rec[GDN_PLAN_POST_NUM_RANKS] == 0) return 0;
+        return (rec[GDN_PLAN_LOCAL_NUM_SEQS] == 1 && !rec[GDN_PLAN_IS_FIRST_RANK]) ? 2 : 1;
+    };
+    auto stage = [&](int r) {  // M of shard r into buffer r & 1 (one cp.async group, maybe empty)
+        if (r < P - 1 && kind(r) == 2) {
+            const float* src = M + ((int64_t)r * Hv + h) * DK * DK;
+            float* dst = Ms + (r & 1) * DK * DK;
+            for (int e = tid; e < DK * DK / 4; e += NT) cp_async16(dst + 4 * e, src + 4 * e, 16);
+        }
+        cp_async_commit();
+    };
+    for (int i = warp; i < DK; i += 8) S[i * CT + lane] = S0 ? S0[h * hs + (int64_t)i * dv + c0 + lane] : 0.f;
+    stage(0);
     __syncthreads();
     for (int r = 0; r < P; ++r) {
         float* out = S_in + ((int64_t)r * Hv + h) * hs;
-        for (int e = tid; e < dk * CT; e += NT) {
-            const int i = e / CT, c = e % CT;
-            out[(int64_t)i * dv + c0 + c] = S[i][c];
-        }
+        for (int i = warp; i < DK; i += 8) out[(int64_t)i * dv + c0 + lane] = S[i * CT + lane];
         if (r == P - 1) break;
-        int kind = 2;  // 2 = affine, 1 = constant, 0 = none
-        if (plan) {
-            const int32_t* rec = plan + GDN_PLAN_REC(r);
-            if (rec[GDN_PLAN_POST_NUM_RANKS] == 0) kind = 0;
-            else if (rec[GDN_PLAN_LOCAL_NUM_SEQS] == 1 && !rec[GDN_PLAN_IS_FIRST_RANK]) kind = 2;
-            else kind = 1;
-        }
-        float acc[cpt];
-        const float* Nr = N + ((int64_t)r * Hv + h) * hs + (int64_t)row * dv + c0 + cs;
+        const int kd = kind(r);
+        stage(r + 1);  // the next shard's M streams in while this one is applied
+        float acc[RPW];
+        const float* Nr = N + ((int64_t)r * Hv + h) * hs + c0 + lane;
 #pragma unroll
-        for (int c = 0; c < cpt; ++c) acc[c] = (kind >= 1) ? Nr[c] : 0.f;
-        if (kind == 2) {
-            const float* Mr = M + ((int64_t)r * Hv + h) * dk * dk + (int64_t)row * dk;
-            for (int m = 0; m < dk; ++m) {
-                const float a = __ldg(Mr + m);
+        for (int j = 0; j < RPW; ++j) acc[j] = kd >= 1 ? Nr[(int64_t)(warp * RPW + j) * dv] : 0.f;
+        if (kd == 2) {
+            cp_async_wait<1>();  // this shard's M has landed
+            __syncthreads();
+            const float* Mr = Ms + (r & 1) * DK * DK + warp * RPW * DK;
+#pragma unroll 2
+            for (int m = 0; m < DK; m += 4) {
+                const float s0 = S[(m + 0) * CT + lane], s1 = S[(m + 1) * CT + lane];
+                const float s2 = S[(m + 2) * CT + lane], s3 = S[(m + 3) * CT + lane];
 #pragma unroll
-                for (int c = 0; c < cpt; ++c) acc[c] = fmaf(a, S[m][cs + c], acc[c]);
+                for (int j = 0; j < RPW; ++j) {
+                    const float4 mv = *reinterpret_cast<const float4*>(Mr + j * DK + m);
+                    acc[j] = fmaf(mv.x, s0, fmaf(mv.y, s1, fmaf(mv.z, s2, fmaf(mv.w, s3, acc[j]))));
+                }
             }
         }
-        __syncthreads();
+        __syncthreads();  // every warp is done reading S and this M
 #pragma unroll
-        for (int c = 0; c < cpt; ++c) S[row][cs + c] = acc[c];
+        for (int j = 0; j < RPW; ++j) S[(warp * RPW + j) * CT + lane] = acc[j];
         __syncthreads();
     }
+    cp_async_wait_all();
 }
 
 __global__ void empty_seq_final_kernel(const int32_t* __restrict__ cu, int Hv, int dk, int dv,
@@ -129,10 +149,20 @@ gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w,
 gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
                           int dv, float* S_in, const int32_t* plan, cudaStream_t s) {
     dim3 grid(Hv, dv / CT);
+    const size_t smem = sizeof(float) * (2 * (size_t)dk * dk + (size_t)dk * CT);
+    gdn_status st;
     switch (dk) {
-        case 32: combine_kernel<32><<<grid, NT, 0, s>>>(M, N, S0, P, Hv, dv, S_in, plan); break;
-        case 64: combine_kernel<64><<<grid, NT, 0, s>>>(M, N, S0, P, Hv, dv, S_in, plan); break;
-        case 128: combine_kernel<128><<<grid, NT, 0, s>>>(M, N, S0, P, Hv, dv, S_in, plan); break;
+        case 32:
+            combine_kernel<32><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            break;
+        case 64:
+            if ((st = set_smem_attr((const void*)combine_kernel<64>, smem)) != GDN_OK) return st;
+            combine_kernel<64><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            break;
+        case 128:
+            if ((st = set_smem_attr((const void*)combine_kernel<128>, smem)) != GDN_OK) return st;
+            combine_kernel<128><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            break;
         default: return fail(GDN_ERR_UNSUPPORTED_SHAPE, "dk=%d", dk);
     }
     return check_launch("combine_kernel");

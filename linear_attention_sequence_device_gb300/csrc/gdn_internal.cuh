@@ -106,6 +106,11 @@ struct ChunkParams {
     const void* a_raw;
     const float* A_log;
     const float* dt_bias;
+    // head strides (elements) of q, k, v and the token / head strides of o:
+    // token-major [T, H, d] has head stride d (o: token stride Hv*dv); the
+    // head-major [H, T, d] layout has head stride T*d (o: token stride dv)
+    int64_t hsq, hsk, hsv, ldo, hso;
+    int head_major;  // q/k/v/o are head-major (the tensor-core kernel's TMA views)
     // gated RMS norm of the output (z != null, tensor-core kernel only):
     // o <- norm_w * o / sqrt(mean(o^2) + norm_eps) * silu(z), z row stride ldz
     const void* z;
@@ -113,6 +118,16 @@ struct ChunkParams {
     const void* norm_w;
     float norm_eps;
 };
+
+// Token-major head strides (the layout every entry point but the head-major
+// one uses).
+inline void set_token_major(ChunkParams& p) {
+    p.hsq = p.hsk = p.dk;
+    p.hsv = p.dv;
+    p.ldo = (int64_t)p.Hv * p.dv;
+    p.hso = p.dv;
+    p.head_major = 0;
+}
 
 // g and beta of token t, value head hv (E = the input dtype).  With raw
 // projections, the wrappers' formulas ([HP-CP] P2P / all-gather forward):
@@ -347,6 +362,9 @@ gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, c
 // combine.cu: plan == null -> every shard affine
 gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
                           int dv, float* S_in, const int32_t* plan, cudaStream_t s);
+// layout.cu: [T, H, d] (token stride ld) <-> dense [H, T, d]
+gdn_status launch_relayout(const void* src, void* dst, int64_t T, int H, int d, int64_t ld, gdn_dtype dt,
+                           bool to_heads, cudaStream_t s);
 // gated RMS norm of o in place (combine.cu), for the kernels without the epilogue
 gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w, float eps, int64_t T, int Hv,
                              int dv, gdn_dtype dt, cudaStream_t s);

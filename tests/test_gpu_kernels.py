@@ -370,3 +370,44 @@ def test_zz_no_device_wait_expired():
     import linear_attention_sequence_device_gb300 as g
     torch.cuda.synchronize()
     assert g.binding.device_timeouts() == 0
+
+
+# ---------------------------------------------------------------------------
+# head-major layout (the Ulysses wrapper's per-rank view, on one device)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_relayout_round_trip_is_exact(dtype):
+    """[T, H, d] token-strided -> dense [H, T, d] -> back: bit-exact, and the
+    head-major tensor is the plain transpose."""
+    import linear_attention_sequence_device_gb300 as g
+    T, H, d, extra = 333, 5, 64, 24
+    x = W.fill(9, W.TID_X, H * d + extra, (0, T), (0, H * d + extra), dtype=W.DT_BF16 if dtype == "bf16" else W.DT_F32)
+    xd = to_dev(x, dtype)
+    xv = xd[:, :H * d].view(T, H, d)
+    y = g.binding.to_head_major(xv)
+    assert torch.equal(y, xv.permute(1, 0, 2).contiguous())
+    back = torch.zeros_like(xd)
+    g.binding.to_token_major(y, out=back[:, :H * d].view(T, H, d))
+    assert torch.equal(back[:, :H * d], xd[:, :H * d])
+    assert bool((back[:, H * d:] == 0).all())
+
+
+@pytest.mark.parametrize("case", [CHUNK_CASES[5], CHUNK_CASES[4], CHUNK_CASES[1], CHUNK_CASES[12]],
+                         ids=lambda c: f"{c[0]}-{c[3]}x{c[4]}")
+def test_chunk_fwd_heads_matches_token_major(case):
+    """The head-major chunked forward on transposed inputs gives the
+    token-major call's outputs bit for bit (same arithmetic), and both match
+    the oracle."""
+    import linear_attention_sequence_device_gb300 as g
+    w = make_chunk_workload(case)
+    host, d = chunk_inputs(w)
+    o_t, hf_t = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], h0=d["h0"])
+    qh, kh, vh = (g.binding.to_head_major(d[n]) for n in ("q", "k", "v"))
+    o_h, hf_h = g.binding.gdn_chunk_fwd_heads(qh, kh, vh, d["g"], d["beta"], d["cu"], h0=d["h0"])
+    o_back = g.binding.to_token_major(o_h)
+    assert torch.equal(o_back, o_t) and torch.equal(hf_h, hf_t)
+    o_ref, hf_ref = oracle.gdn_forward(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                                       host["h0"], w.cu_seqlens(), w.scale)
+    assert_close(f64(o_back), o_ref, w.dtype, "o")
+    assert_close(f64(hf_h), hf_ref, w.dtype, "h_final")
