@@ -126,6 +126,12 @@ gdn_status gdn_debug_set_phase_events(void *const *events, int32_t n);
  *   plan[GDN_PLAN_REC(r) + GDN_PLAN_*]       the fields below for shard r
  *   plan[GDN_PLAN_CU(num_seqs, n_shards, r) + i], 0 <= i <= local_num_seqs
  *                                            local cu_seqlens of shard r
+ *   plan[GDN_PLAN_SEQ(num_seqs, n_shards, r) + j], 0 <= j < local_num_seqs
+ *                                            global index of the sequence that
+ *                                            local segment j belongs to (the one
+ *                                            holding the segment's first token;
+ *                                            empty sequences, which the dedupe
+ *                                            of step 4 removes, own no segment)
  * Needs 1 <= n_shards <= 65536 and num_seqs >= 1.  The whole plan is
  * computed on the device: no device-to-host copy of cu_seqlens.
  * ---------------------------------------------------------------------- */
@@ -144,6 +150,8 @@ enum {
 #define GDN_PLAN_REC(r) (1 + (int64_t)(r) * GDN_PLAN_NFIELDS)
 #define GDN_PLAN_CU(num_seqs, n_shards, r) \
     (1 + (int64_t)(n_shards) * GDN_PLAN_NFIELDS + (int64_t)(r) * ((num_seqs) + 1))
+#define GDN_PLAN_SEQ(num_seqs, n_shards, r) \
+    (GDN_PLAN_CU(num_seqs, n_shards, n_shards) + (int64_t)(r) * ((num_seqs) + 1))
 
 int64_t gdn_cp_plan_words(int32_t num_seqs, int32_t n_shards);
 

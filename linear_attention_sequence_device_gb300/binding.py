@@ -171,7 +171,8 @@ def gdn_cp_plan(cu_seqlens: torch.Tensor, n_shards: int, out: torch.Tensor | Non
 
 
 def decode_plan(plan, num_seqs: int, n_shards: int):
-    """Host view of plan words: (status, [per-shard dict with local_cu])."""
+    """Host view of plan words: (status, [per-shard dict with local_cu and
+    local_seq, the global sequence of each local segment])."""
     w = plan.cpu().tolist() if isinstance(plan, torch.Tensor) else list(plan)
     recs = []
     base_cu = 1 + n_shards * len(PLAN_FIELDS)
@@ -179,6 +180,8 @@ def decode_plan(plan, num_seqs: int, n_shards: int):
         rec = dict(zip(PLAN_FIELDS, w[1 + r * len(PLAN_FIELDS):1 + (r + 1) * len(PLAN_FIELDS)]))
         off = base_cu + r * (num_seqs + 1)
         rec["local_cu"] = w[off:off + rec["local_num_seqs"] + 1]
+        soff = base_cu + (n_shards + r) * (num_seqs + 1)
+        rec["local_seq"] = w[soff:soff + rec["local_num_seqs"]]
         recs.append(rec)
     return w[0], recs
 

@@ -136,7 +136,7 @@ gdn_status gdn_device_timeouts(int32_t* count, int reset) {
 
 int64_t gdn_cp_plan_words(int32_t num_seqs, int32_t n_shards) {
     if (num_seqs < 1 || n_shards < 1) return 0;
-    return 1 + (int64_t)n_shards * GDN_PLAN_NFIELDS + (int64_t)n_shards * ((int64_t)num_seqs + 1);
+    return 1 + (int64_t)n_shards * GDN_PLAN_NFIELDS + 2 * (int64_t)n_shards * ((int64_t)num_seqs + 1);
 }
 
 gdn_status gdn_cp_plan(const int32_t* cu_seqlens, int32_t num_seqs, int32_t n_shards, int32_t* plan,

@@ -17,22 +17,31 @@
 // Only the two chain products and the tensor-memory <-> shared-memory moves
 // of v_new and S are serial from chunk to chunk; everything else works a
 // chunk ahead.  Operands sit in shared memory in the 128-byte-swizzled
-// canonical layouts: Q/K tiles and A K-major, K~ and W^T MN-major (K~ is a
-// row-scaled copy of the K rows; W^T is read out of tensor memory one key row
-// per thread), so no operand is ever transposed element by element.
+// canonical layouts: the Q/K tiles and A K-major, K~ MN-major (a row-scaled
+// copy of the K rows), and W K-major in the K rows of its Q/K tile once K~ is
+// copied (read out of tensor memory one key row per thread); v_new and the
+// bf16 state are A operands in tensor memory.  No operand is transposed
+// element by element.
 //
 // Two roles of two warpgroups each work on different chunks at once:
-//   producer (warps 0-7), chunk c+1 ahead of the consumer: A and L read from
-//     the [Q;K] K^T columns (warps 1-7); then the UT inverse on warps 0-3
-//     (tf32 mma.sync 16x16 blocks, written as the bf16 operands Tb and Tbg)
-//     while warps 4-7 scale Q to Q~ in place, copy K~, and take the next
-//     chunk's L2 norms, gate prefix and per-row factors; then thread 0 issues
-//     W and U (and issues V as soon as the previous chunk's U has read it);
-//   consumer (warps 8-15), chunk c: issues [Q;K] K^T of chunk c+1 as soon as
-//     the producer has read chunk c's columns, runs the chain, reads W^T of
-//     chunk c+1 out of tensor memory while its state update runs, writes the
-//     previous chunk's output while its first product runs, and refills the
-//     freed Q/K slot with chunk c+2 (TMA, 128-byte swizzle = operand layout).
+//   producer (warps 0-7), chunk g, a chunk ahead of the consumer:
+//     A) warps 1-7 read A and L out of chunk g's [rows] K^T columns; thread 0
+//        waits for chunk g-1's W/U products and issues chunk g's V load;
+//     B) warps 0-3 run the UT inverse (tf32 mma.sync 16x16 blocks, written as
+//        the bf16 operands Tb and Tbg); warps 4-7 load chunk g+1's g and beta
+//        and take jobs / fill chunk infos two chunks ahead;
+//     C) thread 0 issues W^T and U^T once V has landed and the consumer has
+//        read chunk g-1's W; thread 32 issues chunk g+1's [rows] K^T once its
+//        Q/K have landed; warps 4-7 take chunk g+1's L2 norms, gate prefix
+//        and per-row factors;
+//   consumer (warps 8-15), chunk g: writes the previous chunk's output
+//     (staged for 16-byte stores; the gated-norm epilogue in the layer
+//     instantiation), forms -Q~ in place and the K~ copy, moves W^T out of
+//     tensor memory into the K rows, issues the first product, refills the
+//     freed Q/K slot with chunk g+2 (TMA, 128-byte swizzle = operand layout),
+//     packs v_new to bf16 in place in tensor memory (the A operand of the
+//     second product), issues the second product, and while it runs forms
+//     chunk g+1's -Q~ / K~ and reads its W if that chunk's W/U are done.
 // The fp32 state stays in tensor memory: after each update it is read once
 // for its bf16 copy (the next chunk's A operand) and written back scaled by
 // the next chunk's e^{G_last}, onto which the next update accumulates.

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(NT) plan_kernel(const int32_t* __restrict__ cu
         const int s = count_le(cu + 1, N, rs);   // first sequence whose end > rs
         const int e = count_lt(cu, N, re);       // first sequence whose start >= re
         int32_t* lc = plan + GDN_PLAN_CU(N, P, r);
+        int32_t* sq = plan + GDN_PLAN_SEQ(N, P, r);
         int count = 0;
         for (int base = s; base <= e; base += 32) {
             const int i = base + lane;
@@ -66,7 +67,13 @@ __global__ void __launch_bounds__(NT) plan_kernel(const int32_t* __restrict__ cu
             }
             const bool keep = ok && (i == s || c != cp);
             const unsigned m = __ballot_sync(0xffffffffu, keep);
-            if (keep) lc[count + __popc(m & ((1u << lane) - 1u))] = c;
+            if (keep) {
+                // a kept boundary is the first of its value, so the segment
+                // that ends there belongs to the sequence just before it
+                const int pos = count + __popc(m & ((1u << lane) - 1u));
+                lc[pos] = c;
+                if (pos > 0) sq[pos - 1] = i - 1;
+            }
             count += __popc(m);
         }
         if (lane == 0) {

@@ -48,7 +48,7 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-            lib.orc_plan_shard.argtypes = [vp, i64, i64, i64, vp, vp]
+            lib.orc_plan_shard.argtypes = [vp, i64, i64, i64, vp, vp, vp]
             lib.orc_plan_shard.restype = i64
             lib.orc_conv_silu.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, i64, vp]
             lib.orc_conv_silu.restype = None
@@ -87,17 +87,19 @@ PLAN_FIELDS = ("start_seq_idx", "end_seq_idx", "pre_num_ranks", "post_num_ranks"
 
 
 def plan(cu_seqlens, n_shards: int):
-    """Per-shard plan records: a list of dicts with ``local_cu`` (int64 array)
-    and the fields of PLAN_FIELDS.  Requires total % n_shards == 0."""
+    """Per-shard plan records: a list of dicts with ``local_cu`` (int64 array),
+    ``local_seq`` (global sequence of each local segment) and the fields of
+    PLAN_FIELDS.  Requires total % n_shards == 0."""
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
     n = len(cu) - 1
     out = []
     for r in range(n_shards):
         loc = np.zeros(n + 1, dtype=np.int64)
         fields = np.zeros(8, dtype=np.int64)
+        seq = np.zeros(n + 1, dtype=np.int64)
         m = _load().orc_plan_shard(cu.ctypes.data, n, n_shards, r, loc.ctypes.data,
-                                   fields.ctypes.data)
-        rec = {"local_cu": loc[:m].copy()}
+                                   fields.ctypes.data, seq.ctypes.data)
+        rec = {"local_cu": loc[:m].copy(), "local_seq": seq[:max(m - 1, 0)].copy()}
         rec.update({f: int(fields[i]) for i, f in enumerate(PLAN_FIELDS)})
         out.append(rec)
     return out

@@ -54,7 +54,7 @@ static int64_t ss_left(const int64_t *a, int64_t n, int64_t x) {
  * Assumes cu is non-decreasing, cu[0] = 0 and total % world == 0.
  */
 int64_t orc_plan_shard(const int64_t *cu, int64_t n_seqs, int64_t world, int64_t rank,
-                       int64_t *local_cu, int64_t *fields) {
+                       int64_t *local_cu, int64_t *fields, int64_t *local_seq) {
     /* step 2: total tokens and this rank's range */
     int64_t total = cu[n_seqs];
     int64_t part_len = total / world;
@@ -87,6 +87,10 @@ int64_t orc_plan_shard(const int64_t *cu, int64_t n_seqs, int64_t world, int64_t
     fields[5] = (rank == last_rank_of_last_seq);
     fields[6] = pre_conv;
     fields[7] = part_len;
+    /* the global sequence of each local segment: the one that holds the
+       segment's first token (largest i with cu[i] <= that token) */
+    for (int64_t j = 0; j + 1 < n_local; ++j)
+        local_seq[j] = ss_right(cu + 1, n_seqs, rank_start + local_cu[j]);
     return n_local;
 }
 

@@ -40,7 +40,7 @@ def test_status_strings(lib):
 
 
 def test_plan_words(lib):
-    assert lib.gdn_cp_plan_words(3, 2) == 1 + 2 * 9 + 2 * 4
+    assert lib.gdn_cp_plan_words(3, 2) == 1 + 2 * 9 + 2 * 2 * 4  # records, local cu, local sequence map
     assert lib.gdn_cp_plan_words(0, 2) == 0
 
 

@@ -42,6 +42,7 @@ def compare_plan(cu, P):
     off = 0
     for r, (a, b) in enumerate(zip(recs, exp)):
         assert a["local_cu"] == b["local_cu"].tolist(), r
+        assert a["local_seq"] == b["local_seq"].tolist(), r
         for f in ("start_seq_idx", "end_seq_idx", "pre_num_ranks", "post_num_ranks",
                   "is_first_rank", "is_last_rank", "pre_num_conv_tokens"):
             assert a[f] == b[f], (r, f, a[f], b[f])

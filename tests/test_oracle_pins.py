@@ -54,10 +54,11 @@ def brute_plan(cu, P):
     for r in range(P):
         rs, re = r * part, (r + 1) * part
         local = [0] + [t - rs for t in range(rs + 1, re) if sid[t] != sid[t - 1]] + [part]
+        seqs = [int(sid[rs + b]) for b in local[:-1]]  # owner sequence of each segment's first token
         first_seq, last_seq = sid[rs], sid[re - 1]
         first_tok = np.flatnonzero(sid == first_seq)[0]
         last_tok = np.flatnonzero(sid == last_seq)[-1]
-        out.append(dict(local_cu=local,
+        out.append(dict(local_cu=local, local_seq=seqs,
                         start_seq_idx=int(first_seq),
                         pre_num_conv_tokens=int(np.sum(sid[:rs] == first_seq)),
                         pre_num_ranks=int(r - owner[first_tok]),
@@ -80,6 +81,7 @@ def test_plan_brute_force(trial):
     exp = brute_plan(cu, P)
     for a, b in zip(got, exp):
         assert a["local_cu"].tolist() == b["local_cu"]
+        assert a["local_seq"].tolist() == b["local_seq"]
         for f in ("start_seq_idx", "pre_num_conv_tokens", "pre_num_ranks", "post_num_ranks",
                   "is_first_rank", "is_last_rank"):
             assert a[f] == b[f], f
