@@ -11,7 +11,10 @@ Sources: flash-linear-attention ``fla/ops/cp/context.py``
 (``get_cp_cu_seqlens``, steps 1-5) for the shard plan; hyper-parallel
 ``linear_attention_context_parallel.py`` (``_causal_conv1d_with_cp_halo``,
 ``_l2norm_torch``, the chunked gated delta rule, the state summary and the
-prefix merge) for everything else.
+prefix merge) for everything else; the backward (``gdn_backward``) is the
+reverse-mode gradient of the token recurrence, whose state gradient flows
+the way the page's ``_RecvInitialStateP2PFunction`` /
+``_SendFinalStateP2PFunction`` send it back.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 brute force, closed forms, library routines or an independent restatement.
@@ -64,6 +67,9 @@ def _load():
             lib.orc_gates.restype = None
             lib.orc_gated_rmsnorm.argtypes = [vp, vp, vp, dbl, i64, i64, vp]
             lib.orc_gated_rmsnorm.restype = None
+            lib.orc_gdn_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                             dbl, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.orc_gdn_backward.restype = None
             lib.orc_max_threads.argtypes = []
             lib.orc_max_threads.restype = i32
             _lib = lib
@@ -136,6 +142,25 @@ def gdn_forward(q, k, v, g, beta, h0, cu_seqlens, scale, l2norm=False, want_o=Tr
                             beta.ctypes.data, _ptr(h0), cu.ctypes.data, n, Hk, Hv, K, V,
                             float(scale), int(bool(l2norm)), _ptr(o), hf.ctypes.data)
     return o, hf
+
+
+def gdn_backward(q, k, v, g, beta, h0, cu_seqlens, scale, dout, dh_final=None, l2norm=False):
+    """Gradients of the token recurrence (gdn_forward) for the loss gradients
+    dout [T, Hv, V] and dh_final [N, Hv, K, V] (or None): a dict with dq, dk
+    [T, Hk, K] (summed over the value heads of each q/k head), dv [T, Hv, V],
+    dg, dbeta [T, Hv] and dh0 [N, Hv, K, V]."""
+    q, k, v, g, beta, h0, dout, dh_final = map(_f64, (q, k, v, g, beta, h0, dout, dh_final))
+    T, Hk, K = k.shape
+    Hv, V = v.shape[1], v.shape[2]
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    n = len(cu) - 1
+    out = dict(dq=np.empty((T, Hk, K)), dk=np.empty((T, Hk, K)), dv=np.empty((T, Hv, V)),
+               dg=np.empty((T, Hv)), dbeta=np.empty((T, Hv)), dh0=np.empty((n, Hv, K, V)))
+    _load().orc_gdn_backward(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                             beta.ctypes.data, _ptr(h0), cu.ctypes.data, n, Hk, Hv, K, V,
+                             float(scale), int(bool(l2norm)), dout.ctypes.data, _ptr(dh_final),
+                             *(out[x].ctypes.data for x in ("dq", "dk", "dv", "dg", "dbeta", "dh0")))
+    return out
 
 
 def gdn_summary(k, v, g, beta, cu_seqlens, l2norm=False):

@@ -17,7 +17,10 @@
  *             exact for the token recurrence below),
  *             _compute_gdn_state_summary_from_prepared (state_out =
  *             M @ state_in + S) and _merge_gdn_prefix_state_summaries_torch
- *             (the prefix merge over shards).
+ *             (the prefix merge over shards); the backward of the token
+ *             recurrence (reverse mode, the state gradient flowing back the
+ *             way _RecvInitialStateP2PFunction / _SendFinalStateP2PFunction
+ *             send it).
  *
  * Layouts (all dense, row-major, fp64 unless stated):
  *   q, k [T, Hk, K]; v [T, Hv, V]; g, beta [T, Hv]; o [T, Hv, V]
@@ -321,6 +324,177 @@ void orc_gated_rmsnorm(const double *o, const double *z, const double *w, double
         for (int64_t d = 0; d < D; ++d) {
             const double zz = z[r * D + d];
             y[r * D + d] = w[d] * (o[r * D + d] * inv) * (zz / (1.0 + exp(-zz)));
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward of the token recurrence of orc_gdn_forward (reverse mode)        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Given the loss gradients dout [T, Hv, V] (w.r.t. o) and dh_final
+ * [N, Hv, K, V] (w.r.t. the final states, or NULL), the gradients w.r.t.
+ * q, k [T, Hk, K] (summed over the value heads that share a q/k head),
+ * v [T, Hv, V], g, beta [T, Hv] and h0 [N, Hv, K, V].  Per token, with
+ * a = e^g, P = a S_prev, u = v - P^T k, S = P + beta k u^T, o = S^T (scale q),
+ * walked backwards with the state gradient dS:
+ *   dq = scale S do;               dS += scale q do^T
+ *   dbeta = k . (dS u);            dk = beta dS u;    du = beta dS^T k;  dv = du
+ *   dP = dS - k du^T;              dk -= P du;        dg = <P, dP>;      dS_prev = a dP
+ * (q, k here are the normalised vectors when l2 is set; their gradients are
+ * carried back through x / sqrt(|x|^2 + 1e-6) at the end.)  The states before
+ * each token are recomputed chunk by chunk (64 tokens) from states kept at
+ * the chunk starts.
+ */
+static void l2norm_back(const double *x, const double *dxn, double *dx, int64_t K) {
+    double ss = 0.0, xd = 0.0;
+    for (int64_t i = 0; i < K; ++i) { ss += x[i] * x[i]; xd += x[i] * dxn[i]; }
+    const double r = 1.0 / sqrt(ss + 1e-6);
+    for (int64_t i = 0; i < K; ++i) dx[i] = r * dxn[i] - r * r * r * xd * x[i];
+}
+
+void orc_gdn_backward(const double *q, const double *k, const double *v,
+                      const double *g, const double *beta, const double *h0,
+                      const int64_t *cu, int64_t n_seqs, int64_t Hk, int64_t Hv,
+                      int64_t K, int64_t V, double scale, int l2,
+                      const double *dout, const double *dh_final,
+                      double *dq, double *dk, double *dv, double *dg, double *dbeta, double *dh0) {
+    const int64_t G = Hv / Hk, C = 64;
+    const int64_t T = cu[n_seqs];
+    memset(dq, 0, sizeof(double) * T * Hk * K);
+    memset(dk, 0, sizeof(double) * T * Hk * K);
+    /* a q/k head's gradient collects its G value heads: one task per (n, hk) */
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int64_t n = 0; n < n_seqs; ++n) {
+        for (int64_t hk = 0; hk < Hk; ++hk) {
+            const int64_t t0 = cu[n], L = cu[n + 1] - cu[n];
+            const int64_t nch = (L + C - 1) / C;
+            double *chk = (double *)malloc(sizeof(double) * K * V * (nch > 0 ? nch : 1));
+            double *Sp = (double *)malloc(sizeof(double) * K * V * C);   /* states before each token of a chunk */
+            double *S = (double *)malloc(sizeof(double) * K * V);
+            double *dS = (double *)malloc(sizeof(double) * K * V);
+            double *kn = (double *)malloc(sizeof(double) * K * (L > 0 ? L : 1));
+            double *qn = (double *)malloc(sizeof(double) * K * (L > 0 ? L : 1));
+            double *u = (double *)malloc(sizeof(double) * V);
+            double *du = (double *)malloc(sizeof(double) * V);
+            double *w1 = (double *)malloc(sizeof(double) * K);
+            double *w2 = (double *)malloc(sizeof(double) * K);
+            double *dqn = (double *)calloc((size_t)K * (L > 0 ? L : 1), sizeof(double));
+            double *dkn = (double *)calloc((size_t)K * (L > 0 ? L : 1), sizeof(double));
+            for (int64_t j = 0; j < L; ++j) {
+                const double *kr = k + ((t0 + j) * Hk + hk) * K, *qr = q + ((t0 + j) * Hk + hk) * K;
+                if (l2) { l2norm(kr, kn + j * K, K); l2norm(qr, qn + j * K, K); }
+                else { memcpy(kn + j * K, kr, sizeof(double) * K); memcpy(qn + j * K, qr, sizeof(double) * K); }
+            }
+            for (int64_t h = hk * G; h < (hk + 1) * G; ++h) {
+                /* forward: the state at every chunk start */
+                if (h0) memcpy(S, h0 + ((n * Hv + h) * K) * V, sizeof(double) * K * V);
+                else memset(S, 0, sizeof(double) * K * V);
+                for (int64_t j = 0; j < L; ++j) {
+                    if (j % C == 0) memcpy(chk + (j / C) * K * V, S, sizeof(double) * K * V);
+                    const int64_t t = t0 + j;
+                    const double a = exp(g[t * Hv + h]), b = beta[t * Hv + h];
+                    const double *kt = kn + j * K, *vr = v + (t * Hv + h) * V;
+                    for (int64_t i = 0; i < K * V; ++i) S[i] *= a;
+                    for (int64_t c = 0; c < V; ++c) {
+                        double s = vr[c];
+                        for (int64_t i = 0; i < K; ++i) s -= S[i * V + c] * kt[i];
+                        u[c] = s;
+                    }
+                    for (int64_t i = 0; i < K; ++i)
+                        for (int64_t c = 0; c < V; ++c) S[i * V + c] += b * kt[i] * u[c];
+                }
+                /* backward, chunk by chunk from the last */
+                if (dh_final) memcpy(dS, dh_final + ((n * Hv + h) * K) * V, sizeof(double) * K * V);
+                else memset(dS, 0, sizeof(double) * K * V);
+                for (int64_t ch = nch - 1; ch >= 0; --ch) {
+                    const int64_t j0 = ch * C, j1 = (j0 + C < L) ? j0 + C : L;
+                    memcpy(S, chk + ch * K * V, sizeof(double) * K * V);
+                    for (int64_t j = j0; j < j1; ++j) {   /* recompute the states before each token */
+                        memcpy(Sp + (j - j0) * K * V, S, sizeof(double) * K * V);
+                        const int64_t t = t0 + j;
+                        const double a = exp(g[t * Hv + h]), b = beta[t * Hv + h];
+                        const double *kt = kn + j * K, *vr = v + (t * Hv + h) * V;
+                        for (int64_t i = 0; i < K * V; ++i) S[i] *= a;
+                        for (int64_t c = 0; c < V; ++c) {
+                            double s = vr[c];
+                            for (int64_t i = 0; i < K; ++i) s -= S[i * V + c] * kt[i];
+                            u[c] = s;
+                        }
+                        for (int64_t i = 0; i < K; ++i)
+                            for (int64_t c = 0; c < V; ++c) S[i * V + c] += b * kt[i] * u[c];
+                    }
+                    for (int64_t j = j1 - 1; j >= j0; --j) {
+                        const int64_t t = t0 + j;
+                        const double a = exp(g[t * Hv + h]), b = beta[t * Hv + h];
+                        const double *kt = kn + j * K, *qt = qn + j * K, *vr = v + (t * Hv + h) * V;
+                        const double *dor = dout + (t * Hv + h) * V;
+                        const double *Sprev = Sp + (j - j0) * K * V;
+                        /* u from P = a S_prev */
+                        for (int64_t c = 0; c < V; ++c) {
+                            double s = vr[c];
+                            for (int64_t i = 0; i < K; ++i) s -= a * Sprev[i * V + c] * kt[i];
+                            u[c] = s;
+                        }
+                        /* dq = scale S do with S = P + beta k u^T */
+                        double udo = 0.0;
+                        for (int64_t c = 0; c < V; ++c) udo += u[c] * dor[c];
+                        for (int64_t i = 0; i < K; ++i) {
+                            double s = 0.0;
+                            for (int64_t c = 0; c < V; ++c) s += a * Sprev[i * V + c] * dor[c];
+                            dqn[j * K + i] += scale * (s + b * kt[i] * udo);
+                        }
+                        /* the output's contribution to the state gradient */
+                        for (int64_t i = 0; i < K; ++i)
+                            for (int64_t c = 0; c < V; ++c) dS[i * V + c] += scale * qt[i] * dor[c];
+                        /* through S = P + beta k u^T */
+                        double db = 0.0;
+                        for (int64_t i = 0; i < K; ++i) {
+                            double s = 0.0;
+                            for (int64_t c = 0; c < V; ++c) s += dS[i * V + c] * u[c];
+                            w1[i] = s;                      /* dS u */
+                            db += kt[i] * s;
+                        }
+                        for (int64_t c = 0; c < V; ++c) {
+                            double s = 0.0;
+                            for (int64_t i = 0; i < K; ++i) s += dS[i * V + c] * kt[i];
+                            du[c] = b * s;                  /* beta dS^T k */
+                        }
+                        dbeta[t * Hv + h] = db;
+                        for (int64_t c = 0; c < V; ++c) dv[(t * Hv + h) * V + c] = du[c];
+                        /* through u = v - P^T k: dP = dS - k du^T, dk -= P du */
+                        for (int64_t i = 0; i < K; ++i) {
+                            double s = 0.0;
+                            for (int64_t c = 0; c < V; ++c) s += a * Sprev[i * V + c] * du[c];
+                            w2[i] = s;
+                        }
+                        for (int64_t i = 0; i < K; ++i) dkn[j * K + i] += b * w1[i] - w2[i];
+                        for (int64_t i = 0; i < K; ++i)
+                            for (int64_t c = 0; c < V; ++c) dS[i * V + c] -= kt[i] * du[c];
+                        /* through P = a S_prev */
+                        double pd = 0.0;
+                        for (int64_t i = 0; i < K * V; ++i) pd += a * Sprev[i] * dS[i];
+                        dg[t * Hv + h] = pd;
+                        for (int64_t i = 0; i < K * V; ++i) dS[i] *= a;
+                    }
+                }
+                if (dh0) memcpy(dh0 + ((n * Hv + h) * K) * V, dS, sizeof(double) * K * V);
+            }
+            /* q/k gradients of the stored (un-normalised) vectors */
+            for (int64_t j = 0; j < L; ++j) {
+                const int64_t t = t0 + j;
+                double *dqo = dq + (t * Hk + hk) * K, *dko = dk + (t * Hk + hk) * K;
+                if (l2) {
+                    l2norm_back(q + (t * Hk + hk) * K, dqn + j * K, dqo, K);
+                    l2norm_back(k + (t * Hk + hk) * K, dkn + j * K, dko, K);
+                } else {
+                    memcpy(dqo, dqn + j * K, sizeof(double) * K);
+                    memcpy(dko, dkn + j * K, sizeof(double) * K);
+                }
+            }
+            free(chk); free(Sp); free(S); free(dS); free(kn); free(qn); free(u); free(du);
+            free(w1); free(w2); free(dqn); free(dkn);
         }
     }
 }

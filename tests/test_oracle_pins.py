@@ -419,3 +419,86 @@ def test_gated_rmsnorm_closed_forms():
                                rtol=1e-13)
     y = oracle.gated_rmsnorm(np.full((2, 64), 2.5), z[:2], np.ones(64), 0.0)
     np.testing.assert_allclose(y, z[:2] / (1.0 + np.exp(-z[:2])), rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# backward of the token recurrence
+# ---------------------------------------------------------------------------
+
+def _bwd_problem(seed, T_lens, Hk, Hv, K, V, h0=True):
+    r = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(T_lens)]).astype(np.int64)
+    T, N = int(cu[-1]), len(T_lens)
+    q = r.normal(size=(T, Hk, K))
+    k = r.normal(size=(T, Hk, K))
+    v = r.normal(size=(T, Hv, V))
+    g = -np.log1p(np.exp(r.normal(size=(T, Hv)) - 1.0))
+    b = 1.0 / (1.0 + np.exp(-r.normal(size=(T, Hv))))
+    h0 = r.normal(size=(N, Hv, K, V)) * 0.5 if h0 else None
+    Wo = r.normal(size=(T, Hv, V))
+    Wh = r.normal(size=(N, Hv, K, V))
+    return cu, q, k, v, g, b, h0, Wo, Wh
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_backward_vs_finite_differences(l2):
+    """Every gradient against central differences of the oracle's forward
+    for the loss sum(o * Wo) + sum(h_final * Wh): GQA (two value heads per
+    q/k head), a 70-token sequence (two checkpointed chunks), an empty
+    sequence and a short one, nonzero h0."""
+    cu, q, k, v, g, b, h0, Wo, Wh = _bwd_problem(5, [70, 0, 9], 1, 2, 3, 2)
+    scale = 0.7
+
+    def loss(**a):
+        o, hf = oracle.gdn_forward(a["q"], a["k"], a["v"], a["g"], a["b"], a["h0"], cu, scale,
+                                   l2norm=l2)
+        return float((o * Wo).sum() + (hf * Wh).sum())
+
+    args = dict(q=q, k=k, v=v, g=g, b=b, h0=h0)
+    got = oracle.gdn_backward(q, k, v, g, b, h0, cu, scale, Wo, Wh, l2norm=l2)
+    names = dict(q="dq", k="dk", v="dv", g="dg", b="dbeta", h0="dh0")
+    eps = 1e-6
+    for nm, x in args.items():
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            fd[idx] = (loss(**{**args, nm: xp}) - loss(**{**args, nm: xm})) / (2 * eps)
+        err = np.abs(fd - got[names[nm]]).max() / np.abs(fd).max()
+        assert err < 1e-6, (nm, err)
+
+
+def test_backward_closed_form_without_updates():
+    """beta = 0: the state only decays, o_t = e^{G_t} S0^T (scale q_t), so
+    dv = dk = 0, dh0 = sum_t e^{G_t} scale q_t do_t^T + e^{G_T} dh_final,
+    dq_t = scale e^{G_t} S0 do_t and dbeta_t = k_t . (dS_t u_t)."""
+    cu, q, k, v, g, b, h0, Wo, Wh = _bwd_problem(6, [23], 1, 1, 4, 3)
+    b = np.zeros_like(b)
+    scale = 0.5
+    got = oracle.gdn_backward(q, k, v, g, b, h0, cu, scale, Wo, Wh)
+    G = np.cumsum(g[:, 0])
+    S0 = h0[0, 0]
+    assert np.abs(got["dv"]).max() == 0 and np.abs(got["dk"]).max() == 0
+    dh0 = np.exp(G[-1]) * Wh[0, 0] + sum(np.exp(G[t]) * scale * np.outer(q[t, 0], Wo[t, 0])
+                                         for t in range(23))
+    np.testing.assert_allclose(got["dh0"][0, 0], dh0, rtol=1e-12, atol=1e-12)
+    dq = np.stack([scale * np.exp(G[t]) * (S0 @ Wo[t, 0]) for t in range(23)])
+    np.testing.assert_allclose(got["dq"][:, 0], dq, rtol=1e-12, atol=1e-12)
+    # dbeta_t = k_t^T dS_t u_t with u_t = v_t - e^{G_t} S0^T k_t and dS_t the
+    # gradient w.r.t. S_t: e^{G_T - G_t} dh_final + sum_{s >= t} e^{G_s - G_t} scale q_s do_s^T
+    for t in (0, 11, 22):
+        dS = np.exp(G[-1] - G[t]) * Wh[0, 0] + sum(np.exp(G[s] - G[t]) * scale * np.outer(q[s, 0], Wo[s, 0])
+                                                   for s in range(t, 23))
+        u = v[t, 0] - np.exp(G[t]) * S0.T @ k[t, 0]
+        np.testing.assert_allclose(got["dbeta"][t, 0], k[t, 0] @ dS @ u, rtol=1e-10)
+
+
+def test_backward_linear_in_output_gradients():
+    """The gradients are linear in (do, dh_final)."""
+    cu, q, k, v, g, b, h0, Wo, Wh = _bwd_problem(7, [40, 30], 2, 4, 5, 4)
+    a1 = oracle.gdn_backward(q, k, v, g, b, h0, cu, 1.0, Wo, None)
+    a2 = oracle.gdn_backward(q, k, v, g, b, h0, cu, 1.0, np.zeros_like(Wo), Wh)
+    a3 = oracle.gdn_backward(q, k, v, g, b, h0, cu, 1.0, 2 * Wo, -3 * Wh)
+    for x in a1:
+        np.testing.assert_allclose(a3[x], 2 * a1[x] - 3 * a2[x], rtol=1e-9, atol=1e-9)
