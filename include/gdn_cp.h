@@ -340,6 +340,75 @@ gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const void *conv_b, 
                          void *y, float *h_final, int32_t *plan_out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of the gated delta rule ([HP-CP] the custom autograd functions
+ * _RecvInitialStateP2PFunction / _SendFinalStateP2PFunction, whose backward
+ * sends the state gradient the other way; the forward is gdn_chunk_fwd's).
+ * Given the loss gradients dout (w.r.t. o) and dh_final (w.r.t. the final
+ * states), computes the gradients w.r.t. every input of gdn_chunk_fwd:
+ *   per token, with a = e^g, P = a S_prev, u = v - P^T k, S = P + beta k u^T,
+ *   o = S^T (scale q), walked backwards with the state gradient dS:
+ *     dq = scale S do,  dS += scale q do^T,  dbeta = k . (dS u),
+ *     du = beta dS^T k = dv,  dk = beta dS u - P du,  dP = dS - k du^T,
+ *     dg = <P, dP>,  dS_prev = a dP;   dh0 = dS before the first token.
+ *   q, k, v, ldq, ldk, ldv, dtype, g, beta, h0, cu_seqlens, num_seqs, T, Hk,
+ *           Hv, dk, dv, scale, flags: as in gdn_chunk_fwd (the same forward)
+ *   dout    device [T, Hv, dv] dtype, dense
+ *   dh_final device [num_seqs, Hv, dk, dv] fp32, or NULL (zero)
+ *   dq, dk_ device [T, Hk, dk] fp32 (summed over the Hv/Hk value heads that
+ *           read the q/k head; gradients of the stored q, k, through the L2
+ *           norm when flags has GDN_QK_L2NORM)
+ *   dv_     device [T, Hv, dv] fp32;  dg, dbeta device [T, Hv] fp32
+ *   dh0     device [num_seqs, Hv, dk, dv] fp32 (also when h0 is NULL)
+ *   workspace device, >= gdn_chunk_bwd_workspace_size(...) bytes, 256-byte
+ *           aligned, contents on entry irrelevant (8-token block-start states of every
+ *           sequence and a per-(sequence, head) replay scratch)
+ * dk, dv in {32, 64, 128}.  One block of 512 threads per (sequence, value
+ * head); the states before each token are recomputed from block-start
+ * checkpoints, so the cost grows with the longest sequence.
+ * ---------------------------------------------------------------------- */
+size_t gdn_chunk_bwd_workspace_size(int32_t T, int32_t num_seqs, int32_t Hk, int32_t Hv, int32_t dk,
+                                    int32_t dv);
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, int64_t ldq, int64_t ldk,
+                         int64_t ldv, gdn_dtype dtype, const float *g, const void *beta,
+                         const float *h0, const void *dout, const float *dh_final,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags, float *dq,
+                         float *dk_, float *dv_, float *dg, float *dbeta, float *dh0,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * gdn_chunk_bwd with every sequence cut into its pieces on n_shards virtual
+ * shards ([HP-CP] the backward of _RecvInitialStateP2PFunction /
+ * _SendFinalStateP2PFunction: the state gradient travels from a shard to the
+ * one before it).  The pieces (the shard plan's local segments) run in
+ * parallel: each piece's state map S_end = M S_start + N comes from its
+ * summary, the start states from a forward merge over each sequence's pieces,
+ * each piece's start-state gradient from its own outputs (b) from a first
+ * backward pass, the end-state gradients from the reverse merge
+ * dS_end(j - 1) = M_j^T dS_end(j) + b_j (dS_end of a sequence's last piece =
+ * dh_final), and the input gradients from a second backward pass.
+ * Arguments and results as in gdn_chunk_bwd, plus:
+ *   n_shards  1..65536, T % n_shards == 0
+ *   workspace device, >= gdn_shard_bwd_workspace_size(...) bytes, 256-byte
+ *             aligned, contents on entry irrelevant
+ *   plan_out  device int32 [gdn_cp_plan_words(num_seqs, n_shards)] or NULL:
+ *             receives the shard plan; its status word is
+ *             GDN_ERR_BAD_CU_SEQLENS when cu_seqlens is malformed, in which
+ *             case no gradient beyond zeroed dq / dk is written
+ * Results equal gdn_chunk_bwd's up to rounding.
+ * ---------------------------------------------------------------------- */
+size_t gdn_shard_bwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
+                                    int32_t Hv, int32_t dk, int32_t dv);
+gdn_status gdn_shard_bwd(const void *q, const void *k, const void *v, int64_t ldq, int64_t ldk,
+                         int64_t ldv, gdn_dtype dtype, const float *g, const void *beta,
+                         const float *h0, const void *dout, const float *dh_final,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                         int32_t n_shards, float *dq, float *dk_, float *dv_, float *dg,
+                         float *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
+                         int32_t *plan_out, void *stream);
+
+/* ------------------------------------------------------------------------
  * gdn_shard_fwd without a caller workspace.  The source pages have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory -- a plugin whose host application owns all device buffers

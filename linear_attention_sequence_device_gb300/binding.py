@@ -47,6 +47,14 @@ SIGNATURES = {
     "gdn_to_head_major": (ctypes.c_int, [_vp, _i64, ctypes.c_int, _i32, _i32, _i32, _vp, _vp]),
     "gdn_to_token_major": (ctypes.c_int, [_vp, ctypes.c_int, _i32, _i32, _i32, _vp, _i64, _vp]),
     "gdn_chunk_fwd_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, ctypes.c_int]),
+    "gdn_chunk_bwd_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "gdn_shard_bwd_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "gdn_shard_bwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _u32, _i32, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
+    "gdn_chunk_bwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _u32, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "gdn_chunk_summary": (ctypes.c_int, [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
                                          _i32, _i32, _i32, _i32, _i32, _i32, _u32, _vp, _vp,
                                          _vp]),
@@ -237,6 +245,65 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, h0=None, scale=None, l2norm=Fals
                              GDN_QK_L2NORM if l2norm else 0, _p(o), _p(hf), _p(ws),
                              0 if ws is None else ws.numel(), _stream()))
     return o, hf
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, h0=None, dh_final=None, scale=None, l2norm=False,
+                  workspace=None, n_shards=None, want_plan=False):
+    """Gradients of gdn_chunk_fwd's outputs (o, h_final) w.r.t. its inputs, for
+    the loss gradients dout [T, Hv, dv] (dtype of v) and dh_final [N, Hv, dk,
+    dv] fp32 (None: zero).  Returns a dict of fp32 tensors dq, dk [T, Hk, dk],
+    dv [T, Hv, dv], dg, dbeta [T, Hv] and dh0 [N, Hv, dk, dv].  workspace: a
+    uint8 device tensor of at least chunk_bwd_workspace_size bytes (allocated
+    per call when None).  n_shards: run it on that many virtual shards
+    (gdn_shard_bwd; want_plan also returns the plan words as "plan")."""
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (dout, "dout")):
+        _need(t, n, dt)
+    _need(g, "g", torch.float32)
+    _need(h0, "h0", torch.float32)
+    _need(dh_final, "dh_final", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    scale = dk ** -0.5 if scale is None else scale
+    dev = q.device
+    f32 = torch.float32
+    out = dict(dq=torch.empty((T, Hk, dk), dtype=f32, device=dev), dk=torch.empty((T, Hk, dk), dtype=f32, device=dev),
+               dv=torch.empty((T, Hv, dv), dtype=f32, device=dev), dg=torch.empty((T, Hv), dtype=f32, device=dev),
+               dbeta=torch.empty((T, Hv), dtype=f32, device=dev),
+               dh0=torch.empty((N, Hv, dk, dv), dtype=f32, device=dev))
+    lib = load()
+    if n_shards is not None:
+        if workspace is None:
+            workspace = torch.empty(max(lib.gdn_shard_bwd_workspace_size(T, N, n_shards, Hk, Hv, dk, dv), 256),
+                                    dtype=torch.uint8, device=dev)
+        plan = torch.empty(plan_words(N, n_shards), dtype=torch.int32, device=dev) if want_plan else None
+        _check(lib.gdn_shard_bwd(_p(q), _p(k), _p(v), _row_stride(q, "q"), _row_stride(k, "k"), _row_stride(v, "v"),
+                                 _dt(q), _p(g.contiguous()), _p(beta.contiguous()),
+                                 _p(None if h0 is None else h0.contiguous()), _p(dout.contiguous()),
+                                 _p(None if dh_final is None else dh_final.contiguous()), _p(cu_seqlens), N, T, Hk,
+                                 Hv, dk, dv, float(scale), GDN_QK_L2NORM if l2norm else 0, int(n_shards),
+                                 *(_p(out[x]) for x in ("dq", "dk", "dv", "dg", "dbeta", "dh0")),
+                                 _p(workspace), workspace.numel(), _p(plan), _stream()))
+        if want_plan:
+            out["plan"] = plan
+        return out
+    if workspace is None:
+        workspace = torch.empty(max(lib.gdn_chunk_bwd_workspace_size(T, N, Hk, Hv, dk, dv), 256), dtype=torch.uint8,
+                                device=dev)
+    _check(lib.gdn_chunk_bwd(_p(q), _p(k), _p(v), _row_stride(q, "q"), _row_stride(k, "k"), _row_stride(v, "v"),
+                             _dt(q), _p(g.contiguous()), _p(beta.contiguous()),
+                             _p(None if h0 is None else h0.contiguous()), _p(dout.contiguous()),
+                             _p(None if dh_final is None else dh_final.contiguous()), _p(cu_seqlens), N, T, Hk, Hv,
+                             dk, dv, float(scale), GDN_QK_L2NORM if l2norm else 0,
+                             *(_p(out[x]) for x in ("dq", "dk", "dv", "dg", "dbeta", "dh0")),
+                             _p(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def chunk_bwd_workspace_size(T, num_seqs, Hk, Hv, dk, dv) -> int:
+    return int(load().gdn_chunk_bwd_workspace_size(T, num_seqs, Hk, Hv, dk, dv))
 
 
 def to_head_major(x, out=None):

@@ -204,6 +204,134 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, int64_t ld
     return launch_chunk(p, dtype, JOBS_SEQS, grid, (cudaStream_t)stream);
 }
 
+size_t gdn_chunk_bwd_workspace_size(int32_t T, int32_t num_seqs, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv) {
+    if (T < 0 || num_seqs < 1 || Hk < 1 || Hv < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    return chunk_bwd_workspace_bytes(T, num_seqs, Hk, Hv, dk, dv);
+}
+
+gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, int64_t ldq, int64_t ldk, int64_t ldv,
+                         gdn_dtype dtype, const float* g, const void* beta, const float* h0, const void* dout,
+                         const float* dh_final, const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags, float* dq, float* dk_,
+                         float* dv_, float* dg, float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens || !dh0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens/dh0 is NULL");
+    if (flags & ~(uint32_t)GDN_QK_L2NORM) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const size_t need = chunk_bwd_workspace_bytes(T, num_seqs, Hk, Hv, dk, dv);
+    if (!workspace || workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace ? workspace_bytes : 0, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (T > 0) {
+        if ((st = check_row(q, ldq, (int64_t)Hk * dk, "q")) != GDN_OK) return st;
+        if ((st = check_row(k, ldk, (int64_t)Hk * dk, "k")) != GDN_OK) return st;
+        if ((st = check_row(v, ldv, (int64_t)Hv * dv, "v")) != GDN_OK) return st;
+        if (!g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta)
+            return fail(GDN_ERR_INVALID_ARG, "g/beta/dout or a gradient output is NULL");
+    }
+    return launch_chunk_bwd(q, k, v, ldq, ldk, ldv, dtype, g, beta, h0, dout, dh_final, cu_seqlens, num_seqs, T,
+                            Hk, Hv, dk, dv, scale, (flags & GDN_QK_L2NORM) ? 1 : 0, dq, dk_, dv_, dg, dbeta, dh0,
+                            workspace, (cudaStream_t)stream);
+}
+
+// workspace of gdn_shard_bwd: plan words, segment list, per-segment M, N,
+// start states, start-state gradients and end-state gradients, then the
+// backward kernel's own workspace over the segments
+struct ShardBwdLayout {
+    size_t plan, cu_seg, seg_seq, M, N, S, B, D, bwd, total;
+};
+static ShardBwdLayout shard_bwd_layout(int T, int num_seqs, int P, int Hk, int Hv, int dk, int dv) {
+    ShardBwdLayout L{};
+    const int nmax = num_seqs + P;
+    const size_t st = sizeof(float) * (size_t)nmax * Hv * dk * dv;
+    size_t o = 0;
+    L.plan = o; o += align256(sizeof(int32_t) * (size_t)gdn_cp_plan_words(num_seqs, P));
+    L.cu_seg = o; o += align256(sizeof(int32_t) * (size_t)(nmax + 1));
+    L.seg_seq = o; o += align256(sizeof(int32_t) * (size_t)nmax);
+    L.M = o; o += align256(sizeof(float) * (size_t)nmax * Hv * dk * dk);
+    L.N = o; o += align256(st);
+    L.S = o; o += align256(st);
+    L.B = o; o += align256(st);
+    L.D = o; o += align256(st);
+    L.bwd = o; o += align256(chunk_bwd_workspace_bytes(T, nmax, Hk, Hv, dk, dv));
+    L.total = o;
+    return L;
+}
+
+size_t gdn_shard_bwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk, int32_t Hv,
+                                    int32_t dk, int32_t dv) {
+    if (T < 0 || num_seqs < 1 || n_shards < 1 || Hk < 1 || Hv < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    return shard_bwd_layout(T, num_seqs, n_shards, Hk, Hv, dk, dv).total;
+}
+
+gdn_status gdn_shard_bwd(const void* q, const void* k, const void* v, int64_t ldq, int64_t ldk, int64_t ldv,
+                         gdn_dtype dtype, const float* g, const void* beta, const float* h0, const void* dout,
+                         const float* dh_final, const int32_t* cu_seqlens, int32_t num_seqs, int32_t T, int32_t Hk,
+                         int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags, int32_t n_shards,
+                         float* dq, float* dk_, float* dv_, float* dg, float* dbeta, float* dh0, void* workspace,
+                         size_t workspace_bytes, int32_t* plan_out, void* stream) {
+    gdn_status st = check_heads(dtype, T, num_seqs, Hk, Hv, dk, dv);
+    if (st != GDN_OK) return st;
+    const int P = n_shards;
+    if (P < 1 || P > 65536) return fail(GDN_ERR_INVALID_ARG, "n_shards=%d", P);
+    if (T % P != 0) return fail(GDN_ERR_NOT_DIVISIBLE, "T=%d is not a multiple of n_shards=%d", T, P);
+    if (!cu_seqlens || !dh0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens/dh0 is NULL");
+    if (flags & ~(uint32_t)GDN_QK_L2NORM) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const ShardBwdLayout L = shard_bwd_layout(T, num_seqs, P, Hk, Hv, dk, dv);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace ? workspace_bytes : 0,
+                    L.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (T > 0) {
+        if ((st = check_row(q, ldq, (int64_t)Hk * dk, "q")) != GDN_OK) return st;
+        if ((st = check_row(k, ldk, (int64_t)Hk * dk, "k")) != GDN_OK) return st;
+        if ((st = check_row(v, ldv, (int64_t)Hv * dv, "v")) != GDN_OK) return st;
+        if (!g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta)
+            return fail(GDN_ERR_INVALID_ARG, "g/beta/dout or a gradient output is NULL");
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const int l2 = (flags & GDN_QK_L2NORM) ? 1 : 0;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    int32_t* plan = plan_out ? plan_out : reinterpret_cast<int32_t*>(w + L.plan);
+    int32_t* cu_seg = reinterpret_cast<int32_t*>(w + L.cu_seg);
+    int32_t* seg_seq = reinterpret_cast<int32_t*>(w + L.seg_seq);
+    float* Ms = reinterpret_cast<float*>(w + L.M);
+    float* Ns = reinterpret_cast<float*>(w + L.N);
+    float* Ss = reinterpret_cast<float*>(w + L.S);
+    float* Bs = reinterpret_cast<float*>(w + L.B);
+    float* Ds = reinterpret_cast<float*>(w + L.D);
+    void* bws = w + L.bwd;
+    const int nmax = num_seqs + P;
+    // 1. the segments: the shard plan's local segments of all shards
+    if ((st = launch_plan(cu_seqlens, num_seqs, P, plan, s)) != GDN_OK) return st;
+    if ((st = launch_segments(plan, num_seqs, P, T, nmax, cu_seg, seg_seq, s)) != GDN_OK) return st;
+    // 2. every segment's affine state map (M, N) and its start state
+    ChunkParams p{};
+    p.q = k; p.k = k; p.v = v; p.ldq = ldk; p.ldk = ldk; p.ldv = ldv;
+    p.g = g; p.beta = beta; p.cu = cu_seg;
+    p.num_seqs = nmax; p.T = T; p.Hk = Hk; p.Hv = Hv; p.dk = dk; p.dv = dv;
+    p.scale = 1.f; p.flags = flags; p.sumN = Ns; p.sumM = Ms;
+    p.col_tile = chunk_col_tile(dtype, dk, dv);
+    set_token_major(p);
+    if ((st = launch_chunk(p, dtype, JOBS_SUMMARY, dim3(nmax, Hv, (dv + dk) / p.col_tile), s)) != GDN_OK) return st;
+    if ((st = launch_seg_merge(true, plan, seg_seq, nmax, num_seqs, Hv, dk, dv, Ms, Ns, h0, Ss, s)) != GDN_OK)
+        return st;
+    // 3. each segment's start-state gradient from its own outputs (end gradient 0)
+    if ((st = launch_chunk_bwd(q, k, v, ldq, ldk, ldv, dtype, g, beta, Ss, dout, nullptr, cu_seg, nmax, T, Hk, Hv,
+                               dk, dv, scale, l2, dq, dk_, dv_, dg, dbeta, Bs, bws, s)) != GDN_OK)
+        return st;
+    // 4. the end-state gradients, each sequence's segments in reverse order
+    if ((st = launch_seg_merge(false, plan, seg_seq, nmax, num_seqs, Hv, dk, dv, Ms, Bs, dh_final, Ds, s)) != GDN_OK)
+        return st;
+    // 5. the input gradients of every segment, from its true start state and end-state gradient
+    if ((st = launch_chunk_bwd(q, k, v, ldq, ldk, ldv, dtype, g, beta, Ss, dout, Ds, cu_seg, nmax, T, Hk, Hv, dk,
+                               dv, scale, l2, dq, dk_, dv_, dg, dbeta, Bs, bws, s)) != GDN_OK)
+        return st;
+    return launch_seg_dh0(plan, seg_seq, nmax, num_seqs, Hv, dk, dv, Bs, dh_final, dh0, s);
+}
+
 gdn_status gdn_chunk_fwd_heads(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* g,
                                const void* beta, const float* h0, const int32_t* cu_seqlens, int32_t num_seqs,
                                int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, float scale,

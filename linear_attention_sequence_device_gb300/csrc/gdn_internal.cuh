@@ -365,6 +365,21 @@ gdn_status launch_combine(const float* M, const float* N, const float* S0, int P
 // layout.cu: [T, H, d] (token stride ld) <-> dense [H, T, d]
 gdn_status launch_relayout(const void* src, void* dst, int64_t T, int H, int d, int64_t ld, gdn_dtype dt,
                            bool to_heads, cudaStream_t s);
+// backward.cu: the backward of the recurrence over (sequence, value head) jobs
+size_t chunk_bwd_workspace_bytes(int T, int num_seqs, int Hk, int Hv, int dk, int dv);
+gdn_status launch_chunk_bwd(const void* q, const void* k, const void* v, int64_t ldq, int64_t ldk, int64_t ldv,
+                            gdn_dtype dtype, const float* g, const void* beta, const float* h0, const void* dout,
+                            const float* dh_final, const int32_t* cu, int num_seqs, int T, int Hk, int Hv, int dk,
+                            int dv, float scale, int l2, float* dq, float* dk_, float* dv_, float* dg, float* dbeta,
+                            float* dh0, void* workspace, cudaStream_t s);
+// shard_bwd.cu: segments of the shard plan, and the merges of the backward across shards
+gdn_status launch_segments(const int32_t* plan, int num_seqs, int P, int T, int nmax, int32_t* cu_seg,
+                           int32_t* seg_seq, cudaStream_t s);
+gdn_status launch_seg_merge(bool fwd, const int32_t* plan, const int32_t* seg_seq, int nmax, int num_seqs, int Hv,
+                            int dk, int dv, const float* M, const float* NB, const float* init, float* out,
+                            cudaStream_t s);
+gdn_status launch_seg_dh0(const int32_t* plan, const int32_t* seg_seq, int nmax, int num_seqs, int Hv, int dk,
+                          int dv, const float* dh0_seg, const float* dh_final, float* dh0, cudaStream_t s);
 // gated RMS norm of o in place (combine.cu), for the kernels without the epilogue
 gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w, float eps, int64_t T, int Hv,
                              int dv, gdn_dtype dt, cudaStream_t s);
