@@ -12,7 +12,10 @@ merge, chunk pass 2, final states), timed with CUDA events recorded between
 the step's own launches; "roofline" rates the two chunk passes together.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                  [--impl ours|reference] [--no-cpu-baseline]
+                  [--impl ours|reference] [--no-cpu-baseline] [--pass forward|backward]
+
+--pass backward times the backward of the recurrence (gdn_chunk_bwd, or
+gdn_shard_bwd on the config's shards) instead of the forward step.
 
 With N > 1 (launched by torch.distributed.run) every rank runs an
 independent replica of the workload on its own GPU (weak scaling, no
@@ -236,6 +239,73 @@ def config_dict(w):
             "l2": "inputs larger than L2 (raw qkv %.0f MiB)" % (w.T * w.Cch * (2 if w.dtype == "bf16" else 4) / 2**20)}
 
 
+def run_backward(args, rank, world, local_rank):
+    """--pass backward: the backward of the recurrence (gdn_chunk_bwd, or
+    gdn_shard_bwd on the config's P shards) on the config's q, k, v, gates,
+    h0 and seeded output gradients; one JSON line, tokens/s of the backward
+    step with its inputs resident in HBM."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import linear_attention_sequence_device_gb300 as g
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workload(args.config)
+    if rank:
+        w = w.replace(seed=w.seed + 1000 * rank)
+    P = w.n_shards
+    q = to_dev(w.q(), w.dtype, dev).view(w.T, w.Hk, w.dk)
+    k = to_dev(w.k(), w.dtype, dev).view(w.T, w.Hk, w.dk)
+    v = to_dev(w.v(), w.dtype, dev).view(w.T, w.Hv, w.dv)
+    gg, bb = to_dev(w.g(), "f32", dev), to_dev(w.beta(), w.dtype, dev)
+    h0_h = w.h0()
+    h0 = None if h0_h is None else to_dev(h0_h, "f32", dev)
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    do = torch.randn((w.T, w.Hv, w.dv), generator=gen, device=dev).to(v.dtype)
+    dh = torch.randn((w.N, w.Hv, w.dk, w.dv), generator=gen, device=dev)
+    if P > 1:
+        wsz = g.load().gdn_shard_bwd_workspace_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv)
+    else:
+        wsz = g.chunk_bwd_workspace_size(w.T, w.N, w.Hk, w.Hv, w.dk, w.dv)
+    ws = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        g.gdn_chunk_bwd(q, k, v, gg, bb, cu, do, h0=h0, dh_final=dh, workspace=ws,
+                        n_shards=P if P > 1 else None)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(local_rank) as clk:
+        ms = time_loop(step, args.steps, stream)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    e = 2 if w.dtype == "bf16" else 4
+    # algorithmic bytes: q, k, v, dout, g, beta read; fp32 dq, dk, dv, dg, dbeta written;
+    # h0, dh_final read and dh0 written per sequence
+    byts = w.T * (2 * w.Hk * w.dk * e + 2 * w.Hv * w.dv * e + w.Hv * (4 + e)
+                  + 4 * (2 * w.Hk * w.dk + w.Hv * w.dv + 2 * w.Hv)) + 3 * w.N * w.Hv * w.dk * w.dv * 4
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ach = byts / (ms * 1e-3) / 1e9
+    line = {"metric": "GDN backward tokens/s at 1 GB300", "value": world * w.T / (ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded counter-based generator; no dataset)", "config": config_dict(w),
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": None, "kernel": "bwd_job_kernel", "peak_source": src,
+                         "algorithmic_bytes": byts},
+            "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import __graft_entry__
@@ -447,6 +517,7 @@ def main():
     ap.add_argument("--config", default="million")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"])
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -459,7 +530,7 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        run_ours(args, rank, world, local_rank)
+        (run_backward if args.which == "backward" else run_ours)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch
