@@ -19,9 +19,11 @@
 // conflicts).  Row sums (K-vectors) reduce over the TPR lanes
 // of a row by shuffles; column sums (V-vectors) over the rows through shared
 // memory.  The states before each token are recomputed: a forward pass over
-// the job keeps the state at every 8-token block start in the workspace;
-// going backwards, each block is replayed once to keep the state before each
-// of its tokens (a per-job scratch of 8 states, small enough to stay in L2).
+// the job (threads owning state columns, so that its column sums need no
+// block-wide sync) keeps the state at every 8-token block start in the
+// workspace; going backwards, each block is replayed once (row-owning, as
+// the reverse step) to keep the state before each of its tokens (a per-job
+// scratch of 8 states, small enough to stay in L2) and its u = v - P^T k.
 // Each 64-token chunk's q, k, v, do, g and beta are staged in shared memory.
 #include "gdn_internal.cuh"
 
@@ -105,6 +107,11 @@ struct BwdJob {
     static constexpr int TPR = NTB / DK;
     static constexpr int CPT = DV / TPR;
     static_assert(TPR >= 1 && TPR <= 32 && (32 % TPR) == 0 && CPT >= 1 && DV % TPR == 0, "shape");
+    // the forward steps own columns instead: TPC threads per state column,
+    // thread rb of a column holding the RPT rows rb RPT .. rb RPT + RPT
+    static constexpr int TPC = NTB / DV;
+    static constexpr int RPT = DK / TPC;
+    static_assert(TPC >= 1 && TPC <= 32 && (32 % TPC) == 0 && RPT == CPT, "shape");
 
     struct Smem {
         float ks[kChunk][DK], qs[kChunk][DK];
@@ -113,17 +120,18 @@ struct BwdJob {
         float red[NWB][DV];
         float vec[DV];
         float sred[NWB][2];
+        float us[kSub][DV];   // u = v - P^T k of the block's tokens, from the replay
         float dS[CPT][NTB];   // the state gradient, element i of thread t at [i][t]
     };
 
     const BwdParams& p;
     Smem& sm;
-    const int tid, lane, warp, row, lr;
+    const int tid, lane, warp, row, lr, ccol, rb;
     int n, hv, hk;
 
     __device__ BwdJob(const BwdParams& p_, Smem& sm_)
         : p(p_), sm(sm_), tid(threadIdx.x), lane(threadIdx.x & 31), warp(threadIdx.x >> 5),
-          row(threadIdx.x / TPR), lr(threadIdx.x % TPR) {}
+          row(threadIdx.x / TPR), lr(threadIdx.x % TPR), ccol(threadIdx.x / TPC), rb(threadIdx.x % TPC) {}
     __device__ __forceinline__ int col(int i) const { return lr + TPR * i; }
 
     // sum over the rows of each of this thread's columns.  Within a warp the
@@ -178,6 +186,21 @@ struct BwdJob {
         for (int i = 0; i < CPT; ++i) s[i] = __ldcg(d + i * NTB);
     }
 
+    // the same layout addressed by (row, column), for the column-owning steps
+    __device__ __forceinline__ static int64_t at(int r, int c) {
+        return (int64_t)(c / TPR) * NTB + (int64_t)r * TPR + (c % TPR);
+    }
+    __device__ __forceinline__ void store_state_col(float* base, int slot, const float (&s)[RPT]) {
+        float* d = base + (int64_t)slot * CPT * NTB;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) d[at(rb * RPT + j, ccol)] = s[j];
+    }
+    __device__ __forceinline__ void load_state_col(const float* base, int slot, float (&s)[RPT]) {
+        const float* d = base + (int64_t)slot * CPT * NTB;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) s[j] = __ldcg(d + at(rb * RPT + j, ccol));
+    }
+
     // tokens [tb, tb + cnt) of the job into shared memory
     __device__ void stage(int tb, int cnt, bool all) {
         __syncthreads();  // every thread is done with the previous chunk's tiles
@@ -208,8 +231,10 @@ struct BwdJob {
         __syncthreads();
     }
 
-    // S <- a S + beta k (v - a S^T k)^T  for staged token j
-    __device__ __forceinline__ void fwd_step(int j, float (&S)[CPT]) {
+    // the same step row-owning (the replay: its states are stored in the
+    // row-owning layout with whole-line stores); u of its columns to row 0's
+    // threads, which keep it in shared memory for the reverse step
+    __device__ __forceinline__ void fwd_step_rows(int j, float (&S)[CPT], float* us_row) {
         const float a = __expf(sm.gs[j]), b = sm.bs[j];
         const float kr = sm.ks[j][row] * sm.rks[j];
         float x[CPT];
@@ -218,9 +243,47 @@ struct BwdJob {
             S[i] *= a;
             x[i] = S[i] * kr;
         }
-        vred(x);
+        vred(x);  // a S^T k
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) S[i] = fmaf(b * kr, sm.vs[j][col(i)] - x[i], S[i]);
+        for (int i = 0; i < CPT; ++i) {
+            const float u = sm.vs[j][col(i)] - x[i];
+            if (row == 0) us_row[col(i)] = u;
+            S[i] = fmaf(b * kr, u, S[i]);
+        }
+    }
+
+    // S <- a S + beta k (v - a S^T k)^T for staged token j, column-owning
+    // (the column's sum over the rows is a shuffle among its TPC threads, no
+    // block-wide sync); returns u = v - a S^T k of the thread's column
+    __device__ __forceinline__ float fwd_step(int j, float (&S)[RPT]) {
+        const float a = __expf(sm.gs[j]), b = sm.bs[j], rk = sm.rks[j];
+        float kr[RPT];
+        if constexpr (RPT % 4 == 0) {
+            const float4* k4 = reinterpret_cast<const float4*>(&sm.ks[j][rb * RPT]);
+#pragma unroll
+            for (int q4 = 0; q4 < RPT / 4; ++q4) {
+                const float4 f = k4[q4];
+                kr[4 * q4] = f.x * rk;
+                kr[4 * q4 + 1] = f.y * rk;
+                kr[4 * q4 + 2] = f.z * rk;
+                kr[4 * q4 + 3] = f.w * rk;
+            }
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < RPT; ++jj) kr[jj] = sm.ks[j][rb * RPT + jj] * rk;
+        }
+        float x = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < RPT; ++jj) {
+            S[jj] *= a;
+            x = fmaf(S[jj], kr[jj], x);
+        }
+#pragma unroll
+        for (int off = 1; off < TPC; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        const float u = sm.vs[j][ccol] - x;
+#pragma unroll
+        for (int jj = 0; jj < RPT; ++jj) S[jj] = fmaf(b * kr[jj], u, S[jj]);
+        return u;
     }
 
     // the reverse step of staged token j (global token t), from the state
@@ -229,13 +292,10 @@ struct BwdJob {
         const float a = __expf(sm.gs[j]), b = sm.bs[j];
         const float kr = sm.ks[j][row] * sm.rks[j], qr = sm.qs[j][row] * sm.rqs[j] * p.scale;
         float x[CPT];
-#pragma unroll
-        for (int i = 0; i < CPT; ++i) x[i] = a * Sp[i] * kr;
-        vred(x);  // P^T k
         float udo = 0.f, pdo = 0.f, dsu = 0.f;
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const float u = sm.vs[j][col(i)] - x[i], dov = sm.dos[j][col(i)];
+            const float u = sm.us[j % kSub][col(i)], dov = sm.dos[j][col(i)];
             udo = fmaf(u, dov, udo);
             pdo = fmaf(a * Sp[i], dov, pdo);
             const float ds = fmaf(qr, dov, sm.dS[i][tid]);  // dS += scale q do^T
@@ -301,15 +361,16 @@ struct BwdJob {
         const int ck_stride = p.Hv;  // in states, between consecutive blocks
         float* tok = p.scratch + ((int64_t)n * p.Hv + hv) * kSub * state;
         const int64_t sidx = ((int64_t)n * p.Hv + hv) * state + (int64_t)row * DV;
-        float S[CPT];
+        // forward (column-owning): the state at every block start
+        float S[RPT];
+        const int64_t sidx_col = ((int64_t)n * p.Hv + hv) * state + (int64_t)rb * RPT * DV + ccol;
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) S[i] = p.h0 ? p.h0[sidx + col(i)] : 0.f;
-        // forward: the state at every block start
+        for (int jj = 0; jj < RPT; ++jj) S[jj] = p.h0 ? p.h0[sidx_col + (int64_t)jj * DV] : 0.f;
         for (int c = 0; c < nch; ++c) {
             const int cnt = min(kChunk, L - c * kChunk);
             stage(t0 + c * kChunk, cnt, false);
             for (int j = 0; j < cnt; ++j) {
-                if (j % kSub == 0) store_state(ck, (c * (kChunk / kSub) + j / kSub) * ck_stride, S);
+                if (j % kSub == 0) store_state_col(ck, (c * (kChunk / kSub) + j / kSub) * ck_stride, S);
                 fwd_step(j, S);
             }
         }
@@ -322,11 +383,13 @@ struct BwdJob {
             const int nb = (cnt + kSub - 1) / kSub;
             for (int bl = nb - 1; bl >= 0; --bl) {
                 const int j0 = bl * kSub, j1 = min(cnt, j0 + kSub);
-                load_state(ck, (c * (kChunk / kSub) + bl) * ck_stride, S);
-                for (int j = j0; j < j1; ++j) {  // the state before each token
-                    store_state(tok, j - j0, S);
-                    fwd_step(j, S);
+                float R[CPT];
+                load_state(ck, (c * (kChunk / kSub) + bl) * ck_stride, R);
+                for (int j = j0; j < j1; ++j) {  // the state before each token, and its u
+                    store_state(tok, j - j0, R);
+                    fwd_step_rows(j, R, sm.us[j - j0]);
                 }
+                __syncthreads();  // the block's u is visible to every thread
                 for (int j = j1 - 1; j >= j0; --j) {
                     float Sp[CPT];
                     load_state(tok, j - j0, Sp);
