@@ -581,7 +581,7 @@ __device__ __forceinline__ bool norms_fn(SmemWS& sm, int gq, int gt, bool l2) {
     float acc0 = 0.f, acc1 = 0.f;
     if (l2) {
         const bf16* QKn = sm.QK[ss];
-#pragma unroll
+#pragma unroll 4
         for (int ch = 0; ch < 16; ++ch) {
             const uint4 raw = *reinterpret_cast<const uint4*>(&QKn[tc::sw128_chunk(128, r, ch)]);
             const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -683,7 +683,7 @@ __device__ __forceinline__ void store_state_fn(const JobRec& J, uint32_t t_s, in
 __device__ __forceinline__ void w_readout_fn(SmemWS& sm, int ss, uint32_t t_w, int row, int half) {
     const int d = row, wrow0 = ss ? 64 : 0;
     const int dch = (d & 63) >> 3;
-#pragma unroll
+#pragma unroll 1
     for (int h16 = 0; h16 < 2; ++h16) {
         float wv[16];
         tc::ld16(t_w + 32 * half + 16 * h16, wv);
@@ -1234,7 +1234,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     // the new state: its bf16 copy, and the state scaled by the next
                     // chunk's e^{G_last}, back into tensor memory (16-column pieces)
                     const float egn = *reinterpret_cast<volatile float*>(&sm.ci[(g + 1) & 7].eglast);
-#pragma unroll
+#pragma unroll 1  // kept rolled: the kernel's code size costs instruction-fetch stalls
                     for (int q4 = 0; q4 < 4; ++q4) {
                         float sv[16];
                         uint32_t w[8];
