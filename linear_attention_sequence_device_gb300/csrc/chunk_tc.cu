@@ -703,27 +703,31 @@ __device__ __forceinline__ void qk_prep_fn(SmemWS& sm, int gq, int c) {
     bf16* QKs = sm.QK[ss];
     bf16* KTs = sm.KT[ss];
     const int qrow0 = ss ? 0 : 64, krow0 = 64 - qrow0;
-    uint4 raw[8];
+    // the Q rows, then the K rows (kept rolled: code size); loads first
+#pragma unroll 1
+    for (int isk = 0; isk < 2; ++isk) {
+        const int rowb = isk ? krow0 : qrow0;
+        uint4 raw[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {  // k < 4: Q rows, else K rows; chunk e = c + 256 (k & 3)
-        const int e = c + 256 * (k & 3), r = e >> 4, ch = e & 15;
-        raw[k] = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, (k >= 4 ? krow0 : qrow0) + r, ch)]);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int e = c + 256 * (k & 3), r = e >> 4, ch = e & 15;
-        const bool isk = k >= 4;
-        const float fs = isk ? sl.fac[r] : -sl.qf[r];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 t2 = __bfloat1622float2(h[i]);
-            x[2 * i] = t2.x * fs;
-            x[2 * i + 1] = t2.y * fs;
+        for (int k = 0; k < 4; ++k) {  // chunk e = c + 256 k
+            const int e = c + 256 * k, r = e >> 4, ch = e & 15;
+            raw[k] = *reinterpret_cast<const uint4*>(&QKs[tc::sw128_chunk(128, rowb + r, ch)]);
         }
-        bf16* dst = isk ? &KTs[tc::sw128_chunk(64, r, ch)] : &QKs[tc::sw128_chunk(128, qrow0 + r, ch)];
-        *reinterpret_cast<uint4*>(dst) = pack8(x);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = c + 256 * k, r = e >> 4, ch = e & 15;
+            const float fs = isk ? sl.fac[r] : -sl.qf[r];
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 t2 = __bfloat1622float2(h[i]);
+                x[2 * i] = t2.x * fs;
+                x[2 * i + 1] = t2.y * fs;
+            }
+            bf16* dst = isk ? &KTs[tc::sw128_chunk(64, r, ch)] : &QKs[tc::sw128_chunk(128, qrow0 + r, ch)];
+            *reinterpret_cast<uint4*>(dst) = pack8(x);
+        }
     }
 }
 
@@ -851,42 +855,36 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         auto al_readout = [&](int s, int hh) {
             const bool isq = s ? (row < 64) : (row >= 64);
             const int i = row & 63;
-            float gv[32];
-            tc::ld32(T_GRAM + lb + 32 * hh, gv);
-            float a[32];
             const int lim = isq ? i : i - 1;  // A keeps the diagonal, L does not
-            if (sm.factored) {
-                const float fi = isq ? sm.rowA[i] : sm.rowL[i];
-                const float4* cf = reinterpret_cast<const float4*>(sm.colf[i >> 4] + 32 * hh);
+            // 8 columns at a time (kept rolled: code size costs instruction-fetch stalls)
+#pragma unroll 1
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const int cb = 32 * hh + 8 * c8;
+                float gv[8], a[8];
+                tc::ld8(T_GRAM + lb + cb, gv);
+                if (sm.factored) {
+                    const float fi = isq ? sm.rowA[i] : sm.rowL[i];
+                    const float4* cf = reinterpret_cast<const float4*>(sm.colf[i >> 4] + cb);
+                    const float4 f0 = cf[0], f1 = cf[1];
+                    const float fc[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const float4 f4 = cf[c4];
-                    const float fc[4] = {f4.x, f4.y, f4.z, f4.w};
+                    for (int e = 0; e < 8; ++e) a[e] = (cb + e <= lim) ? fi * (fc[e] * gv[e]) : 0.f;
+                } else {  // wide gate range: one exponential per element
+                    const float Gi = sm.G[i];
+                    const float fi = isq ? p.scale * sm.rn[i] : sm.slot[s].beta[i] * sm.rn[64 + i];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c2 = 4 * c4 + e;
-                        a[c2] = (32 * hh + c2 <= lim) ? fi * (fc[e] * gv[c2]) : 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = cb + e;
+                        a[e] = (j <= lim) ? fi * sm.rn[64 + j] * gv[e] * __expf(Gi - sm.G[j]) : 0.f;
                     }
                 }
-            } else {  // wide gate range: one exponential per element
-                const float Gi = sm.G[i];
-                const float fi = isq ? p.scale * sm.rn[i] : sm.slot[s].beta[i] * sm.rn[64 + i];
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) {
-                    const int j = 32 * hh + c2;
-                    a[c2] = (j <= lim) ? fi * sm.rn[64 + j] * gv[c2] * __expf(Gi - sm.G[j]) : 0.f;
+                if (isq) {
+                    *reinterpret_cast<uint4*>(&sm.A[s][tc::sw128_chunk(64, i, cb >> 3)]) = pack8(a);
+                } else {
+                    float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + cb);
+                    Lrow[0] = make_float4(a[0], a[1], a[2], a[3]);
+                    Lrow[1] = make_float4(a[4], a[5], a[6], a[7]);
                 }
-            }
-            if (isq) {
-                bf16* As = sm.A[s];
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4*>(&As[tc::sw128_chunk(64, i, 4 * hh + c8)]) = pack8(&a[8 * c8]);
-            } else {
-                float4* Lrow = reinterpret_cast<float4*>(sm.LT + i * LDF + 32 * hh);
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    Lrow[c4] = make_float4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
             }
         };
         bool pend = true;  // this thread's verdict on work whose barrier is still ahead
@@ -1033,17 +1031,27 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         // shared memory) and the stores write norm_w * o / sqrt(mean(o^2) + eps) * silu(z).
         constexpr bool gnorm = GNORM;
         auto write_output = [&](int otb, int ovalid, int ohv) {
-            float ov[32];
-            tc::ld32(T_O + lb + 32 * half, ov);
             bf16* ot = sm.OST + (32 * half) * 128 + row;
+            if constexpr (gnorm) {
+                float ov[32];
+                tc::ld32(T_O + lb + 32 * half, ov);
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) {
-                const bf16 ob = __float2bfloat16_rn(ov[c2]);
-                ot[c2 * 128] = ob;
-                const float of = __bfloat162float(ob);
-                ov[c2] = of * of;
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const bf16 ob = __float2bfloat16_rn(ov[c2]);
+                    ot[c2 * 128] = ob;
+                    const float of = __bfloat162float(ob);
+                    ov[c2] = of * of;
+                }
+                sm.ored[warp & 3][32 * half + lane] = reduce_scatter32(ov);
+            } else {  // 8 tokens at a time (kept rolled: code size)
+#pragma unroll 1
+                for (int h8 = 0; h8 < 4; ++h8) {
+                    float ov[8];
+                    tc::ld8(T_O + lb + 32 * half + 8 * h8, ov);
+#pragma unroll
+                    for (int c2 = 0; c2 < 8; ++c2) ot[(8 * h8 + c2) * 128] = __float2bfloat16_rn(ov[c2]);
+                }
             }
-            if constexpr (gnorm) sm.ored[warp & 3][32 * half + lane] = reduce_scatter32(ov);
             tc::bar_sync(BAR_S, GS);
             for (int e = gt; e < 64 * 16; e += GS) {
                 const int t = e >> 4, ch = e & 15;

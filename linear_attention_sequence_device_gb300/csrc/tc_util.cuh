@@ -210,6 +210,18 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
         : "memory");
 }
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 // 32 lanes x 16 consecutive 32-bit columns (the x32 forms above, half as wide).
 __device__ __forceinline__ void ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
