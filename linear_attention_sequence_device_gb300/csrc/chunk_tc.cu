@@ -42,6 +42,9 @@
 //     packs v_new to bf16 in place in tensor memory (the A operand of the
 //     second product), issues the second product, and while it runs forms
 //     chunk g+1's -Q~ / K~ and reads its W if that chunk's W/U are done.
+// A chunk whose output is not written (a summary job) uses no Q: its Q norms,
+// A read-out and -Q~ are skipped, and its first product takes the W rows
+// alone (N = 64, straight into v_new's columns).
 // The fp32 state stays in tensor memory: after each update it is read once
 // for its bf16 copy (the next chunk's A operand) and written back scaled by
 // the next chunk's e^{G_last}, onto which the next update accumulates.
@@ -182,6 +185,7 @@ struct SmemWS {
 constexpr uint32_t ID_N64 = tc::idesc_bf16(128, 64, false, false, false);
 constexpr uint32_t ID_N64_AMN = tc::idesc_bf16(128, 64, true, false, false);
 constexpr uint32_t ID_N128_NEG = tc::idesc_bf16(128, 128, false, false, false) | (1u << 14);  // B negated
+constexpr uint32_t ID_N64_NEG = ID_N64 | (1u << 14);
 constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 
 // One warp: the chunk's gate prefix from per-token values held by lanes
@@ -579,7 +583,8 @@ __device__ __forceinline__ bool norms_fn(SmemWS& sm, int gq, int gt, bool l2) {
     if (gt == 128) GDN_STAMP(gq - 1, 14);
     const int r = gt - 128;
     float acc0 = 0.f, acc1 = 0.f;
-    if (l2) {
+    const bool qskip = (ss ? (r < 64) : (r >= 64)) && !sm.ci[gq & 7].write_o;  // no output: Q norms unused
+    if (l2 && !qskip) {
         const bf16* QKn = sm.QK[ss];
 #pragma unroll 4
         for (int ch = 0; ch < 16; ++ch) {
@@ -698,6 +703,7 @@ __device__ __forceinline__ void w_readout_fn(SmemWS& sm, int ss, uint32_t t_w, i
 // 8 chunks each, loads first so that they overlap.  Needs the chunk's
 // factors (published with eg_ready) and its [rows] K^T read (aread).
 __device__ __forceinline__ void qk_prep_fn(SmemWS& sm, int gq, int c) {
+    const int isk0 = sm.ci[gq & 7].write_o ? 0 : 1;  // no output: K~ alone
     const int ss = gq & 1;
     const SlotSmall& sl = sm.slot[ss];
     bf16* QKs = sm.QK[ss];
@@ -705,7 +711,7 @@ __device__ __forceinline__ void qk_prep_fn(SmemWS& sm, int gq, int c) {
     const int qrow0 = ss ? 0 : 64, krow0 = 64 - qrow0;
     // the Q rows, then the K rows (kept rolled: code size); loads first
 #pragma unroll 1
-    for (int isk = 0; isk < 2; ++isk) {
+    for (int isk = isk0; isk < 2; ++isk) {
         const int rowb = isk ? krow0 : qrow0;
         uint4 raw[4];
 #pragma unroll
@@ -919,7 +925,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (gt == 32) GDN_STAMP(g, 1);
                 if (a) {
                     const int qd = warp & 3, hh = warp == 4 ? 0 : (warp >> 2);
-                    if (!(hh == 1 && (qd & 1) == 0)) al_readout(s, hh);  // quarters 0, 2: rows 0-31 of A / L
+                    const bool qq = s ? (qd < 2) : (qd >= 2);  // this warp's lanes are Q rows
+                    if (!(hh == 1 && (qd & 1) == 0) && (!qq || sm.ci[g & 7].write_o)) al_readout(s, hh);  // quarters 0, 2: rows 0-31 of A / L
                 }
                 tc::fence_before();
                 pend = tc::bar_and(BAR_Q, GS - 32, a);
@@ -1120,7 +1127,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     write_output(o_tb, o_valid, o_hv);
                     o_pending = false;
                 }
-                if (g > 0) tc::st32_zero(T_O + lb + 32 * half);
+                if (g > 0 && sm.ci[g & 7].write_o) tc::st32_zero(T_O + lb + 32 * half);
                 // -Q~ and K~ of this chunk, once the producer has published its
                 // factors and read its [rows] K^T columns (while the UT inverse
                 // runs), unless done during the previous chunk
@@ -1164,11 +1171,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     tc::fence_after();
                     // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T (slot 0; slot 1 the
                     // other row order), S^T bf16 from tensor memory
-                    const uint32_t D1 = s ? T_O : T_VN0;
-                    const uint64_t dB = dQK0 + (s ? kQKslot : 0);
+                    if (I.write_o) {
+                        const uint32_t D1 = s ? T_O : T_VN0;
+                        const uint64_t dB = dQK0 + (s ? kQKslot : 0);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ta(D1, T_SB + 8 * kk, dB + tc::koff(128, kk), ID_N128_NEG, 1u);
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ta(D1, T_SB + 8 * kk, dB + tc::koff(128, kk), ID_N128_NEG, 1u);
+                    } else {  // no output: v_new^T = U^T - S^T W^T alone (the slot's K rows)
+                        const uint64_t dB = dQK0 + krows(s);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ta(T_VNs, T_SB + 8 * kk, dB + tc::koff(128, kk), ID_N64_NEG, 1u);
+                    }
                     tc::commit(&sm.mbar_s);
                     GDN_STAMP(g, 20);
                 }
