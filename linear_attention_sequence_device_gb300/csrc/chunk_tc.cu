@@ -25,15 +25,16 @@
 //
 // Two roles of two warpgroups each work on different chunks at once:
 //   producer (warps 0-7), chunk g, a chunk ahead of the consumer:
-//     A) warps 1-7 read A and L out of chunk g's [rows] K^T columns; thread 0
-//        waits for chunk g-1's W/U products and issues chunk g's V load;
+//     A) warps 1-7 read A and L out of chunk g's [rows] K^T columns (once
+//        chunk g-2's output products have read the A slot); thread 0 waits
+//        for chunk g-1's W/U products and issues chunk g's V load;
 //     B) warps 0-3 run the UT inverse (tf32 mma.sync 16x16 blocks, written as
-//        the bf16 operands Tb and Tbg); warps 4-7 load chunk g+1's g and beta
-//        and take jobs / fill chunk infos two chunks ahead;
-//     C) thread 0 issues W^T and U^T once V has landed and the consumer has
-//        read chunk g-1's W; thread 32 issues chunk g+1's [rows] K^T once its
-//        Q/K have landed; warps 4-7 take chunk g+1's L2 norms, gate prefix
-//        and per-row factors;
+//        the bf16 operands Tb and Tbg), then thread 0 issues W^T and U^T
+//        once V has landed and the consumer has read chunk g-1's W; beside
+//        them warps 4-7 load chunk g+1's g and beta, take jobs / fill chunk
+//        infos three chunks ahead, issue chunk g+1's [rows] K^T once its Q/K
+//        have landed (thread 224) and take its L2 norms, gate prefix and
+//        per-row factors;
 //   consumer (warps 8-15), chunk g: writes the previous chunk's output
 //     (staged for 16-byte stores; the gated-norm epilogue in the layer
 //     instantiation), forms -Q~ in place and the K~ copy, moves W^T out of
@@ -125,7 +126,7 @@ struct JobRec {
 };
 constexpr int kRing = 8;  // jobs in flight per CTA: at most about 5 are live at once
 
-// What the roles need of one chunk of the stream, filled two chunks ahead
+// What the roles need of one chunk of the stream, filled three chunks ahead
 // (entry gq & 7 holds chunk gq; it is overwritten when chunk gq + 8 is filled,
 // by which time both roles are past chunk gq).  eglast is written by the
 // producer's gate prefix of the chunk, a chunk ahead of the consumer.
@@ -163,6 +164,7 @@ struct SmemWS {
     int factored;                  // the split factors stay well inside fp32 range
     uint64_t mbar_p, mbar_s, mbar_o;  // tensor-core completion: Gram; chain products; output products
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
+    uint64_t afree[2];             // per A slot: the chunk's output products are done (A may be rewritten)
     uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
     uint64_t fin_p, fin_s, fin_s2, fin_g;  // end-of-kernel drains of the issuing threads' products
     int qk_issued[2], qk_waited[2], v_issued, v_waited;
@@ -756,8 +758,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             sm.lpt_b[0] = bx;
             sm.lpt_b[1] = by;
             sm.lpt_b[2] = bz;
-            sm.acq_ok = acquire_jobs(p, src, sm, 2) ? 1 : 0;  // the first chunks of the stream
-            for (int gq = 0; gq < 2 && gq < sm.chunks; ++gq) fill_chunk_info(sm, gq);
+            sm.acq_ok = acquire_jobs(p, src, sm, 3) ? 1 : 0;  // the first chunks of the stream
+            for (int gq = 0; gq < 3 && gq < sm.chunks; ++gq) fill_chunk_info(sm, gq);
         }
         __syncthreads();
         if (sm.jn == 0) {  // no work for this CTA
@@ -779,6 +781,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::mbar_init(&sm.full[0], 2);  // the W/U products' commit and a producer thread
         tc::mbar_init(&sm.full[1], 2);
         tc::mbar_init(&sm.wfree, 1);
+        tc::mbar_init(&sm.afree[0], 1);
+        tc::mbar_init(&sm.afree[1], 1);
         tc::mbar_init(&sm.ld_qk[0], 1);
         tc::mbar_init(&sm.ld_qk[1], 1);
         tc::mbar_init(&sm.ld_v, 1);
@@ -823,7 +827,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
 
     // The CTA's chunks form one stream over its jobs, indexed by gq; every
     // barrier phase and slot follows gq.  Chunk gq is in the stream once
-    // gq < chunks; the producer keeps the stream (and the chunk infos) two
+    // gq < chunks; the producer keeps the stream (and the chunk infos) three
     // chunks ahead of the chunk it works on.
     auto stream_len = [&]() -> int { return *reinterpret_cast<volatile int*>(&sm.chunks); };
 
@@ -920,6 +924,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (gt == 32) GDN_STAMP(g, 0);
                 bool a = pend;
                 if (gt == 32) a = a && tc::mbar_wait(&sm.mbar_p, ph, kSpin, &sm.abort);
+                // A of chunk g replaces that of chunk g - 2 in its slot: that chunk's
+                // output products must have read it
+                if (gt == 32 && g >= 2) a = a && tc::mbar_wait(&sm.afree[s], ((g >> 1) - 1) & 1, kSpin, &sm.abort);
                 a = tc::bar_and(BAR_Q, GS - 32, a);
                 tc::fence_after();
                 if (gt == 32) GDN_STAMP(g, 1);
@@ -944,64 +951,69 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             if (!(ok = tc::bar_and(BAR_P, GS, pend))) break;
             tc::fence_after();
             if (gt == 0) GDN_STAMP(g, 3);
-            // ---- B: the UT inverse (warps 0-3, straight into Tb and Tbg); warps
-            // 4-7: the next chunk's g / beta, and (thread 128) the stream two
-            // chunks ahead
+            // ---- B: the UT inverse (warps 0-3, straight into Tb and Tbg), then
+            // W/U; warps 4-7: the next chunk's g / beta, (thread 128) the stream
+            // three chunks ahead (the consumer reads chunk g + 2's info once
+            // chunk g's W/U are done), and the next chunk's Gram and factors
             bool nok = true;
             if (gt < 128) {
                 ut_inverse_tb(sm.LT, sm.Tb, sm.Tbg, sm.slot[s].beta, sm.slot[s].fbg, gt,
                               [] { tc::bar_sync(BAR_PA, 128); }, g);
                 if (gt == 0) GDN_STAMP(g, 4);
+                // thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T as soon as the inverse
+                // is written, once V has landed and the consumer has read the previous W
+                tc::fence_async_smem();
+                tc::bar_sync(BAR_PA, 128);
+                if (gt == 0) {
+                    bool w = true;
+                    if (!vz) {
+                        w = tc::mbar_wait(&sm.ld_v, nvw & 1, kSpin, &sm.abort);
+                        nvw += 1;
+                    }
+                    if (w && g >= 1) w = tc::mbar_wait(&sm.wfree, (g - 1) & 1, kSpin, &sm.abort);
+                    GDN_STAMP(g, 9);
+                    if (w) {
+                        if (!vz) sm.v_waited += 1;
+                        tc::fence_after();
+                        const uint32_t T_U = s ? T_VN1 : T_VN0;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            tc::mma(T_W, dKmn0 + krows(s) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                            if (!vz) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
+                        }
+                        tc::commit(&sm.full[s]);
+                        tc::mbar_arrive(&sm.full[s]);
+                    }
+                    GDN_STAMP(g, 10);
+                    pend = w;
+                }
             } else {
                 if (g + 1 < len) load_gb(g + 1);
                 if (gt == 128) {
                     GDN_STAMP(g, 5);
-                    // the job of chunk g + 2, taken no earlier than the pipeline needs
-                    // it (the consumer loads that chunk's Q/K during chunk g; out of
-                    // line, once per job), and that chunk's info
-                    if (!sm.src_end && sm.chunks < g + 3) nok = acquire_jobs(p, src, sm, g + 3);
-                    if (g + 2 < sm.chunks) fill_chunk_info(sm, g + 2);
+                    // the job of chunk g + 3, taken no earlier than the pipeline needs
+                    // it (the consumer loads chunk g + 2's Q/K as soon as chunk g's
+                    // W/U are done, which may be before this role's next barrier; out
+                    // of line, once per job), and that chunk's info
+                    if (!sm.src_end && sm.chunks < g + 4) nok = acquire_jobs(p, src, sm, g + 4);
+                    if (g + 3 < sm.chunks) fill_chunk_info(sm, g + 3);
+                }
+                if (g + 1 < len) {
+                    // beside the inverse: the next chunk's [rows] K^T once its Q/K
+                    // have landed (this role has read this chunk's columns), its
+                    // norms, gate prefix and factors
+                    if (gt == 224) nok = issue_gram(g + 1);
+                    bool in = norms(g + 1);
+                    if (gt == 128) GDN_STAMP(g, 6);
+                    in = prep(g + 1, in);
+                    if (gt == 128) GDN_STAMP(g, 7);
+                    nok = nok && in;
                 }
             }
             tc::fence_async_smem();
             if (!(ok = tc::bar_and(BAR_P, GS, nok))) break;
             len = stream_len();
             if (gt == 0) GDN_STAMP(g, 8);
-            // ---- C: thread 0: W^T = K^T Tbg^T, U^T = V^T Tb^T once V has landed
-            // and the consumer has read the previous W; warps 4-7 meanwhile: the
-            // next chunk's norms (once its Q/K land), gate prefix and factors
-            if (gt == 0) {
-                bool w = true;
-                if (!vz) {
-                    w = tc::mbar_wait(&sm.ld_v, nvw & 1, kSpin, &sm.abort);
-                    nvw += 1;
-                }
-                if (w && g >= 1) w = tc::mbar_wait(&sm.wfree, (g - 1) & 1, kSpin, &sm.abort);
-                GDN_STAMP(g, 9);
-                if (w) {
-                    if (!vz) sm.v_waited += 1;
-                    tc::fence_after();
-                    const uint32_t T_U = s ? T_VN1 : T_VN0;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        tc::mma(T_W, dKmn0 + krows(s) + tc::mnoff(kk), dTbg + tc::koff(64, kk), ID_N64_AMN, kk > 0);
-                        if (!vz) tc::mma(T_U, dVmn + tc::mnoff(kk), dTb + tc::koff(64, kk), ID_N64_AMN, kk > 0);
-                    }
-                    tc::commit(&sm.full[s]);
-                    tc::mbar_arrive(&sm.full[s]);
-                }
-                GDN_STAMP(g, 10);
-                pend = w;
-            } else if (gt == 32 && g + 1 < len) {
-                // the next chunk's [rows] K^T once its Q/K have landed (this
-                // role has read this chunk's columns)
-                pend = issue_gram(g + 1);
-            } else if (gt >= 128 && g + 1 < len) {
-                bool in = norms(g + 1);
-                if (gt == 128) GDN_STAMP(g, 6);
-                pend = prep(g + 1, in);
-                if (gt == 128) GDN_STAMP(g, 7);
-            }
         }
         if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
         if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
@@ -1220,6 +1232,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                             tc::mma_ta(T_O, T_VNs + 32 * (kk >> 1) + 8 * (kk & 1), dAs + tc::koff(64, kk), ID_N64, 1u);
                     }
                     tc::commit(&sm.mbar_o);
+                    tc::commit(&sm.afree[s]);
                     GDN_STAMP(g, 24);
                 }
                 // while it runs: -Q~ / K~ and W of chunk g + 1, if its products are
