@@ -7,7 +7,7 @@ import torch
 
 import workloads as W
 
-# spec parity bars
+# parity bars: relative L2 of o and h_final, max-abs on L2-normalised q/k
 TOL_REL_L2 = {"bf16": 1e-2, "f32": 1e-4}
 TOL_MAX_ABS = 2e-2
 

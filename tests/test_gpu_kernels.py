@@ -1,7 +1,7 @@
 """GPU parity of each entry point against the fp64 oracle (through the C ABI).
 
 plan: bit-exact.  Floats: relative L2 <= 1e-2 (bf16) / 1e-4 (fp32) and
-max-abs <= 2e-2, the spec bars.  Sizes span several 64-token chunks
+max-abs <= 2e-2 (the stated parity bars).  Sizes span several 64-token chunks
 with ragged tails, empty sequences and every supported head size.
 """
 import json
