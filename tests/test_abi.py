@@ -117,3 +117,45 @@ def test_conv_host_errors(lib):
     assert call(K=0) == 2
     assert call(hl=3) == 1            # halo_len > 0 without a halo pointer
     assert call(hl=4, halo=FAKE) == 1  # halo_len > conv_k - 1
+
+
+def test_backward_host_errors(lib):
+    """gdn_chunk_bwd and gdn_shard_bwd reject bad arguments on the host (before
+    any launch) with the documented status codes; their workspace queries
+    return 0 for unsupported shapes."""
+    assert lib.gdn_chunk_bwd_workspace_size(64, 1, 1, 1, 48, 64) == 0
+    assert lib.gdn_chunk_bwd_workspace_size(64, 0, 1, 1, 32, 32) == 0
+    assert lib.gdn_shard_bwd_workspace_size(64, 1, 2, 1, 1, 32, 96) == 0
+    need = lib.gdn_chunk_bwd_workspace_size(64, 1, 2, 2, 32, 32)
+    assert need > 0 and need % 256 == 0
+
+    def chunk(**kw):
+        a = dict(q=FAKE, ldq=64, dt=1, T=64, N=1, Hk=2, Hv=2, dk=32, dv=32, flags=0, cu=FAKE, dh0=FAKE,
+                 ws=FAKE, ws_bytes=need)
+        a.update(kw)
+        return lib.gdn_chunk_bwd(a["q"], FAKE, FAKE, a["ldq"], 64, 64, a["dt"], FAKE, FAKE, None, FAKE, None,
+                                 a["cu"], a["N"], a["T"], a["Hk"], a["Hv"], a["dk"], a["dv"], 0.1, a["flags"],
+                                 FAKE, FAKE, FAKE, FAKE, FAKE, a["dh0"], a["ws"], a["ws_bytes"], None)
+    assert chunk(dk=48) == 2                        # unsupported head size
+    assert chunk(dt=7) == 3                         # dtype
+    assert chunk(N=0) == 1
+    assert chunk(cu=None) == 1 and chunk(dh0=None) == 1
+    assert chunk(flags=4) == 1                      # unknown flag bit
+    assert chunk(ws_bytes=need - 1) == 9            # workspace too small
+    assert chunk(ws=ctypes.c_void_p(4096 + 16)) == 9  # workspace not 256-byte aligned
+    assert chunk(ldq=60) == 1                       # q row stride below Hk * dk
+    assert chunk(q=ctypes.c_void_p(4104)) == 1      # q misaligned
+
+    sneed = lib.gdn_shard_bwd_workspace_size(64, 1, 2, 2, 2, 32, 32)
+    assert sneed > 0
+
+    def shard(**kw):
+        a = dict(T=64, P=2, ws=FAKE, ws_bytes=sneed, flags=0)
+        a.update(kw)
+        return lib.gdn_shard_bwd(FAKE, FAKE, FAKE, 64, 64, 64, 1, FAKE, FAKE, None, FAKE, None, FAKE, 1, a["T"],
+                                 2, 2, 32, 32, 0.1, a["flags"], a["P"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 a["ws"], a["ws_bytes"], None, None)
+    assert shard(T=63) == 4                         # not a multiple of n_shards
+    assert shard(P=0) == 1
+    assert shard(flags=4) == 1
+    assert shard(ws_bytes=sneed - 1) == 9
