@@ -431,6 +431,24 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = float(t.item())
     h2d = xh.numel() * xh.element_size() + gh.numel() * 4 + bh.numel() * bh.element_size() + cuh.numel() * 4
     d2h = oh.numel() * oh.element_size() + hfh.numel() * 4
+    # the host link's own rate: one plain pinned-to-device copy of a slice of
+    # the input, so that the end-to-end figure can be read against it
+    link_n = min(xh.numel(), (1 << 30) // xh.element_size())
+    link_dst = torch.empty(link_n, dtype=xh.dtype, device=dev)
+    link_src = xh.view(-1)[:link_n]
+    for _ in range(2):
+        link_dst.copy_(link_src, non_blocking=True)
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            link_dst.copy_(link_src, non_blocking=True)
+    l1.record(stream)
+    l1.synchronize()
+    link_gbps = 3 * link_n * xh.element_size() / (l0.elapsed_time(l1) * 1e6)
+    del link_dst
+    e2e_gbps = (h2d + d2h) / (e2e_ms * 1e6)
 
     # ---- per-phase times of the same step (events between its kernels) ----
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
@@ -494,7 +512,8 @@ def run_ours(args, rank, world, local_rank):
             "dtype": w.dtype, "data": "synthetic (seeded counter-based generator; no dataset)",
             "config": config_dict(w),
             "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "host_GBps": e2e_gbps, "host_link_GBps": link_gbps},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roof,
             "kernels": {"plan_conv_ms": conv_ms, "pass1_ms": pass1_ms, "combine_ms": combine_ms,
