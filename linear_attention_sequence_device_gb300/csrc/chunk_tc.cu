@@ -166,7 +166,7 @@ struct SmemWS {
     uint64_t full[2], wfree;       // chunk ready for the consumer; W columns read
     uint64_t afree[2];             // per A slot: the chunk's output products are done (A may be rewritten)
     uint64_t ld_qk[2], ld_v;       // TMA arrivals (transaction bytes)
-    uint64_t fin_p, fin_s, fin_s2, fin_g;  // end-of-kernel drains of the issuing threads' products
+    uint64_t fin_p, fin_s, fin_s2;  // end-of-kernel drains of the issuing threads' products
     int qk_issued[2], qk_waited[2], v_issued, v_waited;
     uint32_t tmem_slot;
     int lpt_len[kMaxLptItems];
@@ -789,7 +789,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         tc::mbar_init(&sm.fin_p, 1);
         tc::mbar_init(&sm.fin_s, 1);
         tc::mbar_init(&sm.fin_s2, 1);
-        tc::mbar_init(&sm.fin_g, 1);
         sm.qk_issued[0] = sm.qk_issued[1] = sm.qk_waited[0] = sm.qk_waited[1] = 0;
         sm.v_issued = sm.v_waited = 0;
     }
@@ -1017,8 +1016,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         }
         if (ok && !pend) ok = false;  // thread 0's last W/U issue (the consumer times out as well)
         if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
-        if (gt == 0 || gt == 32 || gt == 224) {  // every product these threads issued has completed
-            uint64_t* fb = gt == 0 ? &sm.fin_p : (gt == 32 ? &sm.fin_g : &sm.fin_s2);
+        if (gt == 0 || gt == 224) {  // every product these threads issued has completed
+            uint64_t* fb = gt == 0 ? &sm.fin_p : &sm.fin_s2;
             tc::commit(fb);
             tc::mbar_wait(fb, 0, kSpin);
         }
