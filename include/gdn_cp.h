@@ -292,7 +292,13 @@ gdn_status gdn_state_combine(const float *M, const float *N, const float *S0, in
  *   plan_out  device int32 [gdn_cp_plan_words(num_seqs, n_shards)] or NULL:
  *           receives a copy of the plan (incl. its status word)
  *   workspace device, >= gdn_shard_fwd_workspace_size(...) bytes, 256-byte
- *           aligned; its contents on entry do not matter
+ *           aligned; its contents on entry do not matter.  For bf16 with
+ *           dk = dv = 128 and n_shards > 1 that size includes room in which
+ *           the summaries' N halves store their chunks' W rows, K~ tiles and
+ *           e^{G_last} (about T * Hv * 512 bytes), so that the M halves run apart on
+ *           the tensor cores; a workspace down to
+ *           gdn_shard_fwd_workspace_min_size(...) bytes is accepted as well,
+ *           with the M halves run in the chunk kernel (same results, slower)
  * With n_shards == 1 this is the ordinary (unsharded) forward.  Checks on
  * the host: T % n_shards == 0 and T / n_shards >= conv_k - 1.  A malformed
  * cu_seqlens sets the plan status word and every later kernel returns
@@ -300,6 +306,10 @@ gdn_status gdn_state_combine(const float *M, const float *N, const float *S0, in
  * ---------------------------------------------------------------------- */
 size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
                                     int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype);
+/* the smallest workspace gdn_shard_fwd accepts (see its workspace argument);
+ * 0 for invalid arguments */
+size_t gdn_shard_fwd_workspace_min_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
+                                        int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype);
 
 gdn_status gdn_shard_fwd(const void *x, const void *conv_w, const void *conv_b, int32_t conv_k,
                          const float *g, const void *beta, const float *h0,
@@ -418,7 +428,7 @@ gdn_status gdn_shard_bwd(const void *q, const void *k, const void *v, int64_t ld
  * Same arguments and results as gdn_shard_fwd, minus the workspace.  The
  * scratch is one file-scope device array of GDN_NOALLOC_SCRATCH_BYTES
  * (32 MiB) that every device loading the library holds until the process
- * exits.  A problem whose gdn_shard_fwd_workspace_size(...) exceeds it is
+ * exits.  A problem whose gdn_shard_fwd_workspace_min_size(...) exceeds it is
  * rejected with GDN_ERR_WORKSPACE before anything is enqueued.  The entry
  * point never calls cudaMalloc/cudaFree or any allocating routine.
  *   - The first call on a device looks up the array's device address

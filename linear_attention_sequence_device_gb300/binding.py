@@ -61,6 +61,8 @@ SIGNATURES = {
     "gdn_state_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "gdn_shard_fwd_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                            ctypes.c_int]),
+    "gdn_shard_fwd_workspace_min_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                               ctypes.c_int]),
     "gdn_shard_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      _i32, _i32, _i32, _f32, _u32, _i32, ctypes.c_int, _vp, _sz,
                                      _vp, _vp, _vp, _vp]),
@@ -394,6 +396,11 @@ def gdn_state_combine(M, N, S0=None):
 
 def shard_fwd_workspace_size(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype) -> int:
     return int(load().gdn_shard_fwd_workspace_size(T, num_seqs, n_shards, Hk, Hv, dk, dv,
+                                                   GDN_BF16 if dtype == torch.bfloat16 else GDN_F32))
+
+
+def shard_fwd_workspace_min_size(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype) -> int:
+    return int(load().gdn_shard_fwd_workspace_min_size(T, num_seqs, n_shards, Hk, Hv, dk, dv,
                                                    GDN_BF16 if dtype == torch.bfloat16 else GDN_F32))
 
 

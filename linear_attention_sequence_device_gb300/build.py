@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdncp.so")
 SOURCES = ["api.cu", "plan.cu", "conv.cu", "chunk_bf16.cu", "chunk_f32.cu", "chunk_tc.cu", "schedule.cu",
-           "combine.cu", "noalloc.cu", "layout.cu", "backward.cu", "shard_bwd.cu"]
+           "combine.cu", "noalloc.cu", "layout.cu", "backward.cu", "shard_bwd.cu", "mchain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "-I", CSRC]

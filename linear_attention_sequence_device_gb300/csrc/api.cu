@@ -441,6 +441,24 @@ static size_t pass1_sched_bytes(int num_seqs, int P, int Hv, int dk, int dv, gdn
 
 size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
                                     int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
+    const size_t need = gdn::shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
+    if (need == 0) return 0;
+    const bool mk = gdn::mchain_eligible(dtype, dk, dv) && n_shards > 1 && T > 0;
+    return need + (mk ? gdn::mchain_scratch_bytes(T, n_shards, Hv) : 0);
+}
+
+size_t gdn_shard_fwd_workspace_min_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
+                                        int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
+    return gdn::shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
+}
+
+}  // extern "C"
+
+namespace gdn {
+// the workspace without the stored summary operands (the M chains then run in
+// the chunk kernel, as the M half of each summary)
+size_t shard_fwd_workspace_min(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk, int32_t Hv, int32_t dk,
+                               int32_t dv, gdn_dtype dtype) {
     if (T < 0 || num_seqs < 1 || n_shards < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
     const size_t cch = 2 * (size_t)Hk * dk + (size_t)Hv * dv;
     const size_t carry = (size_t)n_shards * Hv * dk;
@@ -450,10 +468,6 @@ size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shard
            align256(carry * dk * sizeof(float)) +      // carry M
            pass1_sched_bytes(num_seqs, n_shards, Hv, dk, dv, dtype);
 }
-
-}  // extern "C"
-
-namespace gdn {
 
 // The layer's extras around the path: gates from the raw projections and the
 // gated RMS norm of the output (null: gdn_shard_fwd's g / beta, plain o).
@@ -501,9 +515,14 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
     if (!al16(x) || !al16(o)) return fail(GDN_ERR_INVALID_ARG, "x and o must be 16-byte aligned");
     if (h_final && (reinterpret_cast<uintptr_t>(h_final) & 7u))
         return fail(GDN_ERR_INVALID_ARG, "h_final must be 8-byte aligned");
-    const size_t need = gdn_shard_fwd_workspace_size(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
+    const size_t need = shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
     if (!workspace || workspace_bytes < need)
         return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace_bytes, need);
+    // with room for the stored summary operands, the M chains run apart
+    const size_t mk_bytes =
+        mchain_eligible(dtype, dk, dv) && n_shards > 1 ? mchain_scratch_bytes(T, n_shards, Hv) : 0;
+    const bool use_mk = mk_bytes > 0 && workspace_bytes >= need + mk_bytes &&
+                        (int64_t)n_shards * Hv * ((T / n_shards + 63) / 64) * 64 < ((int64_t)1 << 31);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
@@ -523,6 +542,7 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
     float* carryM = reinterpret_cast<float*>(ws);
     ws += align256(carry * dk * sizeof(float));
     int32_t* sched = reinterpret_cast<int32_t*>(ws);
+    char* mk = static_cast<char*>(workspace) + need;  // stored summary operands (use_mk)
 
     auto mark = [&](int i) {
         if (i < g_phase_n) cudaEventRecord(g_phase_events[i], s);
@@ -556,9 +576,25 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
     set_token_major(p);
     {
         if (chunk_tc_eligible(dtype, dk, dv)) p.sched = sched;  // filled by the order kernel
+        if (use_mk) {
+            const int nch = (T / P + 63) / 64;
+            const size_t chunks = (size_t)P * Hv * nch, tile = chunks * 64 * 128 * es;
+            p.m_external = 1;
+            p.wk_nch = nch;
+            p.wk_w = mk;
+            p.wk_kt = mk + align256(tile);
+            p.wk_eg = reinterpret_cast<float*>(mk + 2 * align256(tile));
+        }
         dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
         p.sched = nullptr;
+        if (use_mk) {  // the M halves of the summaries, from the operands the N halves stored
+            if ((st = launch_mchain(plan, num_seqs, T, P, Hv, p.wk_w, p.wk_kt, p.wk_eg, carryM, s)) != GDN_OK)
+                return st;
+            p.m_external = 0;
+            p.wk_w = p.wk_kt = nullptr;
+            p.wk_eg = nullptr;
+        }
     }
     mark(2);
     if (P > 1) {

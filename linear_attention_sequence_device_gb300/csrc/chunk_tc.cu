@@ -100,6 +100,7 @@ typedef __nv_bfloat16 bf16;
 
 struct TmaMaps {
     CUtensorMap q, k, v;  // [T rows x heads*128 columns] bf16 views, 64x64 boxes, 128-byte swizzle
+    CUtensorMap wst, kst;  // stored W rows / K~ of spanning shards' chunks (same boxes), when the M chains run apart
 };
 
 // Per-slot values that only the producer reads (written a chunk ahead).
@@ -120,6 +121,7 @@ struct JobRec {
     int hv, hk, col0;
     int write_o, value_zero, identity_init;
     int part, flag;    // split half (0 whole, 1 first, 2 second); hand-over flag index
+    int wk_base;       // >= 0: store the chunks' W rows, K~ and e^{G_last} from this slot on
     const float* init;
     float* fin;
     int64_t init_ld, fin_ld;
@@ -483,6 +485,7 @@ __device__ __noinline__ bool acquire_jobs(const ChunkParams& p, int src, SmemWS&
         J.fin = job.fin;
         J.init_ld = job.init_ld;
         J.fin_ld = job.fin_ld;
+        J.wk_base = job.wk_base;
         __threadfence_block();
         *reinterpret_cast<volatile unsigned long long*>(&J.span) =
             ((unsigned long long)(unsigned)nch << 32) | (unsigned)sm.chunks;  // {first chunk, chunks}
@@ -1180,6 +1183,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     GDN_STAMP(g, 19);
                     if (w_now) tc::mbar_arrive(&sm.wfree);  // the W columns are free for the next W product
                     tc::fence_after();
+                    if (J.wk_base >= 0) {
+                        // the M chain of this summary runs apart: this chunk's W rows,
+                        // K~ tile and e^{G_last}, exactly as the products read them
+                        const int y = (J.wk_base + c) * 64;
+                        const bf16* wsrc = sm.QK[s] + (s ? 64 * 64 : 0);
+                        tc::tma_store_2d(&maps.wst, 0, y, wsrc);
+                        tc::tma_store_2d(&maps.wst, 64, y, wsrc + 128 * 64);
+                        tc::tma_store_2d(&maps.kst, 0, y, sm.KT[s]);
+                        tc::tma_store_2d(&maps.kst, 64, y, sm.KT[s] + 64 * 64);
+                        tc::bulk_commit();
+                        p.wk_eg[J.wk_base + c] = I.eglast;
+                    }
                     // [v_new^T | o^T] = [U^T | 0] - S^T [W ; -Q~]^T (slot 0; slot 1 the
                     // other row order), S^T bf16 from tensor memory
                     if (I.write_o) {
@@ -1201,6 +1216,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (gt == 0) GDN_STAMP(g, 22);
                 // the first product was the last reader of the slot's Q/K tile:
                 // refill it with the Q/K of chunk g + 2
+                if (gt == 0 && J.wk_base >= 0) tc::bulk_wait_read();  // the stores have read the slot and K~
                 if (gt == 0 && g + 2 < len) issue_qk(g + 2, sm.ci[(g + 2) & 7].tb, sm.ci[(g + 2) & 7].hk);
                 {  // v_new^T as bf16 pairs in place (this thread's own columns), the
                    // A operand of the updates
@@ -1312,9 +1328,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
             }
         }
         if (!ok && gt == 0) *reinterpret_cast<volatile int*>(&sm.abort) = 1;
-        if (tid == GS) {  // every product this thread issued has completed
+        if (tid == GS) {  // every product and store this thread issued has completed
             tc::commit(&sm.fin_s);
             tc::mbar_wait(&sm.fin_s, 0, kSpin);
+            tc::bulk_wait();
         }
     }
     if (!ok && gt == 0) {
@@ -1358,6 +1375,10 @@ static EncodeTiledFn encode_tiled() {
 
 // [rows x cols] bf16 view with row stride ld (elements), 64x64 boxes, 128B swizzle;
 // rows past the end read as zero.
+static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t cols, int64_t rows);
+gdn_status make_map_bf16(CUtensorMap* m, const void* base, int64_t ld, int64_t cols, int64_t rows) {
+    return make_map(m, base, ld, cols, rows);
+}
 static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t cols, int64_t rows) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -1391,6 +1412,11 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         if ((st = make_map(&maps.q, p.q, 128, 128, (int64_t)p.Hk * p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.k, p.k, 128, 128, (int64_t)p.Hk * p.T)) != GDN_OK) return st;
         if ((st = make_map(&maps.v, p.v, 128, 128, (int64_t)p.Hv * p.T)) != GDN_OK) return st;
+    }
+    if (p.m_external && p.wk_w && p.wk_kt) {  // stored W rows / K~: [P * Hv * wk_nch * 64 rows x 128]
+        const int64_t rows = (int64_t)p.n_shards * p.Hv * p.wk_nch * 64;
+        if ((st = make_map(&maps.wst, p.wk_w, 128, 128, rows)) != GDN_OK) return st;
+        if ((st = make_map(&maps.kst, p.wk_kt, 128, 128, rows)) != GDN_OK) return st;
     }
     if (p.sched && grid.x > (unsigned)kMaxLptItems) p.sched = nullptr;  // beyond the order kernel's scratch
     if (!p.status && p.sched) p.status = p.sched + 2;  // the work queue's status word

@@ -57,6 +57,7 @@ struct ChunkJob {
     bool identity_init;    // M part of a summary: start from identity columns
     bool value_zero;       // M part of a summary: value columns are zero
     bool write_o;
+    int wk_base;           // >= 0: the job stores its chunks' W rows, K~ and e^{G_last} from this chunk slot on
 };
 
 // Where a chunk kernel gets its jobs from.
@@ -117,6 +118,16 @@ struct ChunkParams {
     int64_t ldz;
     const void* norm_w;
     float norm_eps;
+    // shard pass 1 with the M chains run apart (tensor-core kernel, bf16
+    // d = 128): the N job of every spanning shard r stores, per chunk c of the
+    // shard, its bf16 W rows and K~ tile ([slot * 64 rows x 128], slot =
+    // (r * Hv + hv) * wk_nch + c) and e^{G_last} (wk_eg[slot]); the M jobs
+    // are not run here
+    void* wk_w;
+    void* wk_kt;
+    float* wk_eg;
+    int wk_nch;
+    int m_external;
 };
 
 // Token-major head strides (the layout every entry point but the head-major
@@ -157,6 +168,7 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
     j.hv = hv;
     j.identity_init = false;
     j.value_zero = false;
+    j.wk_base = -1;
     j.init = nullptr;
     j.fin = nullptr;
     j.init_ld = p.dv;
@@ -241,7 +253,9 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
         if (z < nvt) {
             j.col0 = z * p.col_tile;
             j.fin = p.sumN + carry_st + j.col0;
+            if (p.m_external) j.wk_base = ((int)r * p.Hv + hv) * p.wk_nch;
         } else {
+            if (p.m_external) return false;  // the M chain runs apart, from the stored operands
             j.col0 = (z - nvt) * p.col_tile;
             j.identity_init = true;
             j.value_zero = true;
@@ -349,6 +363,16 @@ gdn_status launch_chunk_f32(const ChunkParams& p, int src, dim3 grid, cudaStream
 // tcgen05 kernel (chunk_tc.cu): bf16 with d_k = d_v = 128, full-width state tiles
 bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv);
 gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s);
+// the M chains of the shard summaries run apart from their stored operands
+// (csrc/mchain.cu): scratch bytes of the stored W rows, K~ and e^{G_last}
+// (0 for P < 2), and the launch over the plan's spanning shards into M [P, Hv, 128, 128]
+bool mchain_eligible(gdn_dtype dt, int dk, int dv);
+// gdn_shard_fwd's workspace without the stored summary operands
+size_t shard_fwd_workspace_min(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk, int32_t Hv, int32_t dk,
+                               int32_t dv, gdn_dtype dtype);
+size_t mchain_scratch_bytes(int T, int P, int Hv);
+gdn_status launch_mchain(const int32_t* plan, int num_seqs, int T, int P, int Hv, void* w, void* kt,
+                         const float* eg, float* M, cudaStream_t s);
 extern __device__ int g_gdn_timeouts;
 int chunk_col_tile(gdn_dtype dt, int dk, int dv);
 

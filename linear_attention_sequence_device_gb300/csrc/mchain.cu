@@ -1,0 +1,258 @@
+// The M chain of the shard summaries on the tensor cores (hyper-parallel page
+// linear_attention_context_parallel.py: _compute_gdn_state_summary_from_prepared,
+// the transition product M <- M_i M with M_i = e^{G_C} I - Kd^T W).
+//
+// In shard pass 1 the N job of every spanning shard stores, per chunk, the
+// bf16 W rows and K~ tile it built for its own chain, and e^{G_last}.  The M
+// chain of the same shard needs exactly those operands and no value input, so
+// this kernel runs it on its own, from the identity, with the chunk kernel's
+// products and state handling (M comes out as the chunk kernel's M job would
+// give it):
+//   v_new^T = -S^T W^T,   S^T <- e^{G_last} S^T + v_new^T K~.
+// One CTA of 128 threads per (shard, value head); thread = tensor-memory lane
+// = row of S^T.  It holds 256 tensor-memory columns, so two CTAs share an SM
+// and their chains interleave.  The next chunk's W / K~ load (TMA) while the
+// current one runs.  Every wait is bounded: on expiry the kernel counts a
+// timeout, writes GDN_ERR_TIMEOUT to the plan's status word and leaves.
+#include <cuda.h>
+#include <string.h>
+
+#include "gdn_internal.cuh"
+#include "tc_util.cuh"
+
+namespace gdn {
+
+extern __device__ int g_gdn_timeouts;
+gdn_status make_map_bf16(CUtensorMap* m, const void* base, int64_t ld, int64_t cols, int64_t rows);
+gdn_status set_smem_attr(const void* func, size_t bytes);
+
+namespace {
+
+constexpr int MT = 128;
+inline size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr uint32_t kMSpin = 1u << 20;
+constexpr int BAR_M = 1;
+typedef __nv_bfloat16 bf16;
+
+struct MMaps {
+    CUtensorMap w, kt;  // [chunks * 64 rows x 128 columns] bf16, 64x64 boxes, 128-byte swizzle
+};
+
+struct MParams {
+    const int32_t* plan;
+    int num_seqs, P, Hv, nch;  // nch: chunks of a shard
+    const float* eg;            // e^{G_last} of every stored chunk
+    float* M;                   // [P, Hv, 128, 128]: M of shard r at r
+};
+
+struct MSmem {
+    bf16 W[2][64 * 128];   // per stage: W rows [token][key], K-major (two 64-key atoms)
+    bf16 KT[2][64 * 128];  // per stage: K~ [token][key], MN-major (two 64-key atoms)
+    uint64_t ld[2];        // TMA arrivals
+    uint64_t mma;          // product completions
+    uint64_t fin;
+    int issued[2], waited[2];
+    uint32_t tmem_slot;
+};
+
+constexpr uint32_t ID_N64_NEG = tc::idesc_bf16(128, 64, false, false, false) | (1u << 14);
+constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
+
+__global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __grid_constant__ MMaps maps) {
+    extern __shared__ unsigned char smem_raw[];
+    MSmem& sm = *reinterpret_cast<MSmem*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
+    const int r = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    if (__ldg(p.plan) != 0) return;  // malformed cu_seqlens: nothing to do
+    // a spanning shard: one local segment, continued from and into its neighbours
+    const int32_t* rec = p.plan + 1 + (int64_t)r * GDN_PLAN_NFIELDS;
+    if (!(__ldg(rec + GDN_PLAN_LOCAL_NUM_SEQS) == 1 && !__ldg(rec + GDN_PLAN_IS_FIRST_RANK) &&
+          __ldg(rec + GDN_PLAN_POST_NUM_RANKS) > 0))
+        return;
+    const int nch = p.nch;
+    const int64_t item = (int64_t)r * p.Hv + hv;
+    const int y0 = (int)(item * nch * 64);  // first stored row of this shard's chunks
+    const float* eg = p.eg + item * nch;
+
+    if (tid == 0) {
+        tc::mbar_init(&sm.ld[0], 1);
+        tc::mbar_init(&sm.ld[1], 1);
+        tc::mbar_init(&sm.mma, 1);
+        tc::mbar_init(&sm.fin, 1);
+        sm.issued[0] = sm.issued[1] = sm.waited[0] = sm.waited[1] = 0;
+    }
+    tc::fence_async_smem();
+    if (warp == 0) tc::tmem_alloc(&sm.tmem_slot, 256);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = sm.tmem_slot;
+    // columns: fp32 S^T | bf16 S^T (two keys per column) | v_new (fp32, then bf16 pairs in place)
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const uint32_t T_S = tmem + lb, T_SB = tmem + 128 + lb, T_VN = tmem + 192 + lb;
+    const int row = tid;  // tensor-memory lane = row of S^T
+
+    auto issue_load = [&](int c) {  // W rows and K~ of chunk c into stage c & 1 (thread 0)
+        const int st = c & 1, y = y0 + 64 * c;
+        tc::mbar_expect_tx(&sm.ld[st], 4 * 64 * 64 * 2);
+        tc::tma_load_2d(sm.W[st], &maps.w, 0, y, &sm.ld[st]);
+        tc::tma_load_2d(sm.W[st] + 64 * 64, &maps.w, 64, y, &sm.ld[st]);
+        tc::tma_load_2d(sm.KT[st], &maps.kt, 0, y, &sm.ld[st]);
+        tc::tma_load_2d(sm.KT[st] + 64 * 64, &maps.kt, 64, y, &sm.ld[st]);
+        sm.issued[st] += 1;
+    };
+    if (tid == 0) {
+        issue_load(0);
+        if (nch > 1) issue_load(1);
+    }
+    // the identity, as bf16 (the first product's A operand) and scaled by the
+    // first chunk's e^{G_last} (the first update accumulates onto it)
+    {
+        const float e0 = __ldg(eg);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h)
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float v[16];
+                uint32_t w[8];
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) v[c2] = (64 * h + 16 * q4 + c2 == row) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w[j] = tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                tc::stw8(T_SB + 32 * h + 8 * q4, w);
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) v[c2] *= e0;
+                tc::st16(T_S + 64 * h + 16 * q4, v);
+            }
+    }
+    const uint64_t dW0 = tc::desc(tc::smem_addr(sm.W[0]), 16, 1024);
+    const uint64_t dKT0 = tc::desc(tc::smem_addr(sm.KT[0]), 64 * 128, 1024);
+    constexpr uint64_t kStage = sizeof(bf16) * 64 * 128 / 16;  // descriptor start-address step of a stage
+    uint32_t ph = 0;
+    bool ok = true;
+    auto wait_mma = [&]() -> bool {
+        bool d = true;
+        if (tid == 0) d = tc::mbar_wait(&sm.mma, ph, kMSpin);
+        ph ^= 1u;
+        const bool all = tc::bar_and(BAR_M, MT, d);
+        tc::fence_after();
+        return all;
+    };
+    for (int c = 0; c < nch && ok; ++c) {
+        const int st = c & 1;
+        tc::st32_zero(T_VN);  // v_new = 0 - S^T W^T: the product accumulates onto zero
+        tc::st32_zero(T_VN + 32);
+        bool in = true;
+        if (tid == 0) {
+            in = tc::mbar_wait(&sm.ld[st], (c >> 1) & 1, kMSpin);
+            if (in) sm.waited[st] += 1;
+        }
+        tc::wait_st();
+        tc::fence_before();
+        if (!(ok = tc::bar_and(BAR_M, MT, in))) break;
+        if (tid == 0) {
+            tc::fence_after();
+            const uint64_t dW = dW0 + (st ? kStage : 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_ta(T_VN - lb, T_SB - lb + 8 * kk, dW + tc::koff(64, kk), ID_N64_NEG, 1u);
+            tc::commit(&sm.mma);
+        }
+        if (!(ok = wait_mma())) break;
+        // v_new^T as bf16 pairs in place (the second product's A operand)
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            float vv[32];
+            uint32_t w[16];
+            tc::ld32(T_VN + 32 * h, vv);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = tc::pack_bf16x2(vv[2 * j], vv[2 * j + 1]);
+            tc::stw16(T_VN + 32 * h, w);
+        }
+        tc::wait_st();
+        tc::fence_before();
+        tc::bar_sync(BAR_M, MT);
+        if (tid == 0) {
+            tc::fence_after();
+            const uint64_t dKT = dKT0 + (st ? kStage : 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_ta(T_S - lb, T_VN - lb + 32 * (kk >> 1) + 8 * (kk & 1), dKT + tc::mnoff(kk), ID_N128_BMN, 1u);
+            tc::commit(&sm.mma);
+        }
+        if (!(ok = wait_mma())) break;
+        if (tid == 0 && c + 2 < nch) issue_load(c + 2);  // both products of chunk c have read the stage
+        if (c + 1 < nch) {
+            // the new state: its bf16 copy, and the state scaled by the next
+            // chunk's e^{G_last}, back into tensor memory
+            const float egn = __ldg(eg + c + 1);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h)
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float sv[16];
+                    uint32_t w[8];
+                    tc::ld16(T_S + 64 * h + 16 * q4, sv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w[j] = tc::pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
+                    tc::stw8(T_SB + 32 * h + 8 * q4, w);
+#pragma unroll
+                    for (int c2 = 0; c2 < 16; ++c2) sv[c2] *= egn;
+                    tc::st16(T_S + 64 * h + 16 * q4, sv);
+                }
+        } else {
+            float* fin = p.M + item * 128 * 128;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h)
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float v[16];
+                    tc::ld16(T_S + 64 * h + 16 * q4, v);
+#pragma unroll
+                    for (int c2 = 0; c2 < 16; ++c2) fin[(int64_t)(64 * h + 16 * q4 + c2) * 128 + row] = v[c2];
+                }
+        }
+    }
+    if (!ok && tid == 0) {
+        atomicAdd(&g_gdn_timeouts, 1);
+        atomicCAS(const_cast<int32_t*>(p.plan), 0, (int)GDN_ERR_TIMEOUT);
+    }
+    if (tid == 0) {  // the products this thread issued and the loads still in flight are done
+        tc::commit(&sm.fin);
+        tc::mbar_wait(&sm.fin, 0, kMSpin);
+        for (int st = 0; st < 2; ++st)
+            if (sm.issued[st] > sm.waited[st]) tc::mbar_wait(&sm.ld[st], (sm.issued[st] - 1) & 1, kMSpin);
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+bool mchain_eligible(gdn_dtype dt, int dk, int dv) { return dt == GDN_BF16 && dk == 128 && dv == 128; }
+
+size_t mchain_scratch_bytes(int T, int P, int Hv) {
+    if (P < 2) return 0;
+    const size_t nch = ((size_t)(T / P) + 63) / 64;
+    const size_t chunks = (size_t)P * Hv * nch;
+    return 2 * al256(chunks * 64 * 128 * sizeof(bf16)) + al256(chunks * sizeof(float));
+}
+
+gdn_status launch_mchain(const int32_t* plan, int num_seqs, int T, int P, int Hv, void* w, void* kt,
+                         const float* eg, float* M, cudaStream_t s) {
+    if (P < 2 || T <= 0) return GDN_OK;
+    MParams p{};
+    p.plan = plan; p.num_seqs = num_seqs; p.P = P; p.Hv = Hv; p.nch = (T / P + 63) / 64;
+    p.eg = eg; p.M = M;
+    const int64_t rows = (int64_t)P * Hv * p.nch * 64;
+    MMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    gdn_status st;
+    if ((st = make_map_bf16(&maps.w, w, 128, 128, rows)) != GDN_OK) return st;
+    if ((st = make_map_bf16(&maps.kt, kt, 128, 128, rows)) != GDN_OK) return st;
+    const size_t smem = sizeof(MSmem) + 1024;
+    if ((st = set_smem_attr((const void*)mchain_kernel, smem)) != GDN_OK) return st;
+    mchain_kernel<<<dim3(P, Hv), MT, smem, s>>>(p, maps);
+    return check_launch("mchain_kernel");
+}
+
+}  // namespace gdn

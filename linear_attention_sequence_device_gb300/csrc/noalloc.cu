@@ -84,7 +84,7 @@ extern "C" gdn_status gdn_shard_fwd_noalloc(const void* x, const void* conv_w, c
                                             int32_t dk, int32_t dv, float scale, uint32_t flags,
                                             int32_t n_shards, gdn_dtype dtype, void* o,
                                             float* h_final, int32_t* plan_out, void* stream) {
-    const size_t need = gdn_shard_fwd_workspace_size(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
+    const size_t need = gdn::shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
     if (need == 0)
         return fail(GDN_ERR_INVALID_ARG, "invalid sizes (T=%d num_seqs=%d n_shards=%d)", T, num_seqs,
                     n_shards);

@@ -227,3 +227,27 @@ def test_full_size_sampled(name):
                 assert_close(og[sl], o_ref[sl], w.dtype, f"{name} o head {h} after boundary {r}")
     del d, o, hf
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,P,kw", [("long", 8, {}), ("long", 4, {"g_zero": True}), ("ragged", 16, {}),
+                                       ("million", 16, {})])
+def test_summary_m_chains_apart_are_bit_identical(name, P, kw):
+    """With the full workspace the summaries' M halves run in their own kernel
+    from the W rows, K~ tiles and e^{G_last} that the N halves stored; with the
+    minimum workspace they run in the chunk kernel.  Both compute the same
+    products on the same operands, so o and h_final agree bit for bit."""
+    import linear_attention_sequence_device_gb300 as g
+    w = reduced(name, n_shards=P, **kw)
+    _, d = path_inputs(w)
+    dt = torch.bfloat16
+    full = g.shard_fwd_workspace_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
+    small = g.shard_fwd_workspace_min_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
+    assert full > small > 0
+    g.binding.device_timeouts(reset=True)
+    o1, hf1, plan1 = run_gpu(w, d, P, workspace=torch.empty(full, dtype=torch.uint8, device=dev()))
+    o2, hf2, plan2 = run_gpu(w, d, P, workspace=torch.empty(small, dtype=torch.uint8, device=dev()))
+    torch.cuda.synchronize()
+    assert int(plan1[0]) == 0 and int(plan2[0]) == 0
+    assert torch.equal(o1, o2)
+    assert torch.equal(hf1, hf2)
+    assert g.binding.device_timeouts() == 0

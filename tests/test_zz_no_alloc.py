@@ -41,8 +41,8 @@ def _both(g, w):
 
 def test_noalloc_matches_workspace_path_two_calls(g):
     for w in (_case(21, 4), _case(22, 2), W.tiny()):
-        assert g.shard_fwd_workspace_size(w.T, w.N, w.n_shards, w.Hk, w.Hv, w.dk, w.dv,
-                                          torch.bfloat16 if w.dtype == "bf16" else torch.float32) \
+        assert g.shard_fwd_workspace_min_size(w.T, w.N, w.n_shards, w.Hk, w.Hv, w.dk, w.dv,
+                                              torch.bfloat16 if w.dtype == "bf16" else torch.float32) \
             <= g.NOALLOC_SCRATCH_BYTES
         o, hf, o_ref, hf_ref = _both(g, w)
         assert rel_l2(f64(o), f64(o_ref)) <= TOL_REL_L2[w.dtype], w.name
