@@ -521,7 +521,7 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
     // with room for the stored summary operands, the M chains run apart
     const size_t mk_bytes =
         mchain_eligible(dtype, dk, dv) && n_shards > 1 ? mchain_scratch_bytes(T, n_shards, Hv) : 0;
-    const bool use_mk = mk_bytes > 0 && workspace_bytes >= need + mk_bytes &&
+    const bool use_mk = mk_bytes > 0 && workspace_bytes >= need + mk_bytes && !(ex && ex->z) &&
                         (int64_t)n_shards * Hv * ((T / n_shards + 63) / 64) * 64 < ((int64_t)1 << 31);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");

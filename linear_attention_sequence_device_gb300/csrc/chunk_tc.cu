@@ -742,9 +742,11 @@ __device__ __forceinline__ void qk_prep_fn(SmemWS& sm, int gq, int c) {
     }
 }
 
-// GNORM: the gated RMS norm output epilogue (the layer entry point); a
-// separate instantiation, so that the plain forward keeps its registers.
-template <bool GNORM>
+// GNORM: the gated RMS norm output epilogue (the layer entry point); WKST:
+// summary jobs may store their chunks' W rows, K~ and e^{G_last} for the M
+// chains run apart (shard pass 1).  Separate instantiations, so that the plain
+// forward keeps its registers and code layout.
+template <bool GNORM, bool WKST>
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, const int src,
                                                         const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -1183,7 +1185,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                     GDN_STAMP(g, 19);
                     if (w_now) tc::mbar_arrive(&sm.wfree);  // the W columns are free for the next W product
                     tc::fence_after();
-                    if (J.wk_base >= 0) {
+                    if (WKST && J.wk_base >= 0) {
                         // the M chain of this summary runs apart: this chunk's W rows,
                         // K~ tile and e^{G_last}, exactly as the products read them
                         const int y = (J.wk_base + c) * 64;
@@ -1216,7 +1218,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
                 if (gt == 0) GDN_STAMP(g, 22);
                 // the first product was the last reader of the slot's Q/K tile:
                 // refill it with the Q/K of chunk g + 2
-                if (gt == 0 && J.wk_base >= 0) tc::bulk_wait_read();  // the stores have read the slot and K~
+                if (WKST && gt == 0 && J.wk_base >= 0) tc::bulk_wait_read();  // the stores have read the slot and K~
                 if (gt == 0 && g + 2 < len) issue_qk(g + 2, sm.ci[(g + 2) & 7].tb, sm.ci[(g + 2) & 7].hk);
                 {  // v_new^T as bf16 pairs in place (this thread's own columns), the
                    // A operand of the updates
@@ -1331,7 +1333,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(const ChunkParams p, co
         if (tid == GS) {  // every product and store this thread issued has completed
             tc::commit(&sm.fin_s);
             tc::mbar_wait(&sm.fin_s, 0, kSpin);
-            tc::bulk_wait();
+            if (WKST) tc::bulk_wait();
         }
     }
     if (!ok && gt == 0) {
@@ -1400,7 +1402,12 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
     p.handover_ns = g_handover_ns;
     p.no_publish = g_handover_publish ? 0 : 1;
     const size_t smem = sizeof(SmemWS) + 1024;
-    gdn_status st = set_smem_attr(p.z ? (const void*)chunk_tc_kernel<true> : (const void*)chunk_tc_kernel<false>, smem);
+    // three instantiations: the gated-norm epilogue (the layer), the stores of a
+    // summary's W rows / K~ for the M chains run apart (shard pass 1), and plain
+    const bool wkst = !p.z && p.m_external && p.wk_w && src == JOBS_SHARD_PASS1;
+    const void* fn = p.z ? (const void*)chunk_tc_kernel<true, false>
+                         : (wkst ? (const void*)chunk_tc_kernel<false, true> : (const void*)chunk_tc_kernel<false, false>);
+    gdn_status st = set_smem_attr(fn, smem);
     if (st != GDN_OK) return st;
     TmaMaps maps;
     memset(&maps, 0, sizeof(maps));
@@ -1436,8 +1443,9 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         const long long jobs = 2ll * p.sched_items * p.sched_m;
         grid = dim3((unsigned)(jobs < p.num_sms ? jobs : (p.num_sms > 0 ? p.num_sms : 1)), 1, 1);
     }
-    if (p.z) chunk_tc_kernel<true><<<grid, NT, smem, s>>>(p, src, maps);
-    else chunk_tc_kernel<false><<<grid, NT, smem, s>>>(p, src, maps);
+    if (p.z) chunk_tc_kernel<true, false><<<grid, NT, smem, s>>>(p, src, maps);
+    else if (wkst) chunk_tc_kernel<false, true><<<grid, NT, smem, s>>>(p, src, maps);
+    else chunk_tc_kernel<false, false><<<grid, NT, smem, s>>>(p, src, maps);
     return check_launch("chunk_tc_kernel");
 }
 
