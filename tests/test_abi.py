@@ -159,3 +159,20 @@ def test_backward_host_errors(lib):
     assert shard(P=0) == 1
     assert shard(flags=4) == 1
     assert shard(ws_bytes=sneed - 1) == 9
+
+
+def test_shard_fwd_workspace_sizes(lib):
+    """The full workspace adds room for the stored summary operands (bf16,
+    d = 128, P > 1: W rows, K~ tiles and e^{G_last} of every shard chunk);
+    otherwise it equals the minimum.  0 for invalid arguments."""
+    full = lambda *a: lib.gdn_shard_fwd_workspace_size(*a)
+    small = lambda *a: lib.gdn_shard_fwd_workspace_min_size(*a)
+    a = (131072, 1, 8, 16, 16, 128, 128, 1)            # bf16, d = 128, P = 8
+    extra = full(*a) - small(*a)
+    chunks = 8 * 16 * ((131072 // 8 + 63) // 64)
+    assert extra >= chunks * (2 * 64 * 128 * 2 + 4) and extra < chunks * (2 * 64 * 128 * 2 + 4) + 3 * 256
+    for b in ((131072, 1, 1, 16, 16, 128, 128, 1),     # one shard
+              (4096, 2, 4, 2, 2, 64, 64, 1),           # other head size
+              (4096, 2, 4, 2, 2, 128, 128, 0)):        # fp32
+        assert full(*b) == small(*b) > 0
+    assert full(0, 0, 1, 1, 1, 128, 128, 1) == 0 and small(0, 0, 1, 1, 1, 128, 128, 1) == 0
