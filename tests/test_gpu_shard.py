@@ -230,15 +230,18 @@ def test_full_size_sampled(name):
 
 
 @pytest.mark.parametrize("name,P,kw", [("long", 8, {}), ("long", 4, {"g_zero": True}), ("ragged", 16, {}),
-                                       ("million", 16, {})])
+                                       ("million", 16, {}), ("long_ragged_tail", 8, {})])
 def test_summary_m_chains_apart_are_bit_identical(name, P, kw):
     """With the full workspace the summaries' M halves run in their own kernel
     from the W rows, K~ tiles and e^{G_last} that the N halves stored; with the
     minimum workspace they run in the chunk kernel.  Both compute the same
     products on the same operands, so o and h_final agree bit for bit."""
     import linear_attention_sequence_device_gb300 as g
-    w = reduced(name, n_shards=P, **kw)
-    _, d = path_inputs(w)
+    if name == "long_ragged_tail":  # shards of 500 tokens: a partial last chunk in every shard
+        w = W.long_seq(T=4000, n_shards=P, h0_std=0.02)
+    else:
+        w = reduced(name, n_shards=P, **kw)
+    host, d = path_inputs(w)
     dt = torch.bfloat16
     full = g.shard_fwd_workspace_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
     small = g.shard_fwd_workspace_min_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
@@ -251,3 +254,7 @@ def test_summary_m_chains_apart_are_bit_identical(name, P, kw):
     assert torch.equal(o1, o2)
     assert torch.equal(hf1, hf2)
     assert g.binding.device_timeouts() == 0
+    if name == "long_ragged_tail":  # and the result is the oracle's
+        o_ref, hf_ref = oracle_path(w, host)
+        assert_close(f64(o1), o_ref, w.dtype, "o")
+        assert_close(f64(hf1), hf_ref, w.dtype, "h_final")
