@@ -259,13 +259,28 @@ gdn_status launch_tk(ConvParams p, dim3 grid, cudaStream_t s) {
     const size_t smem = (size_t)NSTAGE * RB * (sizeof(T) * 8 / 16) * NT * 16;
     gdn_status st = set_smem_attr((const void*)conv_kernel<T, KC>, smem);
     if (st != GDN_OK) return st;
-    // strips per shard: one wave of resident CTAs over (channel blocks x shards),
+    // strips per shard: the CTAs fill whole waves of resident slots (a partly
+    // filled last wave moves its bytes at a fraction of the bandwidth), with
     // strips of at least 64 rows so that the K-1 halo rows stay a small overhead
     const int part = p.T / p.P;
     const int slots = resident_slots<T, KC>(smem);
     const int per = (int)grid.x * p.P;
-    int n = slots > 0 ? max(1, slots / per) : (part + 127) / 128;
-    n = min(n, max(1, part / 64));
+    const int nmax = max(1, part / 64);
+    int n = (part + 127) / 128;
+    if (slots > 0) {
+        n = 1;
+        double best = 2.0;
+        for (int c = 1; c <= nmax && c <= 1024; ++c) {
+            const double waves = (double)per * c / slots, full = ceil(waves);
+            const double idle = (full - waves) / full;  // share of the launched waves' slots left idle
+            if (idle < best - 1e-9) {
+                best = idle;
+                n = c;
+            }
+            if (best < 0.02) break;
+        }
+    }
+    n = min(n, nmax);
     int rows = (part + n - 1) / n;
     p.rows = (rows + RB - 1) / RB * RB;
     grid.y = (part + p.rows - 1) / p.rows;
