@@ -98,6 +98,14 @@ gdn_status gdn_device_timeouts(int32_t *count, int reset);
    gdn_debug_set_handover(1000000000, 1).  Not for production use. */
 gdn_status gdn_debug_set_handover(int64_t wait_ns, int publish);
 
+/* Testing hook (no counterpart on the source pages): enable = 0 turns off the
+   splitting of work-queue items into two parts handed over through a final
+   state (single-segment launches: long items in halves; shard passes: short
+   tail parts), so that a test can compare split and unsplit runs, which give
+   bit-identical results.  enable = 1 (the default) restores it.  Applies to
+   launches made after the call from any thread.  Not for production use. */
+gdn_status gdn_debug_set_split(int32_t enable);
+
 /* Profiling hook (no counterpart on the source pages): while n > 0, every
    gdn_shard_fwd call on this host thread records events[i] (cudaEvent_t
    handles, created by the caller) on its stream: [0] at entry, [1] after the
@@ -296,9 +304,13 @@ gdn_status gdn_state_combine(const float *M, const float *N, const float *S0, in
  *           dk = dv = 128 and n_shards > 1 that size includes room in which
  *           the summaries' N halves store their chunks' W rows, K~ tiles and
  *           e^{G_last} (about T * Hv * 512 bytes), so that the M halves run apart on
- *           the tensor cores; a workspace down to
+ *           the tensor cores (with few long shards each M chain is cut into
+ *           up to 8 segments, whose fp32 products take n_shards * Hv * 64 KiB
+ *           per segment more); a workspace down to
  *           gdn_shard_fwd_workspace_min_size(...) bytes is accepted as well,
- *           with the M halves run in the chunk kernel (same results, slower)
+ *           with the M halves run in the chunk kernel (the same results up to
+ *           rounding; bit for bit where the chains are not cut; slower).  The
+ *           size depends on the current device's SM count.
  * With n_shards == 1 this is the ordinary (unsharded) forward.  Checks on
  * the host: T % n_shards == 0 and T / n_shards >= conv_k - 1.  A malformed
  * cu_seqlens sets the plan status word and every later kernel returns

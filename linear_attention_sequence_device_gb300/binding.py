@@ -34,6 +34,7 @@ SIGNATURES = {
     "gdn_last_error": (ctypes.c_char_p, []),
     "gdn_device_timeouts": (ctypes.c_int, [_vp, ctypes.c_int]),
     "gdn_debug_set_handover": (ctypes.c_int, [_i64, ctypes.c_int]),
+    "gdn_debug_set_split": (ctypes.c_int, [_i32]),
     "gdn_debug_set_phase_events": (ctypes.c_int, [_vp, _i32]),
     "gdn_cp_plan_words": (_i64, [_i32, _i32]),
     "gdn_cp_plan": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp]),
@@ -155,6 +156,12 @@ def debug_set_handover(wait_ns: int = 1_000_000_000, publish: bool = True):
     halves publish their final state (see gdn_cp.h); the defaults restore
     normal operation."""
     _check(load().gdn_debug_set_handover(int(wait_ns), 1 if publish else 0))
+
+
+def debug_set_split(enable: bool = True):
+    """Testing hook: work-queue splitting of items on or off (see gdn_cp.h);
+    the default restores normal operation."""
+    _check(load().gdn_debug_set_split(1 if enable else 0))
 
 
 def debug_set_phase_events(events=None):

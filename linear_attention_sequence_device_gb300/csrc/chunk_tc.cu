@@ -458,14 +458,31 @@ __device__ __noinline__ bool acquire_jobs(const ChunkParams& p, int src, SmemWS&
         }
         ChunkJob job;
         if (!make_job(p, src, job, bx, by, bz)) continue;
-        if (part) {  // a half of a split item; its final state destination carries the hand-over
-            const int split_t = job.t0 + 64 * first_chunks;
-            if (part == 1) {
-                job.t1 = split_t;
+        if (part) {  // a part of a split item, handed over through a final-state destination
+            // a continuing pass-2 segment has none of its own: its start state
+            // (read once, by the first part) takes the first part's final state
+            float* hand = job.fin;
+            int64_t hand_ld = job.fin_ld;
+            if (!hand && src == JOBS_SHARD_PASS2) {
+                hand = const_cast<float*>(job.init);
+                hand_ld = job.init_ld;
+            }
+            if (!hand) {  // nowhere to hand over: the first part runs the whole item
+                if (part == 2) continue;
+                part = 0;
             } else {
-                job.t0 = split_t;
-                job.init = job.fin;
-                job.init_ld = job.fin_ld;
+                const int split_t = job.t0 + 64 * first_chunks;
+                if (part == 1) {
+                    job.t1 = split_t;
+                    job.fin = hand;
+                    job.fin_ld = hand_ld;
+                } else {
+                    job.t0 = split_t;
+                    job.init = hand;
+                    job.init_ld = hand_ld;
+                    job.identity_init = false;  // an M summary continues from its first part's M
+                    if (job.wk_base >= 0) job.wk_base += first_chunks;  // stored operands: chunk slots
+                }
             }
         }
         const int nch = (job.t1 - job.t0 + 63) / 64;
@@ -1397,6 +1414,7 @@ static gdn_status make_map(CUtensorMap* m, const void* base, int64_t ld, int64_t
 // Split-item hand-over settings (a testing hook, gdn_debug_set_handover).
 static long long g_handover_ns = 1000000000ll;
 static int g_handover_publish = 1;
+static int g_split_items = 1;  // work-queue splitting of items (gdn_debug_set_split)
 
 gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
     p.handover_ns = g_handover_ns;
@@ -1437,9 +1455,16 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
         p.sched_items = (int)grid.x;
         p.sched_m = (int)(grid.y * grid.z);
         p.sched_ny = (int)grid.y;
-        const bool splittable =
-            p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1));
-        if ((st = launch_chunk_order(p, src, p.sched_items, p.sched_m, splittable, s)) != GDN_OK) return st;
+        // halves for single-segment launches with final states; short tails for
+        // the shard passes (every split part has a hand-over destination there,
+        // else its first part runs whole)
+        int rule = kSplitNone;
+        if (!g_split_items) rule = kSplitNone;
+        else if (p.h_final != nullptr && (src == JOBS_SEQS || (src == JOBS_SHARD_PASS1 && p.n_shards == 1)))
+            rule = kSplitHalves;
+        else if (p.n_shards > 1 && (src == JOBS_SHARD_PASS1 || src == JOBS_SHARD_PASS2))
+            rule = kSplitTail;
+        if ((st = launch_chunk_order(p, src, p.sched_items, p.sched_m, rule, s)) != GDN_OK) return st;
         const long long jobs = 2ll * p.sched_items * p.sched_m;
         grid = dim3((unsigned)(jobs < p.num_sms ? jobs : (p.num_sms > 0 ? p.num_sms : 1)), 1, 1);
     }
@@ -1450,6 +1475,11 @@ gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s) {
 }
 
 }  // namespace gdn
+
+extern "C" gdn_status gdn_debug_set_split(int32_t enable) {
+    gdn::g_split_items = enable ? 1 : 0;
+    return GDN_OK;
+}
 
 extern "C" gdn_status gdn_debug_set_handover(int64_t wait_ns, int publish) {
     if (wait_ns < 0) return gdn::fail(GDN_ERR_INVALID_ARG, "wait_ns=%lld < 0", (long long)wait_ns);

@@ -355,7 +355,9 @@ __host__ __device__ __forceinline__ int64_t chunk_sched_order_off(int S, int m) 
 // schedule.cu: words of a launch's schedule (S items, m head/tile pairs) and
 // the kernel that fills them (zeroed ticket and flags, sorted entries)
 inline size_t chunk_sched_words(int S, int m) { return (size_t)chunk_sched_order_off(S, m) + 4 * (size_t)S; }
-gdn_status launch_chunk_order(const ChunkParams& p, int src, int S, int m, bool splittable, cudaStream_t s);
+// split rules of the order kernel: none, middle halves, short tails
+constexpr int kSplitNone = 0, kSplitHalves = 1, kSplitTail = 2;
+gdn_status launch_chunk_order(const ChunkParams& p, int src, int S, int m, int split_rule, cudaStream_t s);
 
 // launchers (chunk_bf16.cu / chunk_f32.cu)
 gdn_status launch_chunk_bf16(const ChunkParams& p, int src, dim3 grid, cudaStream_t s);
@@ -364,8 +366,9 @@ gdn_status launch_chunk_f32(const ChunkParams& p, int src, dim3 grid, cudaStream
 bool chunk_tc_eligible(gdn_dtype dt, int dk, int dv);
 gdn_status launch_chunk_tc(ChunkParams p, int src, dim3 grid, cudaStream_t s);
 // the M chains of the shard summaries run apart from their stored operands
-// (csrc/mchain.cu): scratch bytes of the stored W rows, K~ and e^{G_last}
-// (0 for P < 2), and the launch over the plan's spanning shards into M [P, Hv, 128, 128]
+// (csrc/mchain.cu): scratch bytes of the stored W rows, K~ and e^{G_last},
+// then the segments' products when the chains are cut (0 for P < 2), and the
+// launch over the plan's spanning shards into M [P, Hv, 128, 128]
 bool mchain_eligible(gdn_dtype dt, int dk, int dv);
 // gdn_shard_fwd's workspace without the stored summary operands
 size_t shard_fwd_workspace_min(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk, int32_t Hv, int32_t dk,

@@ -9,11 +9,17 @@
 // products and state handling (M comes out as the chunk kernel's M job would
 // give it):
 //   v_new^T = -S^T W^T,   S^T <- e^{G_last} S^T + v_new^T K~.
-// One CTA of 128 threads per (shard, value head); thread = tensor-memory lane
-// = row of S^T.  It holds 256 tensor-memory columns, so two CTAs share an SM
-// and their chains interleave.  The next chunk's W / K~ load (TMA) while the
-// current one runs.  Every wait is bounded: on expiry the kernel counts a
-// timeout, writes GDN_ERR_TIMEOUT to the plan's status word and leaves.
+// One CTA of 128 threads per (shard, value head, segment); thread =
+// tensor-memory lane = row of S^T.  It holds 256 tensor-memory columns, so two
+// CTAs share an SM and their chains interleave.  The next chunk's W / K~ load
+// (TMA) while the current one runs.  Every wait is bounded: on expiry the
+// kernel counts a timeout, writes GDN_ERR_TIMEOUT to the plan's status word
+// and leaves.
+//
+// When there are fewer chains than resident CTAs (few long shards), each chain
+// is cut into G segments run side by side, each from the identity; M is the
+// ordered product of the segments' transitions (the product is associative),
+// formed in fp32 by mchain_merge_kernel.
 #include <cuda.h>
 #include <string.h>
 
@@ -31,6 +37,7 @@ namespace {
 constexpr int MT = 128;
 inline size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr uint32_t kMSpin = 1u << 20;
+constexpr size_t kMSmemFloor = 96 * 1024;  // shared memory that leaves room for two CTAs an SM, not three
 constexpr int BAR_M = 1;
 typedef __nv_bfloat16 bf16;
 
@@ -43,6 +50,7 @@ struct MParams {
     int num_seqs, P, Hv, nch;  // nch: chunks of a shard
     const float* eg;            // e^{G_last} of every stored chunk
     float* M;                   // [P, Hv, 128, 128]: M of shard r at r
+    float* Mseg;                // [P, Hv, G, 128, 128]: the segments' products (G > 1)
 };
 
 struct MSmem {
@@ -61,7 +69,7 @@ constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __grid_constant__ MMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     MSmem& sm = *reinterpret_cast<MSmem*>(smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023));
-    const int r = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int r = blockIdx.x, hv = blockIdx.y, z = blockIdx.z, G = gridDim.z, tid = threadIdx.x, warp = tid >> 5;
     if (__ldg(p.plan) != 0) return;  // malformed cu_seqlens: nothing to do
     // a spanning shard: one local segment, continued from and into its neighbours
     const int32_t* rec = p.plan + 1 + (int64_t)r * GDN_PLAN_NFIELDS;
@@ -69,6 +77,8 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
           __ldg(rec + GDN_PLAN_POST_NUM_RANKS) > 0))
         return;
     const int nch = p.nch;
+    const int c0 = (int)((int64_t)z * nch / G), c1 = (int)((int64_t)(z + 1) * nch / G);  // this segment's chunks
+    if (c1 <= c0) return;
     const int64_t item = (int64_t)r * p.Hv + hv;
     const int y0 = (int)(item * nch * 64);  // first stored row of this shard's chunks
     const float* eg = p.eg + item * nch;
@@ -91,8 +101,8 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
     const uint32_t T_S = tmem + lb, T_SB = tmem + 128 + lb, T_VN = tmem + 192 + lb;
     const int row = tid;  // tensor-memory lane = row of S^T
 
-    auto issue_load = [&](int c) {  // W rows and K~ of chunk c into stage c & 1 (thread 0)
-        const int st = c & 1, y = y0 + 64 * c;
+    auto issue_load = [&](int c) {  // W rows and K~ of chunk c into stage (c - c0) & 1 (thread 0)
+        const int st = (c - c0) & 1, y = y0 + 64 * c;
         tc::mbar_expect_tx(&sm.ld[st], 4 * 64 * 64 * 2);
         tc::tma_load_2d(sm.W[st], &maps.w, 0, y, &sm.ld[st]);
         tc::tma_load_2d(sm.W[st] + 64 * 64, &maps.w, 64, y, &sm.ld[st]);
@@ -101,13 +111,13 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
         sm.issued[st] += 1;
     };
     if (tid == 0) {
-        issue_load(0);
-        if (nch > 1) issue_load(1);
+        issue_load(c0);
+        if (c0 + 1 < c1) issue_load(c0 + 1);
     }
     // the identity, as bf16 (the first product's A operand) and scaled by the
     // first chunk's e^{G_last} (the first update accumulates onto it)
     {
-        const float e0 = __ldg(eg);
+        const float e0 = __ldg(eg + c0);
 #pragma unroll 1
         for (int h = 0; h < 2; ++h)
 #pragma unroll 1
@@ -137,13 +147,13 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
         tc::fence_after();
         return all;
     };
-    for (int c = 0; c < nch && ok; ++c) {
-        const int st = c & 1;
+    for (int c = c0; c < c1 && ok; ++c) {
+        const int st = (c - c0) & 1;
         tc::st32_zero(T_VN);  // v_new = 0 - S^T W^T: the product accumulates onto zero
         tc::st32_zero(T_VN + 32);
         bool in = true;
         if (tid == 0) {
-            in = tc::mbar_wait(&sm.ld[st], (c >> 1) & 1, kMSpin);
+            in = tc::mbar_wait(&sm.ld[st], ((c - c0) >> 1) & 1, kMSpin);
             if (in) sm.waited[st] += 1;
         }
         tc::wait_st();
@@ -179,8 +189,8 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
             tc::commit(&sm.mma);
         }
         if (!(ok = wait_mma())) break;
-        if (tid == 0 && c + 2 < nch) issue_load(c + 2);  // both products of chunk c have read the stage
-        if (c + 1 < nch) {
+        if (tid == 0 && c + 2 < c1) issue_load(c + 2);  // both products of chunk c have read the stage
+        if (c + 1 < c1) {
             // the new state: its bf16 copy, and the state scaled by the next
             // chunk's e^{G_last}, back into tensor memory
             const float egn = __ldg(eg + c + 1);
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
                     tc::st16(T_S + 64 * h + 16 * q4, sv);
                 }
         } else {
-            float* fin = p.M + item * 128 * 128;
+            float* fin = G > 1 ? p.Mseg + (item * G + z) * 128 * 128 : p.M + item * 128 * 128;
 #pragma unroll 1
             for (int h = 0; h < 2; ++h)
 #pragma unroll 1
@@ -226,7 +236,104 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+// M of every spanning shard from its G segments' products, each stored as
+// the transpose of its S^T product: M = Mseg[G-1] ... Mseg[0], in fp32.  CTA
+// (shard * Hv + head, block of 32 rows of M), 256 threads: warp w holds rows
+// [4w, 4w + 4) of the block and lane l columns [4l, 4l + 4), a 4 x 4 tile of
+// registers.  The running rows (transposed: a column of four rows is one
+// 16-byte load) and each factor are staged in shared memory by coalesced
+// loads, all in flight at once.
+constexpr int kMergeRows = 32;
+constexpr int kRt = 36;  // float stride of a transposed column (16-byte aligned, fewer bank conflicts)
+constexpr size_t kMergeSmem = (size_t)(128 * kRt + 128 * 128) * sizeof(float);
+__global__ void __launch_bounds__(256) mchain_merge_kernel(const int32_t* plan, int Hv, int G, const float* Mseg,
+                                                           float* M) {
+    extern __shared__ float4 merge_smem[];
+    float* Rt = reinterpret_cast<float*>(merge_smem);  // [128 columns][kRt]: running rows, transposed
+    float* F = Rt + 128 * kRt;                          // [128][128] factor
+    const int64_t item = blockIdx.x;
+    const int rb = blockIdx.y, tid = threadIdx.x;
+    if (__ldg(plan) != 0) return;
+    const int32_t* rec = plan + 1 + (item / Hv) * GDN_PLAN_NFIELDS;
+    if (!(__ldg(rec + GDN_PLAN_LOCAL_NUM_SEQS) == 1 && !__ldg(rec + GDN_PLAN_IS_FIRST_RANK) &&
+          __ldg(rec + GDN_PLAN_POST_NUM_RANKS) > 0))
+        return;
+    const float* seg = Mseg + item * G * 128 * 128;
+    {
+        const float4* src = reinterpret_cast<const float4*>(seg + (int64_t)(G - 1) * 128 * 128 + kMergeRows * rb * 128);
+#pragma unroll
+        for (int e0 = 0; e0 < kMergeRows * 32; e0 += 256) {
+            const int e = e0 + tid, r = e >> 5, c = 4 * (e & 31);
+            const float4 v = __ldg(src + e);
+            Rt[(c + 0) * kRt + r] = v.x;
+            Rt[(c + 1) * kRt + r] = v.y;
+            Rt[(c + 2) * kRt + r] = v.z;
+            Rt[(c + 3) * kRt + r] = v.w;
+        }
+    }
+    const int r0 = 4 * (tid >> 5), c0 = 4 * (tid & 31);
+    for (int zz = G - 2; zz >= 0; --zz) {
+        {
+            const float4* src = reinterpret_cast<const float4*>(seg + (int64_t)zz * 128 * 128);
+            float4* dst = reinterpret_cast<float4*>(F);
+#pragma unroll
+            for (int e = 0; e < 128 * 32 / 256; ++e) dst[tid + 256 * e] = __ldg(src + tid + 256 * e);
+        }
+        __syncthreads();
+        float acc[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 128; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(Rt + k * kRt + r0);
+            const float4 f = *reinterpret_cast<const float4*>(F + k * 128 + c0);
+            const float av[4] = {a.x, a.y, a.z, a.w}, fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], fv[c], acc[r][c]);
+        }
+        __syncthreads();
+        if (zz > 0) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) Rt[(c0 + c) * kRt + r0 + r] = acc[r][c];
+        } else {
+            float* out = M + item * 128 * 128 + (int64_t)(kMergeRows * rb + r0) * 128 + c0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<float4*>(out + r * 128) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        }
+    }
+}
+
+int device_sms() {
+    static int sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms[dev] > 0 ? sms[dev] : 148;
+}
+
 }  // namespace
+
+// Segments per M chain: at most (P - 2) * Hv chains (the first and the last
+// shard never span) run two CTAs to an SM; G segments of nch / G chunks take
+// ceil(chains * G / slots) rounds.  G > 1 only where that cuts the rounds'
+// chunks by a fifth or more, with segments of 16 chunks at least.
+int mchain_segments(int T, int P, int Hv) {
+    if (P < 3 || T <= 0) return 1;
+    const long long nch = ((long long)(T / P) + 63) / 64;
+    const long long chains = (long long)(P - 2) * Hv, slots = 2ll * device_sms();
+    auto cost = [&](long long G) { return ((chains * G + slots - 1) / slots) * ((nch + G - 1) / G); };
+    long long best = 1;
+    for (long long G = 2; G <= 8 && nch / G >= 16; ++G)
+        if (cost(G) < cost(best)) best = G;
+    return 5 * cost(best) <= 4 * cost(1) ? (int)best : 1;
+}
 
 bool mchain_eligible(gdn_dtype dt, int dk, int dv) { return dt == GDN_BF16 && dk == 128 && dv == 128; }
 
@@ -234,7 +341,9 @@ size_t mchain_scratch_bytes(int T, int P, int Hv) {
     if (P < 2) return 0;
     const size_t nch = ((size_t)(T / P) + 63) / 64;
     const size_t chunks = (size_t)P * Hv * nch;
-    return 2 * al256(chunks * 64 * 128 * sizeof(bf16)) + al256(chunks * sizeof(float));
+    const int G = mchain_segments(T, P, Hv);
+    return 2 * al256(chunks * 64 * 128 * sizeof(bf16)) + al256(chunks * sizeof(float)) +
+           (G > 1 ? al256((size_t)G * P * Hv * 128 * 128 * sizeof(float)) : 0);
 }
 
 gdn_status launch_mchain(const int32_t* plan, int num_seqs, int T, int P, int Hv, void* w, void* kt,
@@ -243,16 +352,25 @@ gdn_status launch_mchain(const int32_t* plan, int num_seqs, int T, int P, int Hv
     MParams p{};
     p.plan = plan; p.num_seqs = num_seqs; p.P = P; p.Hv = Hv; p.nch = (T / P + 63) / 64;
     p.eg = eg; p.M = M;
+    const int G = mchain_segments(T, P, Hv);
+    // the segments' products follow e^{G_last} in the scratch
+    p.Mseg = reinterpret_cast<float*>(const_cast<char*>(reinterpret_cast<const char*>(eg)) +
+                                      al256((size_t)P * Hv * p.nch * sizeof(float)));
     const int64_t rows = (int64_t)P * Hv * p.nch * 64;
     MMaps maps;
     memset(&maps, 0, sizeof(maps));
     gdn_status st;
     if ((st = make_map_bf16(&maps.w, w, 128, 128, rows)) != GDN_OK) return st;
     if ((st = make_map_bf16(&maps.kt, kt, 128, 128, rows)) != GDN_OK) return st;
-    const size_t smem = sizeof(MSmem) + 1024;
+    // at most two CTAs to an SM, the two that its tensor memory holds (a third
+    // would only wait in its allocation, keeping a place a chain could use)
+    const size_t smem = sizeof(MSmem) + 1024 > kMSmemFloor ? sizeof(MSmem) + 1024 : kMSmemFloor;
     if ((st = set_smem_attr((const void*)mchain_kernel, smem)) != GDN_OK) return st;
-    mchain_kernel<<<dim3(P, Hv), MT, smem, s>>>(p, maps);
-    return check_launch("mchain_kernel");
+    mchain_kernel<<<dim3(P, Hv, G), MT, smem, s>>>(p, maps);
+    if ((st = check_launch("mchain_kernel")) != GDN_OK || G == 1) return st;
+    if ((st = set_smem_attr((const void*)mchain_merge_kernel, kMergeSmem)) != GDN_OK) return st;
+    mchain_merge_kernel<<<dim3(P * Hv, 128 / kMergeRows), 256, kMergeSmem, s>>>(plan, Hv, G, p.Mseg, M);
+    return check_launch("mchain_merge_kernel");
 }
 
 }  // namespace gdn

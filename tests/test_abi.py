@@ -163,14 +163,20 @@ def test_backward_host_errors(lib):
 
 def test_shard_fwd_workspace_sizes(lib):
     """The full workspace adds room for the stored summary operands (bf16,
-    d = 128, P > 1: W rows, K~ tiles and e^{G_last} of every shard chunk);
+    d = 128, P > 1: W rows, K~ tiles and e^{G_last} of every shard chunk),
+    plus, when the M chains are cut into G segments (2 <= G <= 8, chosen from
+    the device's SM count), G fp32 products of 64 KiB per (shard, head);
     otherwise it equals the minimum.  0 for invalid arguments."""
     full = lambda *a: lib.gdn_shard_fwd_workspace_size(*a)
     small = lambda *a: lib.gdn_shard_fwd_workspace_min_size(*a)
     a = (131072, 1, 8, 16, 16, 128, 128, 1)            # bf16, d = 128, P = 8
     extra = full(*a) - small(*a)
     chunks = 8 * 16 * ((131072 // 8 + 63) // 64)
-    assert extra >= chunks * (2 * 64 * 128 * 2 + 4) and extra < chunks * (2 * 64 * 128 * 2 + 4) + 3 * 256
+    ops = chunks * (2 * 64 * 128 * 2 + 4)
+    assert ops <= extra < ops + 3 * 256 + 8 * 8 * 16 * 65536
+    seg = (extra - ops) // (8 * 16 * 65536)            # segments' products (alignment rounds up < 1 KiB)
+    assert seg == 0 or 2 <= seg <= 8
+    assert extra - ops - seg * 8 * 16 * 65536 < 4 * 256
     for b in ((131072, 1, 1, 16, 16, 128, 128, 1),     # one shard
               (4096, 2, 4, 2, 2, 64, 64, 1),           # other head size
               (4096, 2, 4, 2, 2, 128, 128, 0)):        # fp32

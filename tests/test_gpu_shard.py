@@ -258,3 +258,126 @@ def test_summary_m_chains_apart_are_bit_identical(name, P, kw):
         o_ref, hf_ref = oracle_path(w, host)
         assert_close(f64(o1), o_ref, w.dtype, "o")
         assert_close(f64(hf1), hf_ref, w.dtype, "h_final")
+
+
+SPLIT_CASES = {
+    # one sequence, shards of 1000 tokens (a partial last chunk in each): 8 x 32
+    # jobs per pass, more than the SMs, so the shard passes split every item
+    # into a long first part and a short tail part
+    "one_seq_P8": lambda: W.million(T=8000, n_shards=8),
+    # 16 shards of 16 full chunks
+    "one_seq_P16": lambda: W.million(T=16384, n_shards=16),
+    # a sequence ending on a shard boundary: pass-2 segments that end their
+    # sequence hand over through h_final, continuing ones through their start state
+    "two_seqs_P8": lambda: W.Workload("two_seqs", 8000, 32, 32, 128, 128, "bf16", 8, 5, (5000, 3000),
+                                      g_shift=2.0, h0_std=0.02),
+    # one sequence per shard: pass 1 only, handed over through h_final (or,
+    # without final states, run whole by the first part)
+    "aligned_P8": lambda: W.Workload("aligned", 8000, 32, 32, 128, 128, "bf16", 8, 6, (1000,) * 8,
+                                     g_shift=2.0, h0_std=0.02),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+@pytest.mark.parametrize("final", [True, False])
+def test_split_tail_parts_are_bit_identical(name, final):
+    """The shard passes' work queue splits items into a first part and a
+    short tail part when the launch has more jobs than SMs; the tail part
+    starts from the first part's final state (fp32, stored and reloaded
+    exactly).  So the outputs equal, bit for bit, those of the same call
+    with splitting turned off, and they match the oracle."""
+    import linear_attention_sequence_device_gb300 as g
+    w = SPLIT_CASES[name]()
+    host, d = path_inputs(w)
+    P = w.n_shards
+
+    def call():
+        return g.gdn_shard_fwd(d["x"], d["conv_w"], d["conv_b"], d["g"], d["beta"], d["cu"], w.Hk, w.Hv,
+                               w.dk, w.dv, P, h0=d["h0"], want_plan=True, h_final=final)
+
+    g.binding.device_timeouts(reset=True)
+    try:
+        g.binding.debug_set_split(False)
+        o0, hf0, plan0 = call()
+        torch.cuda.synchronize()
+    finally:
+        g.binding.debug_set_split(True)
+    o1, hf1, plan1 = call()
+    torch.cuda.synchronize()
+    assert int(plan0[0]) == 0 and int(plan1[0]) == 0
+    assert g.binding.device_timeouts() == 0
+    assert torch.equal(o0, o1)
+    if final:
+        assert torch.equal(hf0, hf1)
+    else:
+        assert hf0 is None and hf1 is None
+    o_ref, hf_ref = oracle_path(w, host)
+    assert_close(f64(o1), o_ref, w.dtype, f"{name} o")
+    if final:
+        assert_close(f64(hf1), hf_ref, w.dtype, f"{name} h_final")
+
+
+def test_split_tail_parts_wait_for_their_first_parts():
+    """The shard passes do split: with first parts that never publish their
+    final state (the gdn_debug_set_handover hook) the tail parts' waits run
+    out after 2 ms and the call reports GDN_ERR_TIMEOUT (7) in the plan's
+    status word; with splitting turned off nothing waits and the same call
+    succeeds.  Normal calls afterwards report no timeout."""
+    import linear_attention_sequence_device_gb300 as g
+    b = g.binding
+    w = SPLIT_CASES["one_seq_P16"]()
+    _, d = path_inputs(w)
+    b.device_timeouts(reset=True)
+    try:
+        b.debug_set_handover(2_000_000, publish=False)
+        _, _, plan_split = run_gpu(w, d, w.n_shards)
+        torch.cuda.synchronize()
+        n_split = b.device_timeouts(reset=True)
+        b.debug_set_split(False)
+        _, _, plan_whole = run_gpu(w, d, w.n_shards)
+        torch.cuda.synchronize()
+        n_whole = b.device_timeouts(reset=True)
+    finally:
+        b.debug_set_handover()
+        b.debug_set_split(True)
+    assert int(plan_split[0]) == 7 and n_split >= 1
+    assert int(plan_whole[0]) == 0 and n_whole == 0
+    _, _, plan = run_gpu(w, d, w.n_shards)
+    torch.cuda.synchronize()
+    assert int(plan[0]) == 0 and b.device_timeouts() == 0
+
+
+def test_summary_m_chain_segments():
+    """Few long shards: each summary's M chain is cut into segments run side
+    by side (here 2 spanning shards x 16 heads, 64 chunks a shard: 4
+    segments), each from the identity, and M is their ordered product in
+    fp32.  Small beta and g = 0 keep M far from zero, and h0 reaches the last
+    shard only through the M products: without h0 the last shard's outputs
+    move by far more than the tolerance.  The result matches the oracle, as
+    does the same call with the M chains run whole in the chunk kernel
+    (minimum workspace)."""
+    import linear_attention_sequence_device_gb300 as g
+    w = W.long_seq(T=16384, n_shards=4, g_zero=True, h0_std=0.5)
+    host, d = path_inputs(w)
+    small_beta = torch.from_numpy(host["beta"] * 0.03).to(torch.bfloat16)
+    host["beta"] = small_beta.double().numpy()
+    d["beta"] = small_beta.to(dev())
+    P = w.n_shards
+    dt = torch.bfloat16
+    full = g.shard_fwd_workspace_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
+    small = g.shard_fwd_workspace_min_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, dt)
+    g.binding.device_timeouts(reset=True)
+    o1, hf1, plan1 = run_gpu(w, d, P, workspace=torch.empty(full, dtype=torch.uint8, device=dev()))
+    o2, hf2, plan2 = run_gpu(w, d, P, workspace=torch.empty(small, dtype=torch.uint8, device=dev()))
+    torch.cuda.synchronize()
+    assert int(plan1[0]) == 0 and int(plan2[0]) == 0
+    assert g.binding.device_timeouts() == 0
+    o_ref, hf_ref = oracle_path(w, host)
+    last = slice((P - 1) * (w.T // P), w.T)
+    no_h0 = dict(host, h0=np.zeros_like(host["h0"]))
+    o_ref0, _ = oracle_path(w, no_h0)
+    assert rel_l2(o_ref0[last], o_ref[last]) > 0.2  # the carried h0 is visible
+    for o, hf, tag in ((o1, hf1, "segments"), (o2, hf2, "whole")):
+        assert_close(f64(o), o_ref, w.dtype, f"{tag} o")
+        assert_close(f64(o)[last], o_ref[last], w.dtype, f"{tag} o, last shard")
+        assert_close(f64(hf), hf_ref, w.dtype, f"{tag} h_final")
