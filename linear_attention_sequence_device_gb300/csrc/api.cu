@@ -62,6 +62,42 @@ static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 static size_t esize(gdn_dtype dt) { return dt == GDN_BF16 ? 2 : 4; }
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int device_sm_count() {
+    static int sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms[dev] > 0 ? sms[dev] : 148;
+}
+
+// Shards a gdn_shard_fwd call runs on.  The result is the same for any shard
+// count (the sharded path equals the unsharded one), so one sequence cut into
+// fewer shards than the SMs can hold, whose chains then leave SMs idle in both
+// passes, is cut finer inside the call: n_shards * 2^j (j <= 3, dividing T,
+// shards of 1024 tokens at least), each doubling kept only if it cuts the
+// modelled time by a tenth.  Model, in chunk periods: per pass the longer of
+// one shard's chain and the spanning shards' work spread over the SMs, two
+// passes, plus one merge step per shard.  Only the tensor-core path (bf16,
+// d = 128); the plan a caller receives is always that of its own n_shards.
+int internal_shards(int T, int num_seqs, int P, int Hv, int dk, int dv, gdn_dtype dtype) {
+    if (P < 2 || num_seqs != 1 || T <= 0 || !chunk_tc_eligible(dtype, dk, dv)) return P;
+    const double sms = (double)device_sm_count();
+    auto cost = [&](long long Q) {
+        const double L = (double)(T / Q) / 64.0, spread = (double)(Q - 1) * Hv * L / sms;
+        return 2.0 * (L > spread ? L : spread) + (double)Q;
+    };
+    long long best = P;
+    double bc = cost(P);
+    for (long long Q = 2ll * P; Q <= 8ll * P && Q <= 65536 && T % Q == 0 && T / Q >= 1024; Q *= 2) {
+        const double c = cost(Q);
+        if (c < 0.9 * bc) {
+            best = Q;
+            bc = c;
+        }
+    }
+    return (int)best;
+}
+
 // checks shared by gdn_chunk_fwd / gdn_chunk_summary / gdn_shard_fwd
 static gdn_status check_heads(gdn_dtype dt, int T, int num_seqs, int Hk, int Hv, int dk, int dv) {
     if (dt != GDN_F32 && dt != GDN_BF16) return fail(GDN_ERR_DTYPE, "unknown dtype %d", (int)dt);
@@ -443,8 +479,9 @@ size_t gdn_shard_fwd_workspace_size(int32_t T, int32_t num_seqs, int32_t n_shard
                                     int32_t Hv, int32_t dk, int32_t dv, gdn_dtype dtype) {
     const size_t need = gdn::shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
     if (need == 0) return 0;
-    const bool mk = gdn::mchain_eligible(dtype, dk, dv) && n_shards > 1 && T > 0;
-    return need + (mk ? gdn::mchain_scratch_bytes(T, n_shards, Hv) : 0);
+    const int P = gdn::internal_shards(T, num_seqs, n_shards, Hv, dk, dv, dtype);
+    const bool mk = gdn::mchain_eligible(dtype, dk, dv) && P > 1 && T > 0;
+    return need + (mk ? gdn::mchain_scratch_bytes(T, P, Hv) : 0);
 }
 
 size_t gdn_shard_fwd_workspace_min_size(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk,
@@ -460,13 +497,14 @@ namespace gdn {
 size_t shard_fwd_workspace_min(int32_t T, int32_t num_seqs, int32_t n_shards, int32_t Hk, int32_t Hv, int32_t dk,
                                int32_t dv, gdn_dtype dtype) {
     if (T < 0 || num_seqs < 1 || n_shards < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
+    const int P = internal_shards(T, num_seqs, n_shards, Hv, dk, dv, dtype);
     const size_t cch = 2 * (size_t)Hk * dk + (size_t)Hv * dv;
-    const size_t carry = (size_t)n_shards * Hv * dk;
-    return align256(sizeof(int32_t) * (size_t)gdn_cp_plan_words(num_seqs, n_shards)) +
+    const size_t carry = (size_t)P * Hv * dk;
+    return align256(sizeof(int32_t) * (size_t)gdn_cp_plan_words(num_seqs, P)) +
            align256((size_t)T * cch * esize(dtype)) +
            2 * align256(carry * dv * sizeof(float)) +  // carry N, S_in
            align256(carry * dk * sizeof(float)) +      // carry M
-           pass1_sched_bytes(num_seqs, n_shards, Hv, dk, dv, dtype);
+           pass1_sched_bytes(num_seqs, P, Hv, dk, dv, dtype);
 }
 
 // The layer's extras around the path: gates from the raw projections and the
@@ -518,16 +556,16 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
     const size_t need = shard_fwd_workspace_min(T, num_seqs, n_shards, Hk, Hv, dk, dv, dtype);
     if (!workspace || workspace_bytes < need)
         return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", workspace_bytes, need);
+    // the shards the call runs on (the caller's, or finer for one long sequence)
+    const int P = internal_shards(T, num_seqs, n_shards, Hv, dk, dv, dtype);
     // with room for the stored summary operands, the M chains run apart
-    const size_t mk_bytes =
-        mchain_eligible(dtype, dk, dv) && n_shards > 1 ? mchain_scratch_bytes(T, n_shards, Hv) : 0;
+    const size_t mk_bytes = mchain_eligible(dtype, dk, dv) && P > 1 ? mchain_scratch_bytes(T, P, Hv) : 0;
     const bool use_mk = mk_bytes > 0 && workspace_bytes >= need + mk_bytes && !(ex && ex->z) &&
-                        (int64_t)n_shards * Hv * ((T / n_shards + 63) / 64) * 64 < ((int64_t)1 << 31);
+                        (int64_t)P * Hv * ((T / P + 63) / 64) * 64 < ((int64_t)1 << 31);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(GDN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     const int64_t cch = 2 * (int64_t)Hk * dk + (int64_t)Hv * dv;
-    const int P = n_shards;
     char* ws = static_cast<char*>(workspace);
     const int64_t words = gdn_cp_plan_words(num_seqs, P);
     int32_t* plan = reinterpret_cast<int32_t*>(ws);
@@ -621,9 +659,14 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
             return st;
     }
     if (plan_out) {
-        if (cudaMemcpyAsync(plan_out, plan, sizeof(int32_t) * (size_t)words, cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess)
+        if (P != n_shards) {  // the caller's plan, with the status word of the call
+            if ((st = launch_plan(cu_seqlens, num_seqs, n_shards, plan_out, s)) != GDN_OK) return st;
+            if (cudaMemcpyAsync(plan_out, plan, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+                return check_launch("plan status copy");
+        } else if (cudaMemcpyAsync(plan_out, plan, sizeof(int32_t) * (size_t)words, cudaMemcpyDeviceToDevice,
+                                   s) != cudaSuccess) {
             return check_launch("plan copy");
+        }
     }
     mark(5);
     return GDN_OK;

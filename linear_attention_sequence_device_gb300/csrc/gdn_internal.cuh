@@ -381,6 +381,10 @@ int chunk_col_tile(gdn_dtype dt, int dk, int dv);
 
 // plan.cu
 gdn_status launch_plan(const int32_t* cu, int num_seqs, int P, int32_t* plan, cudaStream_t s);
+// SMs of the current device (cached per device)
+int device_sm_count();
+// shards a gdn_shard_fwd call runs on (csrc/api.cu)
+int internal_shards(int T, int num_seqs, int P, int Hv, int dk, int dv, gdn_dtype dtype);
 // conv.cu: per-shard conv; plan == null -> one shard with an explicit halo
 gdn_status launch_conv(const void* x, int64_t ldx, gdn_dtype dt, int T, int C, const void* w,
                        const void* b, int Kc, const int32_t* cu, int num_seqs, const void* halo,

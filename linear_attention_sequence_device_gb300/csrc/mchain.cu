@@ -310,14 +310,6 @@ __global__ void __launch_bounds__(256) mchain_merge_kernel(const int32_t* plan, 
     }
 }
 
-int device_sms() {
-    static int sms[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    return sms[dev] > 0 ? sms[dev] : 148;
-}
-
 }  // namespace
 
 // Segments per M chain: at most (P - 2) * Hv chains (the first and the last
@@ -327,7 +319,7 @@ int device_sms() {
 int mchain_segments(int T, int P, int Hv) {
     if (P < 3 || T <= 0) return 1;
     const long long nch = ((long long)(T / P) + 63) / 64;
-    const long long chains = (long long)(P - 2) * Hv, slots = 2ll * device_sms();
+    const long long chains = (long long)(P - 2) * Hv, slots = 2ll * device_sm_count();
     auto cost = [&](long long G) { return ((chains * G + slots - 1) / slots) * ((nch + G - 1) / G); };
     long long best = 1;
     for (long long G = 2; G <= 8 && nch / G >= 16; ++G)

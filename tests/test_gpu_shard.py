@@ -381,3 +381,39 @@ def test_summary_m_chain_segments():
         assert_close(f64(o), o_ref, w.dtype, f"{tag} o")
         assert_close(f64(o)[last], o_ref[last], w.dtype, f"{tag} o, last shard")
         assert_close(f64(hf), hf_ref, w.dtype, f"{tag} h_final")
+
+
+def test_one_sequence_runs_on_finer_internal_shards():
+    """One 16384-token sequence on 2, 4 or 8 shards: too few chains for the
+    SMs, so every call runs on 8 internal shards of 2048 tokens.  The three
+    calls give bit-identical o and h_final, each returns the plan of its own
+    shard count (the oracle's, field by field), and the result matches the
+    oracle with a carried state that matters (g = 0, small beta, h0)."""
+    import linear_attention_sequence_device_gb300 as g
+    outs = []
+    for P in (2, 4, 8):
+        w = W.long_seq(T=16384, n_shards=P, g_zero=True, h0_std=0.5)
+        host, d = path_inputs(w)
+        small_beta = torch.from_numpy(host["beta"] * 0.03).to(torch.bfloat16)
+        host["beta"] = small_beta.double().numpy()
+        d["beta"] = small_beta.to(dev())
+        g.binding.device_timeouts(reset=True)
+        o, hf, plan = run_gpu(w, d, P)
+        torch.cuda.synchronize()
+        assert g.binding.device_timeouts() == 0
+        assert plan.numel() == g.plan_words(w.N, P)
+        assert g.decode_plan(plan, w.N, P) == g.decode_plan(g.gdn_cp_plan(d["cu"], P), w.N, P)
+        status, recs = g.decode_plan(plan, w.N, P)
+        assert status == 0 and len(recs) == P
+        for a, b in zip(recs, oracle.plan(w.cu_seqlens(), P)):
+            assert a["local_cu"] == b["local_cu"].tolist()
+            assert a["pre_num_conv_tokens"] == b["pre_num_conv_tokens"]
+        outs.append((o, hf))
+    for o, hf in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(hf, outs[0][1])
+    o_ref, hf_ref = oracle_path(w, host)
+    assert_close(f64(outs[0][0]), o_ref, w.dtype, "o")
+    assert_close(f64(outs[0][1]), hf_ref, w.dtype, "h_final")
+    for r in range(1, 8):  # the first chunk after every internal boundary
+        sl = slice(r * 2048, r * 2048 + 64)
+        assert_close(f64(outs[0][0])[sl], o_ref[sl], w.dtype, f"o after {r * 2048}")
