@@ -2,7 +2,8 @@
 // page, _merge_gdn_prefix_state_summaries_torch; _apply_gdn_state_summary):
 //   S_in[0] = S0 or 0;  S_in[r] = M[r-1] S_in[r-1] + N[r-1]
 // Sequential over shards in fp32, as the page's loop; parallel over value
-// heads and 32-column tiles of the state.  In the sharded forward each
+// heads and 16- or 32-column tiles of the state (16 while the CTAs still fit
+// the SMs: the sequential steps then run on twice as many SMs).  In the sharded forward each
 // shard's carry is classified from the plan: affine (M, N) for a shard that
 // a single sequence spans from an earlier shard into a later one, constant
 // (N only, M = 0) when the carried sequence starts inside the shard, and
@@ -15,15 +16,14 @@ gdn_status set_smem_attr(const void* func, size_t bytes);
 namespace {
 
 constexpr int NT = 256;
-constexpr int CT = 32;  // state columns per CTA: one per lane
 
-// grid (Hv, dv / 32), 8 warps.  Lane = state column c0 + lane, warp w = rows
-// [DK/8 w, DK/8 (w + 1)).  Each shard's M (DK x DK fp32) is staged in shared
-// memory with cp.async, the next one in flight while the current is applied
-// (the loads are the only global traffic on the sequential path); reads of M
-// are broadcasts (one row element for the whole warp), reads of S are one
-// column per lane.
-template <int DK>
+// grid (Hv, dv / CT), 256 threads.  Thread = state column c0 + tid % CT and
+// row group tid / CT (CG = 256 / CT groups of DK / CG rows).  Each shard's M
+// (DK x DK fp32) is staged in shared memory with cp.async, the next one in
+// flight while the current is applied (the loads are the only global traffic
+// on the sequential path); reads of M are broadcasts (one row element for the
+// threads of a row group), reads of S are one column per thread.
+template <int DK, int CT>
 __global__ void __launch_bounds__(NT) combine_kernel(const float* __restrict__ M,
                                                      const float* __restrict__ N,
                                                      const float* __restrict__ S0, int P, int Hv,
@@ -33,9 +33,10 @@ __global__ void __launch_bounds__(NT) combine_kernel(const float* __restrict__ M
     float* Ms = csm;                // [2][DK * DK]
     float* S = csm + 2 * DK * DK;   // [DK][CT]
     if (plan && plan[0] != 0) return;
-    constexpr int RPW = DK / 8;     // rows per warp
+    constexpr int CG = NT / CT;     // row groups
+    constexpr int RPW = DK / CG;    // rows per group
     const int h = blockIdx.x, c0 = blockIdx.y * CT;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid % CT, warp = tid / CT;
     const int64_t hs = (int64_t)DK * dv;
     // 2 = affine (M, N), 1 = constant (N only, M = 0), 0 = none
     auto kind = [&](int r) -> int {
@@ -52,12 +53,12 @@ __global__ void __launch_bounds__(NT) combine_kernel(const float* __restrict__ M
         }
         cp_async_commit();
     };
-    for (int i = warp; i < DK; i += 8) S[i * CT + lane] = S0 ? S0[h * hs + (int64_t)i * dv + c0 + lane] : 0.f;
+    for (int i = warp; i < DK; i += CG) S[i * CT + lane] = S0 ? S0[h * hs + (int64_t)i * dv + c0 + lane] : 0.f;
     stage(0);
     __syncthreads();
     for (int r = 0; r < P; ++r) {
         float* out = S_in + ((int64_t)r * Hv + h) * hs;
-        for (int i = warp; i < DK; i += 8) out[(int64_t)i * dv + c0 + lane] = S[i * CT + lane];
+        for (int i = warp; i < DK; i += CG) out[(int64_t)i * dv + c0 + lane] = S[i * CT + lane];
         if (r == P - 1) break;
         const int kd = kind(r);
         stage(r + 1);  // the next shard's M streams in while this one is applied
@@ -146,26 +147,34 @@ gdn_status launch_gated_norm(void* o, const void* z, int64_t ldz, const void* w,
     return check_launch("gated_norm_kernel");
 }
 
-gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
-                          int dv, float* S_in, const int32_t* plan, cudaStream_t s) {
+template <int CT>
+static gdn_status launch_combine_ct(const float* M, const float* N, const float* S0, int P, int Hv, int dk, int dv,
+                                   float* S_in, const int32_t* plan, cudaStream_t s) {
     dim3 grid(Hv, dv / CT);
     const size_t smem = sizeof(float) * (2 * (size_t)dk * dk + (size_t)dk * CT);
     gdn_status st;
     switch (dk) {
         case 32:
-            combine_kernel<32><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            combine_kernel<32, CT><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
             break;
         case 64:
-            if ((st = set_smem_attr((const void*)combine_kernel<64>, smem)) != GDN_OK) return st;
-            combine_kernel<64><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            if ((st = set_smem_attr((const void*)combine_kernel<64, CT>, smem)) != GDN_OK) return st;
+            combine_kernel<64, CT><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
             break;
         case 128:
-            if ((st = set_smem_attr((const void*)combine_kernel<128>, smem)) != GDN_OK) return st;
-            combine_kernel<128><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
+            if ((st = set_smem_attr((const void*)combine_kernel<128, CT>, smem)) != GDN_OK) return st;
+            combine_kernel<128, CT><<<grid, NT, smem, s>>>(M, N, S0, P, Hv, dv, S_in, plan);
             break;
         default: return fail(GDN_ERR_UNSUPPORTED_SHAPE, "dk=%d", dk);
     }
     return check_launch("combine_kernel");
+}
+
+gdn_status launch_combine(const float* M, const float* N, const float* S0, int P, int Hv, int dk,
+                          int dv, float* S_in, const int32_t* plan, cudaStream_t s) {
+    if ((int64_t)Hv * (dv / 16) <= device_sm_count())
+        return launch_combine_ct<16>(M, N, S0, P, Hv, dk, dv, S_in, plan, s);
+    return launch_combine_ct<32>(M, N, S0, P, Hv, dk, dv, S_in, plan, s);
 }
 
 gdn_status launch_empty_seq_final(const int32_t* cu, int num_seqs, int Hv, int dk, int dv,

@@ -348,11 +348,12 @@ def test_chunk_summary_vs_oracle(case):
     assert_close(f64(N), N_ref, w.dtype, "N")
 
 
-@pytest.mark.parametrize("dk,dv,P", [(32, 32, 2), (64, 128, 5), (128, 128, 64), (128, 64, 7)])
-def test_state_combine_vs_oracle(dk, dv, P):
+@pytest.mark.parametrize("dk,dv,P,Hv", [(32, 32, 2, 3), (64, 128, 5, 3), (128, 128, 64, 3), (128, 64, 7, 3),
+                                         (128, 128, 9, 40), (64, 64, 4, 80)])
+def test_state_combine_vs_oracle(dk, dv, P, Hv):
+    """16-column state tiles while the CTAs fit the SMs (few heads), else 32."""
     import linear_attention_sequence_device_gb300 as g
     r = np.random.default_rng(dk + dv + P)
-    Hv = 3
     M = r.standard_normal((P, Hv, dk, dk)) / np.sqrt(dk) * 0.9
     N = r.standard_normal((P, Hv, dk, dv))
     S0 = r.standard_normal((Hv, dk, dv))
