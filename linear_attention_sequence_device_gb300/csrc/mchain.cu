@@ -314,13 +314,18 @@ __global__ void __launch_bounds__(256) mchain_merge_kernel(const int32_t* plan, 
 
 // Segments per M chain: at most (P - 2) * Hv chains (the first and the last
 // shard never span) run two CTAs to an SM; G segments of nch / G chunks take
-// ceil(chains * G / slots) rounds.  G > 1 only where that cuts the rounds'
-// chunks by a fifth or more, with segments of 16 chunks at least.
+// ceil(chains * G / slots) rounds, and the merge adds G - 1 products per
+// chain, about a tenth of a chunk period each over the whole GPU (measured:
+// 0.13-0.18 us per chain and product against 1.7 us per chunk).  G > 1 only
+// where that cuts the modelled time by a fifth or more, with segments of 16
+// chunks at least.
 int mchain_segments(int T, int P, int Hv) {
     if (P < 3 || T <= 0) return 1;
     const long long nch = ((long long)(T / P) + 63) / 64;
     const long long chains = (long long)(P - 2) * Hv, slots = 2ll * device_sm_count();
-    auto cost = [&](long long G) { return ((chains * G + slots - 1) / slots) * ((nch + G - 1) / G); };
+    auto cost = [&](long long G) {
+        return 10 * ((chains * G + slots - 1) / slots) * ((nch + G - 1) / G) + chains * (G - 1);
+    };
     long long best = 1;
     for (long long G = 2; G <= 8 && nch / G >= 16; ++G)
         if (cost(G) < cost(best)) best = G;

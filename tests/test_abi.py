@@ -182,3 +182,30 @@ def test_shard_fwd_workspace_sizes(lib):
               (4096, 2, 4, 2, 2, 128, 128, 0)):        # fp32
         assert full(*b) == small(*b) > 0
     assert full(0, 0, 1, 1, 1, 128, 128, 1) == 0 and small(0, 0, 1, 1, 1, 128, 128, 1) == 0
+
+
+def test_internal_shard_count_in_the_workspace(lib):
+    """The shard count a gdn_shard_fwd call runs on shows in its workspace:
+    plan, conv output, carries (N, S_in, M) and pass-1 schedule are sized for
+    it.  One 131072-token sequence with 16 heads on 8 shards (bf16, d = 128)
+    runs on 16 internal shards (few chains for the SMs: 148 assumed without
+    a GPU); two sequences, fp32 and the million shape keep the caller's
+    count."""
+    a256 = lambda x: (x + 255) // 256 * 256
+
+    def min_size(T, N, P, Hk, Hv, d, bf16):
+        e = 2 if bf16 else 4
+        cch = 2 * Hk * d + Hv * d
+        carry = P * Hv * d
+        tile = 128 if bf16 and d == 128 else (32 if not bf16 else min(d, 64))
+        S, m = N + P, Hv * (2 * d // tile)
+        o = 4 + S * m
+        o += o & 1
+        return (a256(4 * lib.gdn_cp_plan_words(N, P)) + a256(T * cch * e) + 2 * a256(carry * d * 4)
+                + a256(carry * d * 4) + a256(4 * (o + 4 * S)))
+
+    small = lambda *a: lib.gdn_shard_fwd_workspace_min_size(*a)
+    assert small(131072, 1, 8, 16, 16, 128, 128, 1) == min_size(131072, 1, 16, 16, 16, 128, True)
+    assert small(131072, 2, 8, 16, 16, 128, 128, 1) == min_size(131072, 2, 8, 16, 16, 128, True)
+    assert small(131072, 1, 8, 16, 16, 128, 128, 0) == min_size(131072, 1, 8, 16, 16, 128, False)
+    assert small(1048576, 1, 64, 32, 32, 128, 128, 1) == min_size(1048576, 1, 64, 32, 32, 128, True)

@@ -350,14 +350,14 @@ def test_split_tail_parts_wait_for_their_first_parts():
 def test_summary_m_chain_segments():
     """Few long shards: each summary's M chain is cut into segments run side
     by side (here 2 spanning shards x 16 heads, 64 chunks a shard: 4
-    segments), each from the identity, and M is their ordered product in
-    fp32.  Small beta and g = 0 keep M far from zero, and h0 reaches the last
-    shard only through the M products: without h0 the last shard's outputs
-    move by far more than the tolerance.  The result matches the oracle, as
-    does the same call with the M chains run whole in the chunk kernel
-    (minimum workspace)."""
+    segments; two sequences, so the call keeps its 4 shards), each from the
+    identity, and M is their ordered product in fp32.  Small beta and g = 0
+    keep M far from zero, and h0 reaches the last shard only through the M
+    products: without h0 the last shard's outputs move by far more than the
+    tolerance.  The result matches the oracle, as does the same call with
+    the M chains run whole in the chunk kernel (minimum workspace)."""
     import linear_attention_sequence_device_gb300 as g
-    w = W.long_seq(T=16384, n_shards=4, g_zero=True, h0_std=0.5)
+    w = W.Workload("two_seqs_seg", 16384, 16, 16, 128, 128, "bf16", 4, 7, (16320, 64), g_zero=True, h0_std=0.5)
     host, d = path_inputs(w)
     small_beta = torch.from_numpy(host["beta"] * 0.03).to(torch.bfloat16)
     host["beta"] = small_beta.double().numpy()
@@ -373,7 +373,7 @@ def test_summary_m_chain_segments():
     assert int(plan1[0]) == 0 and int(plan2[0]) == 0
     assert g.binding.device_timeouts() == 0
     o_ref, hf_ref = oracle_path(w, host)
-    last = slice((P - 1) * (w.T // P), w.T)
+    last = slice((P - 1) * (w.T // P), 16320)  # the last shard's part of the first sequence
     no_h0 = dict(host, h0=np.zeros_like(host["h0"]))
     o_ref0, _ = oracle_path(w, no_h0)
     assert rel_l2(o_ref0[last], o_ref[last]) > 0.2  # the carried h0 is visible
@@ -385,8 +385,9 @@ def test_summary_m_chain_segments():
 
 def test_one_sequence_runs_on_finer_internal_shards():
     """One 16384-token sequence on 2, 4 or 8 shards: too few chains for the
-    SMs, so every call runs on 8 internal shards of 2048 tokens.  The three
-    calls give bit-identical o and h_final, each returns the plan of its own
+    SMs, so every call runs on 8 internal shards of 2048 tokens (and cuts
+    their 96 M chains into 2 segments).  The three calls give bit-identical
+    o and h_final, each returns the plan of its own
     shard count (the oracle's, field by field), and the result matches the
     oracle with a carried state that matters (g = 0, small beta, h0)."""
     import linear_attention_sequence_device_gb300 as g
