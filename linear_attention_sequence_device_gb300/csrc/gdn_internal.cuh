@@ -265,8 +265,9 @@ __device__ __forceinline__ bool make_job(const ChunkParams& p, int src, ChunkJob
         return true;
     }
     if (z >= nvt) return false;
-    // segment starts a sequence in this shard: initial state is known
-    const int n = upper_bound_minus1(p.cu, p.num_seqs, j.t0);
+    // segment starts a sequence in this shard: initial state is known; its
+    // global sequence from the plan's segment map (one load, no search)
+    const int n = __ldg(plan + cu_base + (int64_t)(P + r) * (p.num_seqs + 1) + i);
     j.col0 = z * p.col_tile;
     j.write_o = true;
     const int64_t st = ((int64_t)n * p.Hv + hv) * p.dk * p.dv + j.col0;

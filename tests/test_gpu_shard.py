@@ -418,3 +418,22 @@ def test_one_sequence_runs_on_finer_internal_shards():
     for r in range(1, 8):  # the first chunk after every internal boundary
         sl = slice(r * 2048, r * 2048 + 64)
         assert_close(f64(outs[0][0])[sl], o_ref[sl], w.dtype, f"o after {r * 2048}")
+
+
+def test_shard_fwd_with_empty_sequences():
+    """Empty sequences at the start, inside a shard, on a shard boundary and
+    at the end: every segment finds its global sequence (h0, h_final) in the
+    plan's segment map, empty sequences get h_final = h0, and the result is
+    the oracle's, sharded and not."""
+    w = W.Workload("empty_seqs", 4096, 16, 32, 128, 128, "bf16", 4, 11, (0, 700, 0, 324, 1024, 0, 0, 2048, 0),
+                   g_shift=-4.0, h0_std=0.5)
+    host, d = path_inputs(w)
+    o_ref, hf_ref = oracle_path(w, host)
+    for P in (4, 1):
+        o, hf, plan = run_gpu(w, d, P)
+        torch.cuda.synchronize()
+        assert int(plan[0]) == 0
+        assert_close(f64(o), o_ref, w.dtype, f"o P={P}")
+        assert_close(f64(hf), hf_ref, w.dtype, f"h_final P={P}")
+        for n in (0, 2, 5, 6, 8):  # the empty ones keep h0 exactly
+            assert torch.equal(hf[n], d["h0"][n])
