@@ -61,6 +61,10 @@ CASES = [
     ("packed_bf16_128", lambda: W.Workload("packed_small", 2048, 16, 32, 128, 128, "bf16", 1, 1,
                                            W.lengths_uniform(1, 2048, 64, 700)), 1),
     ("long_bf16_128_P8", lambda: W.long_seq(T=2048, h0_std=0.02), 8),
+    # one sequence on 2 shards: the call runs on 4 internal shards
+    ("long_bf16_128_P2_internal", lambda: W.long_seq(T=4096, h0_std=0.02), 2),
+    # 8 x 32 jobs a pass: the work queue splits every item, M halves included
+    ("million_bf16_128_P8_split", lambda: W.million(T=8000, n_shards=8), 8),
     ("ragged_bf16_128_P4", lambda: W.Workload("ragged_small", 2048, 4, 8, 128, 128, "bf16", 4, 3,
                                               W.lengths_geometric(3, 2048, 1.0 / 300.0, 1, 4096)), 4),
     ("bf16_64", lambda: W.Workload("small64", 700, 2, 4, 64, 64, "bf16", 1, 7, (300, 1, 399)), 1),

@@ -279,21 +279,28 @@ SPLIT_CASES = {
 
 
 @pytest.mark.parametrize("name", sorted(SPLIT_CASES))
-@pytest.mark.parametrize("final", [True, False])
-def test_split_tail_parts_are_bit_identical(name, final):
+@pytest.mark.parametrize("final,small_ws", [(True, False), (False, False), (True, True)])
+def test_split_tail_parts_are_bit_identical(name, final, small_ws):
     """The shard passes' work queue splits items into a first part and a
     short tail part when the launch has more jobs than SMs; the tail part
     starts from the first part's final state (fp32, stored and reloaded
     exactly).  So the outputs equal, bit for bit, those of the same call
-    with splitting turned off, and they match the oracle."""
+    with splitting turned off, and they match the oracle.  With the minimum
+    workspace the summaries' M halves run in the chunk kernel and are split
+    too: their tail parts continue from the first part's M instead of the
+    identity."""
     import linear_attention_sequence_device_gb300 as g
     w = SPLIT_CASES[name]()
     host, d = path_inputs(w)
     P = w.n_shards
+    ws = None
+    if small_ws:
+        ws = torch.empty(g.shard_fwd_workspace_min_size(w.T, w.N, P, w.Hk, w.Hv, w.dk, w.dv, torch.bfloat16),
+                         dtype=torch.uint8, device=dev())
 
     def call():
         return g.gdn_shard_fwd(d["x"], d["conv_w"], d["conv_b"], d["g"], d["beta"], d["cu"], w.Hk, w.Hv,
-                               w.dk, w.dv, P, h0=d["h0"], want_plan=True, h_final=final)
+                               w.dk, w.dv, P, h0=d["h0"], want_plan=True, h_final=final, workspace=ws)
 
     g.binding.device_timeouts(reset=True)
     try:
