@@ -623,7 +623,9 @@ static gdn_status shard_fwd_core(const void* x, const void* conv_w, const void* 
             p.wk_kt = mk + align256(tile);
             p.wk_eg = reinterpret_cast<float*>(mk + 2 * align256(tile));
         }
-        dim3 grid(num_seqs + P, Hv, (dv + dk) / p.col_tile);
+        // [N | M] column tiles; only the N tiles when the M chains run apart
+        // (no work-queue tickets for M jobs that would be skipped)
+        dim3 grid(num_seqs + P, Hv, (use_mk ? dv : dv + dk) / p.col_tile);
         if ((st = launch_chunk(p, dtype, JOBS_SHARD_PASS1, grid, s)) != GDN_OK) return st;
         p.sched = nullptr;
         if (use_mk) {  // the M halves of the summaries, from the operands the N halves stored
