@@ -63,6 +63,69 @@ struct MSmem {
     uint32_t tmem_slot;
 };
 
+// 32 lanes x 64 consecutive 32-bit columns in one tensor-memory access (one
+// wait for all 64 loads): the state read-back takes two of these per thread.
+__device__ __forceinline__ void ld64(uint32_t taddr, float* v) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63"
+        "}, [%64];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void st64(uint32_t taddr, const float* v) {
+    uint32_t u[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
+        "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+        "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64"
+        "};"
+        :
+        : "r"(taddr),
+          "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+          "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]),
+          "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]),
+          "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31]),
+          "r"(u[32]), "r"(u[33]), "r"(u[34]), "r"(u[35]), "r"(u[36]), "r"(u[37]), "r"(u[38]), "r"(u[39]),
+          "r"(u[40]), "r"(u[41]), "r"(u[42]), "r"(u[43]), "r"(u[44]), "r"(u[45]), "r"(u[46]), "r"(u[47]),
+          "r"(u[48]), "r"(u[49]), "r"(u[50]), "r"(u[51]), "r"(u[52]), "r"(u[53]), "r"(u[54]), "r"(u[55]),
+          "r"(u[56]), "r"(u[57]), "r"(u[58]), "r"(u[59]), "r"(u[60]), "r"(u[61]), "r"(u[62]), "r"(u[63])
+        : "memory");
+}
+__device__ __forceinline__ void stw32(uint32_t taddr, const uint32_t* w) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
+        "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32"
+        "};"
+        :
+        : "r"(taddr),
+          "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+          "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+          "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+          "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+        : "memory");
+}
+
 constexpr uint32_t ID_N64_NEG = tc::idesc_bf16(128, 64, false, false, false) | (1u << 14);
 constexpr uint32_t ID_N128_BMN = tc::idesc_bf16(128, 128, false, true, false);
 
@@ -168,14 +231,14 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
         }
         if (!(ok = wait_mma())) break;
         // v_new^T as bf16 pairs in place (the second product's A operand)
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            float vv[32];
-            uint32_t w[16];
-            tc::ld32(T_VN + 32 * h, vv);
+        {
+            float vv[64];
+            uint32_t w[32];
+            ld64(T_VN, vv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = tc::pack_bf16x2(vv[2 * j], vv[2 * j + 1]);
-            tc::stw16(T_VN + 32 * h, w);
+            for (int j = 0; j < 32; ++j) w[j] = tc::pack_bf16x2(vv[2 * j], vv[2 * j + 1]);
+            tc::stw16(T_VN, w);
+            tc::stw16(T_VN + 32, w + 16);
         }
         tc::wait_st();
         tc::fence_before();
@@ -195,19 +258,17 @@ __global__ void __launch_bounds__(MT) mchain_kernel(const MParams p, const __gri
             // chunk's e^{G_last}, back into tensor memory
             const float egn = __ldg(eg + c + 1);
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h)
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    float sv[16];
-                    uint32_t w[8];
-                    tc::ld16(T_S + 64 * h + 16 * q4, sv);
+            for (int h = 0; h < 2; ++h) {  // 64 columns at a time: one load wait each
+                float sv[64];
+                uint32_t w[32];
+                ld64(T_S + 64 * h, sv);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) w[j] = tc::pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
-                    tc::stw8(T_SB + 32 * h + 8 * q4, w);
+                for (int j = 0; j < 32; ++j) w[j] = tc::pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
+                stw32(T_SB + 32 * h, w);
 #pragma unroll
-                    for (int c2 = 0; c2 < 16; ++c2) sv[c2] *= egn;
-                    tc::st16(T_S + 64 * h + 16 * q4, sv);
-                }
+                for (int c2 = 0; c2 < 64; ++c2) sv[c2] *= egn;
+                st64(T_S + 64 * h, sv);
+            }
         } else {
             float* fin = G > 1 ? p.Mseg + (item * G + z) * 128 * 128 : p.M + item * 128 * 128;
 #pragma unroll 1
