@@ -209,3 +209,23 @@ def test_internal_shard_count_in_the_workspace(lib):
     assert small(131072, 2, 8, 16, 16, 128, 128, 1) == min_size(131072, 2, 8, 16, 16, 128, True)
     assert small(131072, 1, 8, 16, 16, 128, 128, 0) == min_size(131072, 1, 8, 16, 16, 128, False)
     assert small(1048576, 1, 64, 32, 32, 128, 128, 1) == min_size(1048576, 1, 64, 32, 32, 128, True)
+
+
+def test_m_chain_segments_in_the_workspace(lib):
+    """The M chains' segment count shows in the full workspace (G products of
+    64 KiB per (shard, head) when G > 1).  Two sequences on 4 shards of 64
+    chunks with 16 heads: 32 chains for 296 resident slots (148 SMs assumed
+    without a GPU) are cut into 4 segments of 16 chunks; one long sequence
+    (16 internal shards, 224 chains of 128 chunks) keeps whole chains, since
+    the merge would cost more than the cut saves."""
+    a256 = lambda x: (x + 255) // 256 * 256
+
+    def extra(T, N, P, Hv, P_run):
+        full = lib.gdn_shard_fwd_workspace_size(T, N, P, 16, Hv, 128, 128, 1)
+        small = lib.gdn_shard_fwd_workspace_min_size(T, N, P, 16, Hv, 128, 128, 1)
+        chunks = P_run * Hv * ((T // P_run + 63) // 64)
+        ops = 2 * a256(chunks * 64 * 128 * 2) + a256(chunks * 4)
+        return full - small - ops
+
+    assert extra(16384, 2, 4, 16, 4) == a256(4 * 4 * 16 * 65536)
+    assert extra(131072, 1, 8, 16, 16) == 0  # runs on 16 shards of 128 chunks
