@@ -229,3 +229,13 @@ def test_m_chain_segments_in_the_workspace(lib):
 
     assert extra(16384, 2, 4, 16, 4) == a256(4 * 4 * 16 * 65536)
     assert extra(131072, 1, 8, 16, 16) == 0  # runs on 16 shards of 128 chunks
+
+
+def test_testing_hooks_are_host_settings(lib):
+    """The testing hooks only set host-side launch settings (no device call):
+    the split switch takes any int, the hand-over bound rejects a negative
+    limit; the defaults are restored."""
+    assert lib.gdn_debug_set_split(0) == 0
+    assert lib.gdn_debug_set_split(1) == 0
+    assert lib.gdn_debug_set_handover(-1, 1) == 1          # GDN_ERR_INVALID_ARG
+    assert lib.gdn_debug_set_handover(1_000_000_000, 1) == 0
